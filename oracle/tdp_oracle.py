@@ -1,0 +1,340 @@
+"""CPU oracle for the tiled-latent overlap-add path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module:
+only the test-suite, the package smoke check and the benchmark's CPU-baseline
+leg may.  It shares no code with the CUDA library (no kernels, headers,
+tables or helpers); the two meet only through the seeded inputs that the
+tests feed to both.
+
+It is deliberately plain: NumPy slicing and float64 (the pages fix no
+precision for the windows), one tile at a time, no blocking or fusion.
+
+Method sources (the pages are documentation, not code):
+
+* "Tiled Data Parallelism (TDP)", LTX-2 multi-GPU docs,
+  §What it is -- tiles of the patchified (frames, height, width) latent,
+  overlapping regions blended with trapezoidal masks that sum to 1;
+  §Position normalization -- per-(batch, dim) minimum start of the
+  generated tokens is subtracted from every position, widths unchanged;
+  §Shared negative (reference) positions -- conditioning-token keep rule
+  and the 1/(number of tiles that kept it) weight;
+  §API -- TileCountConfig / DimensionTilingConfig(num_tiles, overlap):
+  counts per axis, overlap in latent grid units.
+* mold issue #673 (porting LTX-2's tiled stage 2), §A bug found while
+  porting -- split_by_count, the separable trapezoidal window, the measured
+  window-sum table for splits (21,2,8), (21,3,8), (21,4,8) and the guard
+  overlap <= dim/(n+1).
+* DistVAE docs "Choosing a tile window" -- decoded area, seams and per-rank
+  imbalance of a tile layout (used for plan statistics only).
+
+Readings taken where the pages are silent (each is listed in the design
+notes of the repository):
+
+* split_by_count: stride s = floor((dim - overlap) / n); tile i covers
+  [i*s, i*s + s + overlap); the last tile is stretched to end at dim.  This
+  is the one simple family that reproduces the mold window-sum table
+  exactly (1, 29/27, 94/81).
+* 1-D window of tile i over [a, e): product of a rising ramp
+  min(1, (x - a + 1)/(overlap + 1)) and a falling ramp
+  min(1, (e - x)/(overlap + 1)); the rising ramp is 1 for the first tile,
+  the falling ramp is 1 for the last tile (no ramp at the latent border).
+* Tiles are enumerated frames-major: t = (i_f * n_h + i_h) * n_w + i_w.
+* Generated token n of a (F, H, W) grid is n = (f*H + h)*W + w.
+* A conditioning interval [cs, ce) overlaps the tile's interval [TS, TE)
+  when cs < TE and ce > TS; [TS, TE) is the minimum start / maximum end of
+  the tile's generated tokens; "negative time coordinate" is start_t < 0.
+* 1/count is an IEEE float32 division; a token kept by no tile gets
+  count 0 and weight 0.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from fractions import Fraction
+from typing import List, Sequence, Tuple
+
+import numpy as np
+
+AXES = ("frames", "height", "width")
+
+
+class GuardError(ValueError):
+    """overlap * (n + 1) > dim: the windows no longer sum to 1."""
+
+
+# ---------------------------------------------------------------------------
+# Step 1: interval planning (mold issue #673 §A bug found while porting;
+# TDP docs §API for the count/overlap configuration).
+# ---------------------------------------------------------------------------
+def split_by_count(dim: int, num_tiles: int, overlap: int, compat: bool = False
+                   ) -> List[Tuple[int, int]]:
+    """Half-open intervals of `num_tiles` tiles over an axis of length `dim`.
+
+    Consecutive tiles share `overlap` units.  With `compat=False` the
+    partition-of-unity guard overlap <= dim/(n+1) (written overlap*(n+1) <=
+    dim) is enforced, as the mold port does; `compat=True` reproduces the
+    unguarded upstream behaviour whose excess the mold table measures.
+    """
+    if dim < 1 or num_tiles < 1 or overlap < 0:
+        raise ValueError("dim and num_tiles must be >= 1, overlap >= 0")
+    if num_tiles == 1:
+        if overlap != 0:
+            raise ValueError("a single tile cannot overlap anything")
+        return [(0, dim)]
+    stride = (dim - overlap) // num_tiles
+    if stride < 1:
+        raise ValueError("stride (dim - overlap) // num_tiles must be >= 1")
+    if not compat and overlap * (num_tiles + 1) > dim:
+        raise GuardError(f"overlap {overlap} > dim/(n+1) for dim {dim}, n {num_tiles}")
+    intervals = []
+    for i in range(num_tiles):
+        start = i * stride
+        end = start + stride + overlap
+        intervals.append((start, end))
+    intervals[-1] = (intervals[-1][0], dim)
+    return intervals
+
+
+def ramp_exact(intervals: Sequence[Tuple[int, int]], overlap: int, i: int, x: int) -> Fraction:
+    """1-D trapezoid weight of tile i at coordinate x, as an exact fraction."""
+    a, e = intervals[i]
+    if not (a <= x < e):
+        return Fraction(0)
+    n = len(intervals)
+    up = Fraction(1) if i == 0 else min(Fraction(1), Fraction(x - a + 1, overlap + 1))
+    down = Fraction(1) if i == n - 1 else min(Fraction(1), Fraction(e - x, overlap + 1))
+    return up * down
+
+
+def ramp_1d(intervals: Sequence[Tuple[int, int]], overlap: int, i: int) -> np.ndarray:
+    """float64 weights of tile i over its own local coordinates 0..size-1."""
+    a, e = intervals[i]
+    n = len(intervals)
+    x = np.arange(a, e, dtype=np.float64)
+    up = np.ones_like(x) if i == 0 else np.minimum(1.0, (x - a + 1.0) / (overlap + 1.0))
+    down = np.ones_like(x) if i == n - 1 else np.minimum(1.0, (e - x) / (overlap + 1.0))
+    return up * down
+
+
+@dataclass
+class Plan:
+    dims: Tuple[int, int, int]                 # (F, H, W)
+    counts: Tuple[int, int, int]               # tiles per axis
+    overlaps: Tuple[int, int, int]
+    intervals: Tuple[List[Tuple[int, int]], ...]  # per axis
+
+    @property
+    def num_tiles(self) -> int:
+        return self.counts[0] * self.counts[1] * self.counts[2]
+
+    def tile_index(self, t: int) -> Tuple[int, int, int]:
+        """(i_f, i_h, i_w) of tile t, frames-major order."""
+        i_w = t % self.counts[2]
+        i_h = (t // self.counts[2]) % self.counts[1]
+        i_f = t // (self.counts[2] * self.counts[1])
+        return i_f, i_h, i_w
+
+    def box(self, t: int) -> Tuple[Tuple[int, int], Tuple[int, int], Tuple[int, int]]:
+        i = self.tile_index(t)
+        return tuple(self.intervals[d][i[d]] for d in range(3))
+
+    def shape(self, t: int) -> Tuple[int, int, int]:
+        return tuple(e - s for (s, e) in self.box(t))
+
+
+def make_plan(dims: Sequence[int], cfg: Sequence[Tuple[int, int]], compat: bool = False) -> Plan:
+    """dims = (F, H, W); cfg = ((n_f, o_f), (n_h, o_h), (n_w, o_w)) as in
+    TileCountConfig(frames, height, width) of DimensionTilingConfig(num_tiles, overlap)."""
+    ivs = tuple(split_by_count(int(dims[d]), int(cfg[d][0]), int(cfg[d][1]), compat)
+                for d in range(3))
+    return Plan(tuple(int(v) for v in dims), tuple(int(c[0]) for c in cfg),
+                tuple(int(c[1]) for c in cfg), ivs)
+
+
+def tile_window(plan: Plan, t: int) -> np.ndarray:
+    """Separable trapezoid of tile t: outer product of the three 1-D ramps."""
+    i = plan.tile_index(t)
+    rf, rh, rw = (ramp_1d(plan.intervals[d], plan.overlaps[d], i[d]) for d in range(3))
+    return rf[:, None, None] * rh[None, :, None] * rw[None, None, :]
+
+
+# ---------------------------------------------------------------------------
+# Step 2: tile extract.  tiles[t][b, c, k, y, x] = X[b, c, f0+k, h0+y, w0+x].
+# ---------------------------------------------------------------------------
+def extract(plan: Plan, latent: np.ndarray) -> List[np.ndarray]:
+    assert latent.ndim == 5 and tuple(latent.shape[2:]) == plan.dims
+    out = []
+    for t in range(plan.num_tiles):
+        (f0, f1), (h0, h1), (w0, w1) = plan.box(t)
+        out.append(np.array(latent[:, :, f0:f1, h0:h1, w0:w1], copy=True))
+    return out
+
+
+def pack(tiles: Sequence[np.ndarray]) -> np.ndarray:
+    """Packed layout: tile after tile, each [B, C, f_t, h_t, w_t] row-major."""
+    return np.concatenate([np.ascontiguousarray(x).reshape(-1) for x in tiles])
+
+
+def unpack(plan: Plan, B: int, C: int, flat: np.ndarray) -> List[np.ndarray]:
+    out, pos = [], 0
+    for t in range(plan.num_tiles):
+        shp = (B, C) + plan.shape(t)
+        n = int(np.prod(shp))
+        out.append(flat[pos:pos + n].reshape(shp))
+        pos += n
+    assert pos == flat.size
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Step 5: window and overlap-add (TDP docs §What it is; mold §A bug found
+# while porting: blend has no normalisation pass).
+# ---------------------------------------------------------------------------
+def blend(plan: Plan, tiles: Sequence[np.ndarray]) -> np.ndarray:
+    """Y = sum_t w_t * tile_t, accumulated in float64."""
+    B, C = tiles[0].shape[:2]
+    acc = np.zeros((B, C) + plan.dims, dtype=np.float64)
+    for t in range(plan.num_tiles):
+        (f0, f1), (h0, h1), (w0, w1) = plan.box(t)
+        acc[:, :, f0:f1, h0:h1, w0:w1] += tile_window(plan, t)[None, None] * tiles[t].astype(np.float64)
+    return acc
+
+
+def blend_abs(plan: Plan, tiles: Sequence[np.ndarray]) -> np.ndarray:
+    """sum_t w_t * |tile_t|: the magnitude that rounding error scales with."""
+    return blend(plan, [np.abs(x.astype(np.float64)) for x in tiles])
+
+
+def window_sum(plan: Plan) -> np.ndarray:
+    """S(f, h, w) = sum over tiles covering the point of the 3-D window."""
+    S = np.zeros(plan.dims, dtype=np.float64)
+    for t in range(plan.num_tiles):
+        (f0, f1), (h0, h1), (w0, w1) = plan.box(t)
+        S[f0:f1, h0:h1, w0:w1] += tile_window(plan, t)
+    return S
+
+
+def window_sum_1d_exact(intervals: Sequence[Tuple[int, int]], overlap: int, dim: int) -> List[Fraction]:
+    return [sum((ramp_exact(intervals, overlap, i, x) for i in range(len(intervals))), Fraction(0))
+            for x in range(dim)]
+
+
+def max_abs_deviation(plan: Plan) -> float:
+    return float(np.max(np.abs(window_sum(plan) - 1.0)))
+
+
+# ---------------------------------------------------------------------------
+# Step 3: per-tile positions (TDP docs §Position normalization).
+# gen_pos[b, d, n, :] = [start, end) of generated token n on axis d.
+# ---------------------------------------------------------------------------
+def tile_token_indices(plan: Plan, t: int) -> np.ndarray:
+    """Global token indices n = (f*H + h)*W + w of tile t, in tile row-major order."""
+    F, H, W = plan.dims
+    (f0, f1), (h0, h1), (w0, w1) = plan.box(t)
+    f = np.arange(f0, f1)[:, None, None]
+    h = np.arange(h0, h1)[None, :, None]
+    w = np.arange(w0, w1)[None, None, :]
+    return ((f * H + h) * W + w).reshape(-1)
+
+
+def positions(plan: Plan, gen_pos: np.ndarray, normalize: bool = True
+              ) -> Tuple[List[np.ndarray], np.ndarray]:
+    """Per tile: its generated tokens' positions [B, 3, N_t, 2], shifted by the
+    per-(batch, dim) minimum start when `normalize`; and that minimum, [T, B, 3]."""
+    B = gen_pos.shape[0]
+    out, offsets = [], np.zeros((plan.num_tiles, B, 3), dtype=np.int64)
+    for t in range(plan.num_tiles):
+        p = gen_pos[:, :, tile_token_indices(plan, t), :].astype(np.int64)
+        off = p[..., 0].min(axis=2)                 # min start per (batch, dim)
+        offsets[t] = off
+        if normalize:
+            p = p - off[:, :, None, None]          # start and end move together
+        out.append(p)
+    return out, offsets
+
+
+# ---------------------------------------------------------------------------
+# Step 4: conditioning-token selection (TDP docs §Shared negative (reference)
+# positions).  cond_pos[b, d, m, :] = [start, end) of conditioning token m.
+# ---------------------------------------------------------------------------
+@dataclass
+class CondSelection:
+    extent: np.ndarray          # [T, B, 3, 2]  [min start, max end) of the tile's generated tokens
+    keep: np.ndarray            # [T, B, M] bool
+    count: np.ndarray           # [B, M] int
+    weight: np.ndarray          # [B, M] float32
+    kept: List[List[np.ndarray]]        # kept[t][b] = kept token indices, original order
+    tile_cond_pos: List[List[np.ndarray]]  # [t][b] -> [3, K, 2] positions of kept tokens
+
+
+def cond_select(plan: Plan, gen_pos: np.ndarray, cond_pos: np.ndarray, normalize: bool = True
+                ) -> CondSelection:
+    B, _, M, _ = cond_pos.shape
+    T = plan.num_tiles
+    cond = cond_pos.astype(np.int64)
+    extent = np.zeros((T, B, 3, 2), dtype=np.int64)
+    keep = np.zeros((T, B, M), dtype=bool)
+    for t in range(T):
+        p = gen_pos[:, :, tile_token_indices(plan, t), :].astype(np.int64)
+        TS = p[..., 0].min(axis=2)                  # [B, 3]
+        TE = p[..., 1].max(axis=2)
+        extent[t, :, :, 0], extent[t, :, :, 1] = TS, TE
+        overlaps = (cond[..., 0] < TE[:, :, None]) & (cond[..., 1] > TS[:, :, None])  # [B, 3, M]
+        negative_time = cond[:, 0, :, 0] < 0
+        keep[t] = overlaps.all(axis=1) | negative_time
+    count = keep.sum(axis=0).astype(np.int64)
+    weight = np.zeros((B, M), dtype=np.float32)
+    nz = count > 0
+    weight[nz] = np.float32(1.0) / count[nz].astype(np.float32)
+    kept, tcp = [], []
+    for t in range(T):
+        kept.append([np.nonzero(keep[t, b])[0] for b in range(B)])
+        rows = []
+        for b in range(B):
+            sel = cond[b][:, kept[t][b], :]         # [3, K, 2]
+            if normalize:
+                sel = sel - extent[t, b, :, 0][:, None, None]
+            rows.append(sel)
+        tcp.append(rows)
+    return CondSelection(extent, keep, count, weight, kept, tcp)
+
+
+# ---------------------------------------------------------------------------
+# Plan statistics (DistVAE "Choosing a tile window": decoded area, seams,
+# per-tile activations, heaviest-rank imbalance; TDP §What it is: tiles go to
+# ranks round-robin).
+# ---------------------------------------------------------------------------
+@dataclass
+class LayoutStats:
+    decoded_area: float         # sum of tile volumes / latent volume
+    seams: int                  # internal tile boundaries: sum_a (n_a - 1) * prod_{b != a} n_b
+    tile_fraction: float        # largest tile volume / latent volume
+    imbalance: float            # heaviest rank / even split - 1, round-robin assignment
+
+
+def layout_stats(axis_intervals: Sequence[Sequence[Tuple[int, int]]], dims: Sequence[int],
+                 ranks: int) -> LayoutStats:
+    """Statistics of any separable layout given by its per-axis intervals."""
+    sizes = [[e - s for (s, e) in iv] for iv in axis_intervals]
+    counts = [len(s) for s in sizes]
+    latent = float(np.prod(dims))
+    area = 1.0
+    for d in range(len(dims)):
+        area *= sum(sizes[d]) / dims[d]
+    seams = 0
+    for a in range(len(counts)):
+        others = 1
+        for b in range(len(counts)):
+            if b != a:
+                others *= counts[b]
+        seams += (counts[a] - 1) * others
+    vols = []
+    for idx in np.ndindex(*counts):              # frames-major / row-major tile order
+        v = 1
+        for d in range(len(dims)):
+            v *= sizes[d][idx[d]]
+        vols.append(v)
+    per_rank = [0] * ranks
+    for t, v in enumerate(vols):
+        per_rank[t % ranks] += v
+    even = sum(vols) / ranks
+    return LayoutStats(area, seams, max(vols) / latent, max(per_rank) / even - 1.0)
