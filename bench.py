@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Benchmark of the tiled-latent hot path on one GB300 (or N replicas).
+
+One step is one pass of every step of the path on the 4K-class workload
+(bf16 latent B=1, C=128, F=16, H=68, W=120; tiles 2x4x4 with overlaps
+2/8/12; 256 conditioning tokens, 64 with a negative time start):
+    tdp_extract -> tdp_positions -> tdp_cond_select -> tdp_blend -> tdp_window_sum
+(the per-tile op between extract and blend is the caller's; here identity,
+outside the path).  Inputs are resident in HBM when the timed region starts;
+L2 is flushed (a 256 MiB write) before every step.
+
+Headline: algorithmic extract+blend bytes per step / step time (GB/s):
+    latent read + tile write (extract) + tile read + latent write (blend).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tdp|reference]
+
+Under torchrun every rank runs its own replica (the tiles of the method are
+independent; there is no data-path collective) and rank 0 prints one JSON
+line with the max-over-ranks step time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from overlap_add_blending_gb300 import inputs  # noqa: E402
+from overlap_add_blending_gb300.workloads import WORKLOADS  # noqa: E402
+
+WORKLOAD = WORKLOADS["4k"]
+METRIC = "tile extract+blend HBM GB/s (fraction of GB300 peak) and latent elems/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNELS_PER_STEP = 6  # extract, positions, cond select (2), blend, window sum
+
+
+def esz(dtype: str) -> int:
+    return 2 if dtype == "bf16" else 4
+
+
+def algorithmic_bytes(wl, tiles_numel: int) -> dict:
+    lat = wl.B * wl.C * wl.dims[0] * wl.dims[1] * wl.dims[2]
+    e = esz(wl.dtype)
+    extract = lat * e + tiles_numel * e
+    blend = tiles_numel * e + lat * e
+    return {"latent_elems": lat, "tile_elems": tiles_numel, "extract": extract, "blend": blend,
+            "total": extract + blend, "overlap_factor": tiles_numel / lat}
+
+
+def config_dict(wl, note: str) -> dict:
+    return {"workload": f"4k-class latent {wl.dtype} B={wl.B} C={wl.C} F={wl.dims[0]} H={wl.dims[1]} "
+                        f"W={wl.dims[2]}, tiles (frames {wl.tiling[0][0]}/{wl.tiling[0][1]}, height "
+                        f"{wl.tiling[1][0]}/{wl.tiling[1][1]}, width {wl.tiling[2][0]}/{wl.tiling[2][1]}), "
+                        f"{wl.num_cond} conditioning tokens ({wl.num_cond_negative} with negative time)",
+            "step": "extract + positions + cond_select + blend + window_sum (per-tile op: identity, outside)",
+            "l2": note}
+
+
+def read_peak() -> tuple:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        for k in ("hbm_gbs", "hbm_GBps", "hbm"):
+            if k in d:
+                v = d[k]
+                if isinstance(v, dict):
+                    v = v.get("value", v.get("gbs"))
+                return float(v), "measured"
+    except (OSError, ValueError, TypeError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "overlap_add_blending_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cpp", ".h")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(name.encode() + b"\0" + fh.read())
+    with open(os.path.join(ROOT, "include", "tdp.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_4k.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    if d.get("source_digest") != source_digest():
+        return None
+    k = d.get("kernels", {}).get(kernel)
+    return None if k is None else k.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", gpu_index], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def oracle_step(wl, X, gen, cond, channels: int):
+    """One step of the CPU oracle on the first `channels` channels."""
+    from oracle import tdp_oracle as O
+    plan = O.make_plan(wl.dims, wl.tiling)
+    x = X[:, :channels]
+    tiles = O.extract(plan, x)
+    O.positions(plan, gen)
+    O.cond_select(plan, gen, cond)
+    y = O.blend(plan, tiles)
+    O.max_abs_deviation(plan)
+    return y
+
+
+def oracle_inputs(wl, channels: int):
+    import torch
+    Xf = inputs.latent((wl.B, wl.C) + wl.dims, seed=0)[:, :channels]
+    X = torch.from_numpy(np.ascontiguousarray(Xf)).to(torch.bfloat16).double().numpy()
+    gen = inputs.grid_positions(wl.B, *wl.dims)
+    cond = inputs.cond_positions(wl.B, wl.num_cond, *wl.dims, n_negative=wl.num_cond_negative, seed=2)
+    return X, gen, cond
+
+
+def sample_bytes(wl, channels: int) -> float:
+    frac = channels / wl.C
+    from oracle import tdp_oracle as O
+    plan = O.make_plan(wl.dims, wl.tiling)
+    tiles = sum(int(np.prod(plan.shape(t))) for t in range(plan.num_tiles)) * wl.B * wl.C
+    return algorithmic_bytes(wl, tiles)["total"] * frac
+
+
+def cpu_baseline(wl, budget_s: float = 10.0, channels: int = 16) -> dict:
+    X, gen, cond = oracle_inputs(wl, channels)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle_step(wl, X, gen, cond, channels)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": sample_bytes(wl, channels) * n / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} oracle steps (extract, positions, cond select, blend, window sum; float64 NumPy, "
+                      f"one thread) on {channels} of {wl.C} channels of the 4k-class workload, "
+                      f"{dt:.1f} s; bytes scaled to the sample"}
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return 0
+    wl = WORKLOAD
+    channels = 16
+    X, gen, cond = oracle_inputs(wl, channels)
+    for _ in range(args.warmup):
+        oracle_step(wl, X, gen, cond, channels)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(wl, X, gen, cond, channels)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = sample_bytes(wl, channels) / (ms * 1e-3) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(wl, "n/a (CPU)"),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: oracle extract, positions, cond select, blend and window sum "
+                                       f"on {channels} of {wl.C} channels (float64 NumPy, one thread); "
+                                       f"bytes scaled to the sample"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_tdp(args, rank: int, world: int):
+    import torch
+    import torch.distributed as dist
+    from overlap_add_blending_gb300 import tdp
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the tdp path has no CPU fallback)")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = WORKLOAD
+    dt = torch.bfloat16
+    p = tdp.plan(wl.dims, wl.tiling)
+    ab = algorithmic_bytes(wl, p.tiles_numel(wl.B, wl.C))
+
+    # resident inputs and outputs
+    X = torch.from_numpy(inputs.latent((wl.B, wl.C) + wl.dims, seed=0)).to(dt).to(dev)
+    gen_np = inputs.grid_positions(wl.B, *wl.dims)
+    cond_np = inputs.cond_positions(wl.B, wl.num_cond, *wl.dims, n_negative=wl.num_cond_negative, seed=2)
+    gen = torch.from_numpy(gen_np).to(dev)
+    cond = torch.from_numpy(cond_np).to(dev)
+    tiles = torch.empty(p.tiles_numel(wl.B, wl.C), dtype=dt, device=dev)
+    out = torch.empty_like(X)
+    tile_pos = torch.empty(6 * wl.B * p.tokens_numel(), dtype=torch.int32, device=dev)
+    offsets = torch.empty((p.T, wl.B, 3), dtype=torch.int32, device=dev)
+    cond_out = {}
+    maxdev = torch.empty(4, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def path():
+        tdp.extract(p, X, tiles)
+        tdp.positions(p, gen, True, tile_pos, offsets)
+        tdp.cond_select(p, gen, cond, True, True, cond_out)
+        tdp.blend(p, tiles, wl.B, wl.C, out)
+        tdp.window_sum(p, maxdev)
+
+    # events bracket each kernel of the step, on the launching stream
+    def timed_step(ev):
+        ev[0].record(stream)
+        tdp.extract(p, X, tiles)
+        ev[1].record(stream)
+        tdp.positions(p, gen, True, tile_pos, offsets)
+        ev[2].record(stream)
+        tdp.cond_select(p, gen, cond, True, True, cond_out)
+        ev[3].record(stream)
+        tdp.blend(p, tiles, wl.B, wl.C, out)
+        ev[4].record(stream)
+        tdp.window_sum(p, maxdev)
+        ev[5].record(stream)
+
+    # host enqueue time of one step, to size the head start given to the host
+    path()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(3):
+        path()
+    enqueue_s = (time.perf_counter() - t0) / 3
+    torch.cuda.synchronize()
+    sleep_cycles = int(max(200e-6, 3 * enqueue_s) * 2.0e9)
+
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    gpu_index = visible[local].strip() if len(visible) > local and visible[local].strip() else str(local)
+    sampler = ClockSampler(gpu_index)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        path()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    wall0 = time.perf_counter()
+    for k in range(K):
+        flush.zero_()
+        torch.cuda._sleep(sleep_cycles)      # the host enqueues the whole step meanwhile
+        timed_step(evs[k])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+
+    seg = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(5)] for k in range(K)])  # ms
+    step_ms = float(seg.sum(axis=1).mean())
+    per_kernel_ms = seg.mean(axis=0)
+    names = ["extract", "positions", "cond_select", "blend", "window_sum"]
+
+    # e2e: host buffers in, blended latent out, through the same C-ABI calls
+    X_h = X.cpu().pin_memory()
+    gen_h = gen.cpu().pin_memory()
+    cond_h = cond.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=dt, pin_memory=True)
+    dev_h = torch.empty(1, dtype=torch.float32, pin_memory=True)
+    h2d = X_h.numel() * X_h.element_size() + gen_h.numel() * 4 + cond_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size() + 4
+    e2e_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for k in range(-min(3, args.warmup), K):
+        flush.zero_()
+        torch.cuda._sleep(sleep_cycles)
+        if k >= 0:
+            e2e_evs[k][0].record(stream)
+        X.copy_(X_h, non_blocking=True)
+        gen.copy_(gen_h, non_blocking=True)
+        cond.copy_(cond_h, non_blocking=True)
+        path()
+        out_h.copy_(out, non_blocking=True)
+        dev_h.copy_(maxdev[:1], non_blocking=True)
+        if k >= 0:
+            e2e_evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in e2e_evs]))
+
+    if world > 1:
+        t = torch.tensor([step_ms, e2e_ms] + list(per_kernel_ms), dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, e2e_ms = float(t[0]), float(t[1])
+        per_kernel_ms = t[2:].cpu().numpy()
+
+    if rank != 0:
+        return 0
+    peak, peak_src = read_peak()
+    kern = {n: {"ms": float(per_kernel_ms[i])} for i, n in enumerate(names)}
+    kern["extract"]["gbs"] = ab["extract"] / (kern["extract"]["ms"] * 1e-3) / 1e9
+    kern["blend"]["gbs"] = ab["blend"] / (kern["blend"]["ms"] * 1e-3) / 1e9
+    dom = "blend" if kern["blend"]["ms"] >= kern["extract"]["ms"] else "extract"
+    achieved = kern[dom]["gbs"]
+    traffic = recorded_traffic(dom)
+    value = world * ab["total"] / (step_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(wl, "flushed before every step (256 MiB write, outside the events)"),
+        "latent_elems_per_s": world * ab["latent_elems"] / (step_ms * 1e-3),
+        "extract_blend_gbs": ab["total"] / ((kern["extract"]["ms"] + kern["blend"]["ms"]) * 1e-3) / 1e9,
+        "algorithmic_bytes": {"extract": ab["extract"], "blend": ab["blend"],
+                              "overlap_factor": round(ab["overlap_factor"], 5)},
+        "kernels": kern,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src},
+        "e2e": {"value": world * ab["total"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+        "gpu_launches": KERNELS_PER_STEP * K,
+        "clocks": clocks,
+        "timed_wall_s": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["tdp", "reference"], default="tdp")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)     # rank 0 alone times the oracle
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group(backend=backend)
+    try:
+        return run_tdp(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,260 @@
+/*
+ * tdp.h -- C ABI of the tiled-latent extract / trapezoid overlap-add path
+ * (libtdp.so, CUDA for sm_103a).
+ *
+ * The method is LTX-2's Tiled Data Parallelism ("Tiled Data Parallelism
+ * (TDP)", LTX-2 multi-GPU docs, section "What it is"): the patchified
+ * (frames, height, width) latent is split into overlapping tiles by count
+ * per axis, each tile is processed on its own, and the per-tile results are
+ * recombined with separable trapezoidal masks that sum to 1.  The interval
+ * split and the window are the ones that the mold issue #673 ("A bug found
+ * while porting") measures for upstream's split_by_count / blend.
+ *
+ * Conventions shared by every call
+ *   - Latent X is [B, C, F, H, W], contiguous, W fastest.
+ *   - Tiles are numbered frames-major: t = (i_f * n_h + i_h) * n_w + i_w.
+ *   - Packed tiles: tile after tile, each [B, C, f_t, h_t, w_t] contiguous;
+ *     tile t starts at element tdp_tile_offset(plan, t, B, C).  Tile shapes
+ *     may differ (the last tile of an axis absorbs the remainder).
+ *   - Generated token n of the latent grid is n = (f * H + h) * W + w;
+ *     positions are int32 [start, end) pairs, layout [B, 3, N, 2] with
+ *     axis 0 = time (frames), 1 = height, 2 = width.
+ *   - Device pointers are owned by the caller.  The library allocates no
+ *     device memory, never synchronises the stream and keeps no state
+ *     between calls apart from one diagnostic word (tdp_device_error).
+ *     Every device pointer must be 16-byte aligned (else
+ *     TDP_ERR_ALIGNMENT); buffers must not overlap unless stated.
+ *   - Every call validates its arguments on the host (including that the
+ *     plan is exactly what tdp_plan returns for its own dims, counts,
+ *     overlaps and flags) and returns before any launch when they are
+ *     wrong.  Kernels never trap.  A failed launch or runtime call returns
+ *     TDP_ERR_CUDA; tdp_last_cuda_error gives its cudaError_t code.
+ *   - B or C (or M) equal to 0 is an empty batch: the call validates the
+ *     plan and returns TDP_OK without launching.
+ */
+#ifndef TDP_H_
+#define TDP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TDP_MAX_PER_AXIS 64          /* tiles per axis */
+#define TDP_PLAN_UPSTREAM_COMPAT 1u  /* accept overlap*(n+1) > dim (windows then sum above 1) */
+
+/* DimensionTilingConfig(num_tiles, overlap): a tile COUNT and an overlap in
+ * latent grid units ("Tiled Data Parallelism (TDP)", section API, Tiling
+ * config).  The page's default is {1, 0}. */
+typedef struct {
+    int32_t num_tiles;
+    int32_t overlap;
+} tdp_dim_cfg;
+
+/* TileCountConfig(frames, height, width): counts, not sizes (same section). */
+typedef struct {
+    tdp_dim_cfg frames;
+    tdp_dim_cfg height;
+    tdp_dim_cfg width;
+} tdp_tile_count_cfg;
+
+typedef enum {
+    TDP_OK = 0,
+    TDP_ERR_INVALID_ARG = 1,     /* bad size, count, pointer or dtype */
+    TDP_ERR_GUARD = 2,           /* overlap*(n+1) > dim without TDP_PLAN_UPSTREAM_COMPAT */
+    TDP_ERR_TOO_MANY_TILES = 3,  /* num_tiles > TDP_MAX_PER_AXIS */
+    TDP_ERR_ALIGNMENT = 4,       /* a device pointer is not 16-byte aligned */
+    TDP_ERR_CUDA = 5,            /* a CUDA launch or runtime call failed */
+    TDP_ERR_UNSUPPORTED = 6      /* a tile row is too long for shared-memory staging */
+} tdp_status;
+
+typedef enum { TDP_F32 = 0, TDP_BF16 = 1 } tdp_dtype;
+
+/* Host-side plan.  Plain data: filled by tdp_plan, read by every other call
+ * (it is copied by value into the kernels, so it may be reused or freed as
+ * soon as a call returns). */
+typedef struct {
+    int32_t dims[3];                               /* F, H, W */
+    int32_t num_tiles[3];                          /* n per axis */
+    int32_t overlap[3];                            /* overlap per axis */
+    int32_t stride[3];                             /* floor((dim - overlap) / n) */
+    int32_t start[3][TDP_MAX_PER_AXIS];            /* tile i covers [start, end) */
+    int32_t end[3][TDP_MAX_PER_AXIS];
+    int32_t prefix[3][TDP_MAX_PER_AXIS + 1];       /* sum of sizes of tiles < i */
+    int32_t max_cover[3];                          /* most tiles covering one index */
+    int32_t total_tiles;                           /* T = n_f * n_h * n_w */
+    uint32_t flags;
+} tdp_plan_t;
+
+/*
+ * tdp_plan -- step 1, interval planning per axis.
+ *
+ * Source: the mold issue #673 ("A bug found while porting") describes
+ * split_by_count and the guard overlap <= dim/(n+1) that keeps the windows
+ * a partition of unity; "Tiled Data Parallelism (TDP)" (API) gives the
+ * count/overlap configuration.  The split formula is not printed on the
+ * pages; the one used here -- stride s = floor((dim - overlap)/n), tile i =
+ * [i*s, i*s + s + overlap), last tile stretched to end at dim -- is the
+ * simple split that reproduces the mold issue's measured window sums.
+ *
+ * dims_fhw: host array {F, H, W}, each >= 1.
+ * cfg:      host pointer; per axis num_tiles in [1, TDP_MAX_PER_AXIS],
+ *           overlap >= 0, overlap == 0 when num_tiles == 1, stride >= 1.
+ * flags:    0 (guard enforced) or TDP_PLAN_UPSTREAM_COMPAT.
+ * out:      host pointer, written only on TDP_OK.
+ * Errors: TDP_ERR_INVALID_ARG, TDP_ERR_TOO_MANY_TILES, TDP_ERR_GUARD.
+ * Host only; touches no GPU.
+ */
+tdp_status tdp_plan(const int32_t dims_fhw[3], const tdp_tile_count_cfg* cfg, uint32_t flags,
+                    tdp_plan_t* out);
+
+/* Element offset of tile t in the packed tile buffer, and the total number
+ * of packed elements (sum over tiles of B*C*f_t*h_t*w_t).  Host only;
+ * return -1 on a bad argument. */
+int64_t tdp_tile_offset(const tdp_plan_t* plan, int32_t t, int32_t B, int32_t C);
+int64_t tdp_tiles_numel(const tdp_plan_t* plan, int32_t B, int32_t C);
+
+/* Start and size of tile t per axis (host arrays of 3). */
+tdp_status tdp_tile_box(const tdp_plan_t* plan, int32_t t, int32_t start[3], int32_t size[3]);
+
+/*
+ * tdp_plan_stats -- layout statistics of a plan (host only).
+ *
+ * Source: DistVAE docs "Choosing a tile window" (decoded area, seams,
+ * per-tile activations, heaviest-rank imbalance) and "Tiled Data
+ * Parallelism (TDP)" (tiles assigned to ranks round-robin, t mod ranks).
+ *   decoded_area   = prod_d (sum of tile sizes on d) / dim_d
+ *   seams          = sum_a (n_a - 1) * prod_{b != a} n_b
+ *   tile_fraction  = largest tile volume / latent volume
+ *   imbalance      = heaviest rank's volume / (total / ranks) - 1
+ *   max_window_sum = max over the grid of sum_t w_t (exact rational
+ *                    arithmetic, rounded once to double)
+ * Any output pointer may be NULL.  ranks >= 1.
+ */
+tdp_status tdp_plan_stats(const tdp_plan_t* plan, int32_t ranks, double* decoded_area,
+                          int32_t* seams, double* tile_fraction, double* imbalance,
+                          double* max_window_sum);
+
+/*
+ * tdp_extract -- step 2, tile extract (K1).
+ *
+ * Source: "Tiled Data Parallelism (TDP)", What it is (each tile is the
+ * latent's sub-box); mold issue #673, Scope (per-tile latent slice).
+ *   tiles[t][b, c, k, y, x] = latent[b, c, f0_t + k, h0_t + y, w0_t + x]
+ * latent: device, [B, C, F, H, W] of `dtype`.
+ * tiles:  device, packed (tdp_tiles_numel elements of `dtype`).
+ * Bit-exact copy.  Asynchronous on `stream`.
+ */
+tdp_status tdp_extract(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype dtype,
+                       const void* latent, void* tiles, cudaStream_t stream);
+
+/*
+ * tdp_positions -- step 3, per-tile position grids (K4).
+ *
+ * Source: "Tiled Data Parallelism (TDP)", Position normalization: the
+ * tile's positions are shifted by the minimum start of its generated
+ * tokens, per (batch, axis), so they start at zero; interval widths are
+ * unchanged.
+ * gen_pos:   device int32 [B, 3, N, 2], N = F*H*W.
+ * normalize: nonzero -> subtract the offset from start and end.
+ * tile_pos:  device int32, packed [T][B, 3, N_t, 2], N_t = f_t*h_t*w_t,
+ *            tokens in tile row-major order; tile t starts at element
+ *            6 * B * (sum of N_t' for t' < t).
+ * offsets:   device int32 [T, B, 3], min start of tile t's generated tokens
+ *            (written whether or not `normalize` is set).
+ * Bit-exact.  Asynchronous on `stream`.
+ */
+tdp_status tdp_positions(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos,
+                         int32_t normalize, int32_t* tile_pos, int32_t* offsets,
+                         cudaStream_t stream);
+
+/*
+ * tdp_cond_select -- step 4, conditioning-token selection (K5).
+ *
+ * Source: "Tiled Data Parallelism (TDP)", Shared negative (reference)
+ * positions: a tile keeps a conditioning token whose [start, end) overlaps
+ * the tile in all three axes, or whose time start is negative; a token
+ * kept by k tiles has blend weight 1/k.  Kept tokens go after the tile's
+ * generated tokens, so they are shifted by the same offset (Position
+ * normalization).
+ *   extent[t,b,d] = [TS, TE): min start / max end of tile t's generated
+ *                   tokens on axis d (before any shift).
+ *   keep[t,b,m]   = cond_t_start < 0  or  for all d: cs_d < TE_d and ce_d > TS_d
+ *   count[b,m]    = sum_t keep[t,b,m];  weight = count ? 1.0f/count : 0 (IEEE fp32)
+ * gen_pos:       device int32 [B, 3, N, 2].
+ * cond_pos:      device int32 [B, 3, M, 2] (M >= 0).
+ * normalize:     nonzero -> tile_cond_pos is shifted by TS.
+ * tile_extent:   device int32 [T, B, 3, 2] (required).
+ * keep:          device uint8 [T, B, M] (required, 0/1).
+ * count:         device int32 [B, M] (required).
+ * weight:        device float [B, M] (required).
+ * kept_idx:      device int32 [T, B, M] or NULL: indices of kept tokens in
+ *                their original order, -1 after the last one.
+ * num_kept:      device int32 [T, B] or NULL.
+ * tile_cond_pos: device int32 [T, B, 3, M, 2] or NULL: positions of the
+ *                kept tokens in kept order, zero after the last one.
+ * Bit-exact.  Asynchronous on `stream`.
+ */
+tdp_status tdp_cond_select(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos,
+                           int32_t M, const int32_t* cond_pos, int32_t normalize,
+                           int32_t* tile_extent, uint8_t* keep, int32_t* count, float* weight,
+                           int32_t* kept_idx, int32_t* num_kept, int32_t* tile_cond_pos,
+                           cudaStream_t stream);
+
+/*
+ * tdp_blend -- step 5, fused separable trapezoid window + overlap-add (K2).
+ *
+ * Source: "Tiled Data Parallelism (TDP)", What it is (overlapping regions
+ * blended with trapezoidal masks that sum to 1); mold issue #673 (a
+ * separable trapezoidal window; blend has no normalisation pass).
+ *   out[b,c,f,h,w] = sum over tiles t covering (f,h,w) of
+ *                    r_f(f) * r_h(h) * r_w(w) * tiles[t][b,c,f-f0,h-h0,w-w0]
+ * with, on each axis for tile i of n over [a, e) and overlap o,
+ *   r(x) = up * down,  up = (i > 0) ? min(1, (x-a+1)/(o+1)) : 1,
+ *                      down = (i < n-1) ? min(1, (e-x)/(o+1)) : 1.
+ * The weights are formed in fp32 registers, the sum is accumulated in fp32
+ * and written once in `out_dtype` (round to nearest even for bf16); there
+ * is no zero-fill pass and no atomics.  Every element of `out` is written.
+ * tiles: device, packed, `in_dtype`.  out: device [B, C, F, H, W].
+ * Asynchronous on `stream`.
+ */
+tdp_status tdp_blend(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_dtype,
+                     const void* tiles, tdp_dtype out_dtype, void* out, cudaStream_t stream);
+
+/*
+ * tdp_window_sum -- window-sum check (K3).
+ *
+ * Source: "Tiled Data Parallelism (TDP)", What it is (masks sum to 1
+ * globally) and mold issue #673 (the sum exceeds 1 when the guard is
+ * violated: up to 1.074 for (21,3,8), 1.161 for (21,4,8)).
+ *   S(f,h,w) = sum_t r_f * r_h * r_w (fp32, the weights tdp_blend applies)
+ * max_abs_dev: device float, receives max |S - 1| (required).
+ * sum_out:     device float [F, H, W] or NULL, receives S.
+ * Asynchronous on `stream`.
+ */
+tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum_out,
+                          cudaStream_t stream);
+
+/* Diagnostic word of the current device: nonzero when a kernel gave up
+ * waiting for its staged copies (bounded wait) and skipped its work.
+ * Reads it synchronously into *code and, when `clear` is nonzero, resets
+ * it.  Returns TDP_ERR_CUDA if the read fails. */
+tdp_status tdp_device_error(uint32_t* code, int32_t clear);
+
+const char* tdp_status_str(tdp_status status);
+
+/* cudaError_t code of the most recent TDP_ERR_CUDA on the calling thread
+ * (0 if none). */
+int32_t tdp_last_cuda_error(void);
+
+/* sizeof(tdp_plan_t), so that bindings can check their mirror of it. */
+size_t tdp_plan_struct_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TDP_H_ */
