@@ -131,7 +131,7 @@ __device__ __forceinline__ float axis_weight(const tdp_plan_t& p, int d, int i, 
     float up = 1.0f, dn = 1.0f;
     if (i > 0) up = fminf(1.0f, static_cast<float>(x - p.start[d][i] + 1) / o1);
     if (i < p.num_tiles[d] - 1) dn = fminf(1.0f, static_cast<float>(p.end[d][i] - x) / o1);
-    return up * dn;
+    return __fmul_rn(up, dn);
 }
 
 // ------------------------------------------------------------------ block / warp scans
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(kThreads) blend_kernel(const __grid_constant__
             const float wf = fcov[fa].w;
             for (int k = 0; k < hc; ++k) {
                 const Cov hk = hcov[r * a.kh + k];
-                const float wfh = wf * hk.w;
+                const float wfh = __fmul_rn(wf, hk.w);
                 const int sbase = (fa * NH + (hk.i - ih_lo)) * nw;
 #pragma unroll
                 for (int v = 0; v < U; ++v) {
@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(kThreads) blend_kernel(const __grid_constant__
                         const Cov wq = wcov[col * a.kw + q];
                         const int2 wt = wtile[wq.i];
                         const int idx = slotbase[sbase + wq.i] + h * wt.y + (col - wt.x);
-                        acc[v] = fmaf(wfh * wq.w, load_f(sdata, idx), acc[v]);
+                        acc[v] = fmaf(__fmul_rn(wfh, wq.w), load_f(sdata, idx), acc[v]);
                     }
                 }
             }
@@ -512,13 +512,14 @@ __global__ void __launch_bounds__(kThreads) window_sum_kernel(const __grid_const
         tdp::axis_cover(p, 0, f, f0, f1);
         tdp::axis_cover(p, 1, h, h0, h1);
         tdp::axis_cover(p, 2, w, w0, w1);
-        // Same weights, products and summation order as the blend kernel.
+        // Same weights, products and summation order as the blend kernel
+        // (products rounded on their own: never contracted into the sum).
         float S = 0.0f;
         for (int i = f0; i <= f1; ++i) {
             const float wf = axis_weight(p, 0, i, f);
             for (int j = h0; j <= h1; ++j) {
-                const float wfh = wf * axis_weight(p, 1, j, h);
-                for (int k = w0; k <= w1; ++k) S = fmaf(wfh * axis_weight(p, 2, k, w), 1.0f, S);
+                const float wfh = __fmul_rn(wf, axis_weight(p, 1, j, h));
+                for (int k = w0; k <= w1; ++k) S = __fadd_rn(S, __fmul_rn(wfh, axis_weight(p, 2, k, w)));
             }
         }
         if (sum_out) sum_out[idx] = S;
