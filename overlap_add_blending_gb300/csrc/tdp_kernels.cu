@@ -40,10 +40,11 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kCluster = 8;                  // CTAs cooperating on one tile's token reduction
 constexpr uint64_t kWaitNs = 200ull * 1000 * 1000;  // give up on staged copies after 200 ms
+constexpr uint32_t kSuspendHintNs = 20000;           // a polling thread sleeps up to 20 us per try
 constexpr uint32_t kErrExtractWait = 1u;
 constexpr uint32_t kErrBlendWait = 2u;
-constexpr int kExtractSmemBudget = 48 * 1024;
-constexpr int kBlendSmemBudget = 48 * 1024;
+constexpr int kExtractSmemBudget = 64 * 1024;   // two staged bands + slot table
+constexpr int kBlendSmemBudget = 72 * 1024;     // two stages of tile rows + tables
 
 __device__ unsigned int g_device_error = 0;
 
@@ -77,10 +78,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -91,28 +92,34 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Poll phase 0 of `bar` until it completes or kWaitNs of wall time pass.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar) {
+// Poll phase `parity` of `bar` until it completes or kWaitNs of wall time pass.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = global_ns();
     for (;;) {
-        if (mbar_try_wait(bar, 0)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (global_ns() - t0 > kWaitNs) return false;
     }
 }
 
-// Bounded wait for the CTA's staged copies.  Returns true (uniformly over
-// the CTA) when they have landed.  On a timeout the CTA records `code` in
-// the diagnostic word, waits once more (bounded) so that no copy is still
-// writing into its shared memory, and the caller returns without working.
-__device__ bool mbar_wait_or_flag(uint64_t* bar, uint32_t code) {
-    bool ok = mbar_wait_bounded(bar);
-    const bool any_fail = __syncthreads_or(!ok);
-    if (any_fail) {
-        if (threadIdx.x == 0) atomicOr(&g_device_error, code);
-        if (!ok) mbar_wait_bounded(bar);
-        return false;
-    }
-    return true;
+// CTA-wide wait for a staged phase: thread 0 polls while the other warps sit
+// in the hardware barrier (they take no issue slots).  The barrier also
+// publishes everything the CTA wrote to shared memory before it.  Returns
+// false, uniformly, if the copies did not land within kWaitNs.
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity) {
+    bool ok = true;
+    if (threadIdx.x == 0) ok = mbar_wait_bounded(bar, parity);
+    return !__syncthreads_or(!ok);
+}
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// The plan is a __grid_constant__ kernel parameter; indexed reads of it with
+// a different index in each lane are serialised by the constant cache, so
+// every kernel first copies it into shared memory and reads that copy.
+__device__ __forceinline__ void load_plan(tdp_plan_t* dst, const tdp_plan_t& src) {
+    const int* from = reinterpret_cast<const int*>(&src);
+    int* to = reinterpret_cast<int*>(dst);
+    for (int i = threadIdx.x; i < static_cast<int>(sizeof(tdp_plan_t) / 4); i += blockDim.x) to[i] = from[i];
 }
 
 // ------------------------------------------------------------------ element helpers
@@ -164,126 +171,244 @@ __device__ int block_excl_scan(int v, int* sh, int* total) {
     return r;
 }
 
+// =================================================================== staging
+// A contiguous span [g0, g1) of a global buffer staged into shared memory:
+// one bulk copy of the 16-byte chunks it touches, except that a chunk
+// reaching past the buffer's last full 16 bytes (`limit`) is not copied in
+// bulk -- those last elements are loaded one by one.  The shared region
+// needs round_up(span bytes, 16) + 16 bytes.
+struct SpanCopy {
+    uintptr_t lo;    // first byte copied in bulk (16-byte aligned)
+    uint32_t bulk;   // bytes copied in bulk (multiple of 16, may be 0)
+    int shift;       // elements between the region start and g0
+    int tail0;       // first span element not covered by the bulk copy
+};
+
+template <typename E>
+__device__ __forceinline__ SpanCopy plan_span(const E* base, long long first, int len, uintptr_t limit) {
+    const uintptr_t g0 = reinterpret_cast<uintptr_t>(base + first);
+    const uintptr_t g1 = reinterpret_cast<uintptr_t>(base + first + len);
+    SpanCopy c;
+    c.lo = g0 & ~uintptr_t(15);
+    uintptr_t hi = (g1 + 15) & ~uintptr_t(15);
+    if (hi > limit) hi = g1 & ~uintptr_t(15);
+    c.bulk = hi > c.lo ? static_cast<uint32_t>(hi - c.lo) : 0u;
+    c.shift = static_cast<int>((g0 - c.lo) / sizeof(E));
+    c.tail0 = hi >= g1 ? len : (hi > g0 ? static_cast<int>((hi - g0) / sizeof(E)) : 0);
+    return c;
+}
+
+// =================================================================== work split
+// Items are numbered (frame, band) major, then b * C + c, and every CTA of a
+// persistent kernel takes one contiguous range of them: consecutive items
+// share their frame and band, so the geometry built for one serves the
+// next, and ranges differ in length by at most one item.
+__device__ __forceinline__ void cta_item_range(int n_items, int& first, int& last) {
+    first = static_cast<int>(((long long)blockIdx.x * n_items) / gridDim.x);
+    last = static_cast<int>(((long long)(blockIdx.x + 1) * n_items) / gridDim.x);
+}
+
+struct FrameBand {
+    int f, hb0, hb1;
+};
+
+__device__ __forceinline__ FrameBand frame_band(const tdp_plan_t& p, int fb, int band_rows, int nbands) {
+    FrameBand x;
+    x.f = fb / nbands;
+    x.hb0 = (fb - x.f * nbands) * band_rows;
+    x.hb1 = min(p.dims[1], x.hb0 + band_rows);
+    return x;
+}
+
+// Walks (fb, bc) = divmod(item, BC) without dividing per step.
+struct ItemCursor {
+    int fb, bc, BC;
+    __device__ __forceinline__ void init(int item, int BC_) {
+        BC = BC_;
+        fb = item / BC;
+        bc = item - fb * BC;
+    }
+    __device__ __forceinline__ void next() {
+        if (++bc == BC) { bc = 0; ++fb; }
+    }
+};
+
 // =================================================================== K1: extract
 struct ExtractSlot {
-    long long dst;  // element index of the span in the packed tiles
-    int src;        // shared-memory element index of (first row, column 0) of the tile
-    int rows;       // tile rows inside the band
-    int sw;         // tile width
-    int pad;
+    long long dst0;  // packed-tile element index of the slot's first element for b*C + c = 0
+    long long vol;   // elements per (b, c) of the slot's tile: dst = dst0 + (b*C + c) * vol
+    int src;         // band element index of (first row, column 0), before the staging shift
+    int rows;        // tile rows inside the band
+    int sw;          // tile width
+    float inv_sw;    // 1 / sw, for the lanes' start (exact for the small numerators used)
 };
 
 struct ExtractArgs {
     const void* latent;
     void* tiles;
+    long long latent_numel;
     int BC;          // B * C
     int band_rows;
     int nbands;
-    int data_off;    // byte offset of the staged band in shared memory
+    int n_items;     // F * nbands * B * C
+    int off_slots;   // byte offsets in shared memory
+    int off_data;    // stage s starts at off_data + s * stage_bytes
+    int stage_bytes;
 };
 
+// floor(e / sw) for 0 <= e < 4096 via the rounded reciprocal: (e + 1/2) / sw
+// is at least 1/(2 sw) away from an integer, far more than the error.
+__device__ __forceinline__ int small_div(int e, float inv_sw) {
+    return __float2int_rz((static_cast<float>(e) + 0.5f) * inv_sw);
+}
+
+// One warp copies one slot: the slot's rows (sw elements each, W apart in
+// the staged band) are written back to back into the packed tile.  Lanes
+// walk the output in steps of 64 elements (32 lanes x 2) for 2-byte types,
+// 32 elements for 4-byte types, tracking the source index incrementally.
 template <typename E>
-__device__ __forceinline__ void extract_copy_slot(const ExtractSlot& sl, const E* __restrict__ band,
-                                                  E* __restrict__ tiles, int W) {
-    const int len = sl.rows * sl.sw;
-    E* dst = tiles + sl.dst;
+__device__ __forceinline__ void extract_copy_slot_warp(E* __restrict__ dst, const E* __restrict__ src,
+                                                       const ExtractSlot& e, int W, int lane) {
+    const int sw = e.sw;
+    const int len = e.rows * sw;
+    const int wrap = W - sw;
     if constexpr (sizeof(E) == 2) {
-        // Element pairs -> 32-bit stores; an odd span start leaves one head element.
-        const int head = static_cast<int>(sl.dst & 1);
-        const int npairs = (len - head) >> 1;
-        if (threadIdx.x == 0 && head && len > 0) dst[0] = band[sl.src];
-        if (threadIdx.x == blockDim.x - 1 && ((len - head) & 1)) {
-            const int e = len - 1, row = e / sl.sw, x = e - row * sl.sw;
-            dst[e] = band[sl.src + row * W + x];
+        const int head = static_cast<int>((reinterpret_cast<uintptr_t>(dst) >> 1) & 1);  // odd start
+        const int body = len - head;
+        const int npairs = body >> 1;
+        if (lane == 0 && head) dst[0] = src[0];
+        if (lane == 31 && (body & 1)) {
+            const int last = len - 1, row = last / sw;
+            dst[last] = src[row * W + (last - row * sw)];
         }
-        int e0 = head + 2 * static_cast<int>(threadIdx.x);
-        int row = e0 / sl.sw, x = e0 - row * sl.sw;
-        const int step = 2 * static_cast<int>(blockDim.x);
-        const int dq = step / sl.sw, dr = step - dq * sl.sw;
-        uint32_t* dst32 = reinterpret_cast<uint32_t*>(dst + head);
-        for (int j = threadIdx.x; j < npairs; j += blockDim.x) {
-            const uint32_t lo = band[sl.src + row * W + x];
-            int x1 = x + 1, row1 = row;
-            if (x1 == sl.sw) { x1 = 0; ++row1; }
-            const uint32_t hi = band[sl.src + row1 * W + x1];
-            dst32[j] = lo | (hi << 16);
+        const int e0 = head + 2 * lane;
+        const int r0 = small_div(e0, e.inv_sw);
+        int x = e0 - r0 * sw;
+        int a = r0 * W + x;                          // source index of the pair's first element
+        const int dq = small_div(64, e.inv_sw), dr = 64 - dq * sw;
+        const int step = dq * W + dr;
+        uint32_t* d32 = reinterpret_cast<uint32_t*>(dst + head);
+#pragma unroll 4
+        for (int j = lane; j < npairs; j += 32) {
+            const int a2 = a + 1 + ((x + 1 < sw) ? 0 : wrap);   // second element may open the next row
+            d32[j] = static_cast<uint32_t>(src[a]) | (static_cast<uint32_t>(src[a2]) << 16);
             x += dr;
-            row += dq;
-            if (x >= sl.sw) { x -= sl.sw; ++row; }
+            a += step;
+            if (x >= sw) { x -= sw; a += wrap; }
         }
     } else {
-        int row = static_cast<int>(threadIdx.x) / sl.sw, x = static_cast<int>(threadIdx.x) - row * sl.sw;
-        const int step = static_cast<int>(blockDim.x);
-        const int dq = step / sl.sw, dr = step - dq * sl.sw;
-        for (int j = threadIdx.x; j < len; j += blockDim.x) {
-            dst[j] = band[sl.src + row * W + x];
+        const int r0 = small_div(lane, e.inv_sw);
+        int x = lane - r0 * sw;
+        int a = r0 * W + x;
+        const int dq = small_div(32, e.inv_sw), dr = 32 - dq * sw;
+        const int step = dq * W + dr;
+#pragma unroll 4
+        for (int j = lane; j < len; j += 32) {
+            dst[j] = src[a];
             x += dr;
-            row += dq;
-            if (x >= sl.sw) { x -= sl.sw; ++row; }
+            a += step;
+            if (x >= sw) { x -= sw; a += wrap; }
         }
     }
 }
 
+// Persistent: each CTA walks its item range; an item is one (frame, row
+// band, b, c) box of the latent, staged as one contiguous span.  Two
+// shared-memory stages: thread 0 issues the next item's bulk copy before
+// the current one is written out.
 template <typename E>
-__global__ void __launch_bounds__(kThreads) extract_kernel(const __grid_constant__ tdp_plan_t p,
+__global__ void __launch_bounds__(kThreads) extract_kernel(const __grid_constant__ tdp_plan_t pg,
                                                            const ExtractArgs a) {
+    __shared__ tdp_plan_t p;
+    load_plan(&p, pg);
+    __syncthreads();
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    ExtractSlot* slots = reinterpret_cast<ExtractSlot*>(smem + 16);
-    E* band = reinterpret_cast<E*>(smem + a.data_off);
+    ExtractSlot* slots = reinterpret_cast<ExtractSlot*>(smem + a.off_slots);
+    E* stage0 = reinterpret_cast<E*>(smem + a.off_data);
+    const int stage_elems = a.stage_bytes / static_cast<int>(sizeof(E));
     const E* latent = static_cast<const E*>(a.latent);
     E* tiles = static_cast<E*>(a.tiles);
+    const int F = p.dims[0], H = p.dims[1], W = p.dims[2], nw = p.num_tiles[2];
+    const uintptr_t limit = reinterpret_cast<uintptr_t>(latent + a.latent_numel) & ~uintptr_t(15);
 
-    const int F = p.dims[0], H = p.dims[1], W = p.dims[2];
-    int cta = blockIdx.x;
-    const int bi = cta % a.nbands;
-    cta /= a.nbands;
-    const int f = cta % F;
-    const int bc = cta / F;
-    const int hb0 = bi * a.band_rows, hb1 = min(H, hb0 + a.band_rows);
-
-    // The band [hb0, hb1) x [0, W) of plane (bc, f) is one contiguous span.
-    const long long span0 = ((long long)bc * F + f) * H * W + (long long)hb0 * W;
-    const int span_len = (hb1 - hb0) * W;
-    const uintptr_t g0 = reinterpret_cast<uintptr_t>(latent + span0);
-    const uintptr_t g1 = reinterpret_cast<uintptr_t>(latent + span0 + span_len);
-    const uintptr_t lo = g0 & ~uintptr_t(15), mid = g1 & ~uintptr_t(15);
-    const int shift = static_cast<int>((g0 - lo) / sizeof(E));
-    const uint32_t bulk = mid > lo ? static_cast<uint32_t>(mid - lo) : 0u;
-
-    if (threadIdx.x == 0) mbar_init(bar, 1);
-    __syncthreads();
+    int first, last;
+    cta_item_range(a.n_items, first, last);
+    if (first >= last) return;
+    // thread 0 stages ahead with its own cursor
+    ItemCursor ahead;
+    ahead.init(first, a.BC);
+    auto issue = [&](int s) {  // thread 0: stage the item under `ahead` into stage s
+        const FrameBand x = frame_band(p, ahead.fb, a.band_rows, a.nbands);
+        const long long span0 = ((long long)ahead.bc * F + x.f) * H * W + (long long)x.hb0 * W;
+        const int len = (x.hb1 - x.hb0) * W;
+        const SpanCopy cp = plan_span(latent, span0, len, limit);
+        E* band = stage0 + s * stage_elems;
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&bar[s], cp.bulk);
+        if (cp.bulk) bulk_copy_g2s(band, reinterpret_cast<const void*>(cp.lo), cp.bulk, &bar[s]);
+        for (int e = cp.tail0; e < len; ++e) band[cp.shift + e] = latent[span0 + e];
+    };
     if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(bar, bulk);
-        if (bulk) bulk_copy_g2s(band, reinterpret_cast<const void*>(lo), bulk, bar);
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        issue(0);
+        ahead.next();
     }
-    // Partial last 16 bytes: plain loads.
-    {
-        const int t0 = mid > g0 ? static_cast<int>((mid - g0) / sizeof(E)) : 0;
-        for (int e = t0 + threadIdx.x; e < span_len; e += blockDim.x) band[shift + e] = latent[span0 + e];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    ItemCursor cur;
+    cur.init(first, a.BC);
+    int cached_fb = -1, nslots = 0, band_len = 0, f = 0, hb0 = 0;
+    for (int k = 0, item = first; item < last; ++k, ++item, cur.next()) {
+        const int s = k & 1;
+        if (threadIdx.x == 0 && item + 1 < last) {
+            issue(s ^ 1);
+            ahead.next();
+        }
+        if (cur.fb != cached_fb) {
+            // One slot per (covering frame tile, row tile meeting the band, column tile).
+            const FrameBand x = frame_band(p, cur.fb, a.band_rows, a.nbands);
+            f = x.f;
+            hb0 = x.hb0;
+            band_len = (x.hb1 - x.hb0) * W;
+            int if_lo, if_hi, ih_lo, ih_hi;
+            tdp::axis_cover(p, 0, x.f, if_lo, if_hi);
+            tdp::axis_range_cover(p, 1, x.hb0, x.hb1, ih_lo, ih_hi);
+            const int NH = ih_hi - ih_lo + 1;
+            nslots = (if_hi - if_lo + 1) * NH * nw;
+            for (int sl = threadIdx.x; sl < nslots; sl += blockDim.x) {
+                const int iw = sl % nw, jh = (sl / nw) % NH, i_f = if_lo + sl / (nw * NH), i_h = ih_lo + jh;
+                const int sf = tdp::tile_size(p, 0, i_f), sh = tdp::tile_size(p, 1, i_h), sw = tdp::tile_size(p, 2, iw);
+                const int r0 = max(p.start[1][i_h], x.hb0), r1 = min(p.end[1][i_h], x.hb1);
+                ExtractSlot e;
+                e.vol = (long long)sf * sh * sw;
+                e.dst0 = (long long)a.BC * tdp::tile_prefix_volume(p, i_f, i_h, iw) +
+                         ((long long)(x.f - p.start[0][i_f]) * sh + (r0 - p.start[1][i_h])) * sw;
+                e.src = (r0 - x.hb0) * W + p.start[2][iw];
+                e.rows = r1 - r0;
+                e.sw = sw;
+                e.inv_sw = 1.0f / static_cast<float>(sw);
+                slots[sl] = e;
+            }
+            cached_fb = cur.fb;
+        }
+        const long long span0 = ((long long)cur.bc * F + f) * H * W + (long long)hb0 * W;
+        const int shift = plan_span(latent, span0, band_len, limit).shift;
+        if (!cta_wait(&bar[s], (k >> 1) & 1)) {
+            if (threadIdx.x == 0) {
+                atomicOr(&g_device_error, kErrExtractWait);
+                mbar_wait_bounded(&bar[s], (k >> 1) & 1);
+                if (item + 1 < last) mbar_wait_bounded(&bar[s ^ 1], ((k + 1) >> 1) & 1);
+            }
+            return;
+        }
+        const E* band = stage0 + s * stage_elems + shift;
+        for (int sl = warp; sl < nslots; sl += nwarps) {
+            const ExtractSlot e = slots[sl];
+            extract_copy_slot_warp<E>(tiles + e.dst0 + (long long)cur.bc * e.vol, band + e.src, e, W, lane);
+        }
+        __syncthreads();  // stage s is free again; the slot table may be rebuilt
     }
-    // One slot per (covering frame tile, row tile meeting the band, column tile).
-    int if_lo, if_hi, ih_lo, ih_hi;
-    tdp::axis_cover(p, 0, f, if_lo, if_hi);
-    tdp::axis_range_cover(p, 1, hb0, hb1, ih_lo, ih_hi);
-    const int nw = p.num_tiles[2], NH = ih_hi - ih_lo + 1;
-    const int nslots = (if_hi - if_lo + 1) * NH * nw;
-    for (int s = threadIdx.x; s < nslots; s += blockDim.x) {
-        const int iw = s % nw, jh = (s / nw) % NH, i_f = if_lo + s / (nw * NH), i_h = ih_lo + jh;
-        const int sf = tdp::tile_size(p, 0, i_f), sh = tdp::tile_size(p, 1, i_h), sw = tdp::tile_size(p, 2, iw);
-        const int r0 = max(p.start[1][i_h], hb0), r1 = min(p.end[1][i_h], hb1);
-        const long long tile0 = (long long)a.BC * tdp::tile_prefix_volume(p, i_f, i_h, iw);
-        ExtractSlot sl;
-        sl.dst = tile0 + (((long long)bc * sf + (f - p.start[0][i_f])) * sh + (r0 - p.start[1][i_h])) * sw;
-        sl.src = shift + (r0 - hb0) * W + p.start[2][iw];
-        sl.rows = r1 - r0;
-        sl.sw = sw;
-        sl.pad = 0;
-        slots[s] = sl;
-    }
-    __syncthreads();
-    if (!mbar_wait_or_flag(bar, kErrExtractWait)) return;
-    for (int s = 0; s < nslots; ++s) extract_copy_slot<E>(slots[s], band, tiles, W);
 }
 
 // =================================================================== K2: blend
@@ -292,214 +417,421 @@ struct Cov {
     float w;
 };
 
-struct StageSlot {       // one staged run of tile rows
-    long long src;       // element index in the packed tiles
-    int len;             // elements
-    int smem_off;        // byte offset inside the data region
+struct Combo {          // one (frame tile, row tile) pair covering a band row
+    int slot0;          // slot index of its column tile 0
+    float w;            // r_f * r_h, rounded
+};
+
+struct StageSlot {      // one run of tile rows of a (frame, band) box
+    long long src0;     // packed element index for b*C + c = 0
+    long long vol;      // elements per (b, c) of the tile: src = src0 + (b*C + c) * vol
+    int len;            // elements
+    int smem_off;       // byte offset inside a stage's data region
+    int r0sw;           // first row of the run times the tile width
+    int pad;
 };
 
 struct BlendArgs {
     const void* tiles;
     void* out;
+    long long tiles_numel;
     int BC;
     int band_rows;
     int nbands;
-    // shared-memory layout (bytes); computed on the host by blend_layout()
-    int off_fcov, off_hcnt, off_hcov, off_wcnt, off_wcov, off_wtile, off_slotbase, off_stage, off_data;
+    int n_items;
+    // shared-memory layout (bytes), computed on the host; slotbase and data
+    // have one copy per stage
+    int off_a, off_b, off_c, off_d, off_e, off_stage, off_slotbase, off_data;
+    int max_slots, data_bytes;
     int kf, kh, kw;
-};
-
-struct BlendLayout {
-    int off_fcov, off_hcnt, off_hcov, off_wcnt, off_wcov, off_wtile, off_slotbase, off_stage, off_data;
 };
 
 __host__ __device__ inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
-BlendLayout blend_layout(int kf, int kh, int kw, int band_rows, int W, int nw, int max_slots) {
-    BlendLayout L;
-    int o = 16;  // mbarrier
-    L.off_fcov = o; o = round_up(o + kf * (int)sizeof(Cov), 16);
-    L.off_hcnt = o; o = round_up(o + band_rows * 4, 16);
-    L.off_hcov = o; o = round_up(o + band_rows * kh * (int)sizeof(Cov), 16);
-    L.off_wcnt = o; o = round_up(o + W * 4, 16);
-    L.off_wcov = o; o = round_up(o + W * kw * (int)sizeof(Cov), 16);
-    L.off_wtile = o; o = round_up(o + nw * 8, 16);
-    L.off_slotbase = o; o = round_up(o + max_slots * 4, 16);
-    L.off_stage = o; o = round_up(o + max_slots * (int)sizeof(StageSlot), 16);
-    L.off_data = o;
-    return L;
+struct BlendBox {
+    int f, hb0, hb1, rows, if_lo, if_hi, ih_lo, ih_hi, NF, NH, nslots;
+};
+
+__device__ __forceinline__ BlendBox blend_box(const tdp_plan_t& p, const BlendArgs& a, int fb) {
+    BlendBox c;
+    const FrameBand x = frame_band(p, fb, a.band_rows, a.nbands);
+    c.f = x.f;
+    c.hb0 = x.hb0;
+    c.hb1 = x.hb1;
+    c.rows = c.hb1 - c.hb0;
+    tdp::axis_cover(p, 0, c.f, c.if_lo, c.if_hi);
+    tdp::axis_range_cover(p, 1, c.hb0, c.hb1, c.ih_lo, c.ih_hi);
+    c.NF = c.if_hi - c.if_lo + 1;
+    c.NH = c.ih_hi - c.ih_lo + 1;
+    c.nslots = c.NF * c.NH * p.num_tiles[2];
+    return c;
 }
 
-__device__ __forceinline__ void store_out(float* out, long long i, const float (&v)[1]) { out[i] = v[0]; }
-__device__ __forceinline__ void store_out(__nv_bfloat16* out, long long i, const float (&v)[1]) {
-    out[i] = __float2bfloat16_rn(v[0]);
-}
-__device__ __forceinline__ void store_out(__nv_bfloat16* out, long long i, const float (&v)[2]) {
-    const uint32_t lo = to_bits(__float2bfloat16_rn(v[0]));
-    const uint32_t hi = to_bits(__float2bfloat16_rn(v[1]));
-    *reinterpret_cast<uint32_t*>(out + i) = lo | (hi << 16);
-}
-__device__ __forceinline__ void store_out(float* out, long long i, const float (&v)[2]) {
-    *reinterpret_cast<float2*>(out + i) = make_float2(v[0], v[1]);
+// Warp 0: the staged runs of one (frame, band) box -- one per (covering
+// frame tile, row tile meeting the band, column tile) -- and their layout
+// in a stage's data region (exclusive scan of padded sizes).
+template <typename Tin>
+__device__ void blend_build_stage_table(const tdp_plan_t& p, const BlendArgs& a, const BlendBox& c,
+                                        StageSlot* table) {
+    const int lane = threadIdx.x & 31, nw = p.num_tiles[2];
+    int carry = 0;
+    for (int s0 = 0; s0 < c.nslots; s0 += 32) {
+        const int s = s0 + lane;
+        int padded = 0;
+        StageSlot st;
+        if (s < c.nslots) {
+            const int iw = s % nw, jh = (s / nw) % c.NH, i_f = c.if_lo + s / (nw * c.NH), i_h = c.ih_lo + jh;
+            const int sf = tdp::tile_size(p, 0, i_f), sh = tdp::tile_size(p, 1, i_h), sw = tdp::tile_size(p, 2, iw);
+            const int r0 = max(p.start[1][i_h], c.hb0), r1 = min(p.end[1][i_h], c.hb1);
+            st.vol = (long long)sf * sh * sw;
+            st.src0 = (long long)a.BC * tdp::tile_prefix_volume(p, i_f, i_h, iw) +
+                      ((long long)(c.f - p.start[0][i_f]) * sh + (r0 - p.start[1][i_h])) * sw;
+            st.len = (r1 - r0) * sw;
+            st.r0sw = r0 * sw;
+            st.pad = 0;
+            padded = round_up(st.len * (int)sizeof(Tin), 16) + 16;
+        }
+        const int incl = warp_incl_scan(padded);
+        if (s < c.nslots) {
+            st.smem_off = carry + incl - padded;
+            table[s] = st;
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    __syncwarp();
 }
 
-// U = output columns per thread item (2 when a pair store is aligned).
-template <typename Tin, typename Tout, int U>
-__global__ void __launch_bounds__(kThreads) blend_kernel(const __grid_constant__ tdp_plan_t p, const BlendArgs a) {
+// Warp 0: stage item (box table, b*C + c) into a stage: arm its barrier
+// with the bulk bytes, issue one bulk copy per run (plain loads for a run
+// ending in the buffer's last partial 16 bytes) and record, per run, the
+// shared element index of (its row 0, column 0).
+template <typename Tin>
+__device__ void blend_stage_item(const Tin* tiles, uintptr_t limit, const StageSlot* table, int nslots, int bc,
+                                 int* slotbase, unsigned char* data, uint64_t* bar) {
+    const int lane = threadIdx.x & 31;
+    uint32_t bytes = 0;
+    for (int s = lane; s < nslots; s += 32) {
+        const StageSlot st = table[s];
+        bytes += plan_span(tiles, st.src0 + (long long)bc * st.vol, st.len, limit).bulk;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+    fence_proxy_async();
+    if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+    __syncwarp();
+    for (int s = lane; s < nslots; s += 32) {
+        const StageSlot st = table[s];
+        const long long src = st.src0 + (long long)bc * st.vol;
+        const SpanCopy cp = plan_span(tiles, src, st.len, limit);
+        if (cp.bulk) bulk_copy_g2s(data + st.smem_off, reinterpret_cast<const void*>(cp.lo), cp.bulk, bar);
+        Tin* dst = reinterpret_cast<Tin*>(data + st.smem_off) + cp.shift;
+        for (int e = cp.tail0; e < st.len; ++e) dst[e] = tiles[src + e];
+        slotbase[s] = st.smem_off / (int)sizeof(Tin) + cp.shift - st.r0sw;
+    }
+}
+
+// A thread's column tiles ("terms") for its output columns c .. c+U-1: the
+// tiles covering any of them, each with the columns' offset into the tile
+// row, the tile width, and per column the weight r_w and whether the tile
+// reaches it.  Terms past the count are copies of the last one with no
+// column reached (weight 0, value masked to 0), so every thread runs the
+// same KT terms.
+template <int U, int KT>
+struct Terms {
+    int iw[KT], xo[KT], sw[KT];
+    float w[KT][U];
+    bool in[KT][U];
+};
+
+template <int U, int KT>
+__device__ __forceinline__ void load_terms(const tdp_plan_t& p, int c, int W, Terms<U, KT>& t) {
+    int lo, hi;
+    tdp::axis_cover(p, 2, c, lo, hi);
+#pragma unroll
+    for (int v = 1; v < U; ++v) {
+        if (c + v < W) {
+            int l2, h2;
+            tdp::axis_cover(p, 2, c + v, l2, h2);
+            lo = min(lo, l2);
+            hi = max(hi, h2);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < KT; ++q) {
+        const bool real = lo + q <= hi;
+        const int i = min(lo + q, hi);
+        const int w0 = p.start[2][i], w1 = p.end[2][i];
+        t.iw[q] = i;
+        t.sw[q] = w1 - w0;
+        t.xo[q] = c - w0;
+#pragma unroll
+        for (int v = 0; v < U; ++v) {
+            const bool in = real && c + v >= w0 && c + v < w1;
+            t.in[q][v] = in;
+            t.w[q][v] = in ? axis_weight(p, 2, i, c + v) : 0.0f;
+        }
+    }
+}
+
+__device__ __forceinline__ float load_elem(const __nv_bfloat16* d, int i) {
+    return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(d)[i]) << 16);
+}
+__device__ __forceinline__ float load_elem(const float* d, int i) { return d[i]; }
+
+template <int U>
+__device__ __forceinline__ void store_cols(float* out, long long i, const float (&v)[U]) {
+    if constexpr (U == 2) *reinterpret_cast<float2*>(out + i) = make_float2(v[0], v[1]);
+    else out[i] = v[0];
+}
+template <int U>
+__device__ __forceinline__ void store_cols(__nv_bfloat16* out, long long i, const float (&v)[U]) {
+    if constexpr (U == 2) {
+        uint32_t b;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b) : "f"(v[1]), "f"(v[0]));
+        *reinterpret_cast<uint32_t*>(out + i) = b;
+    } else {
+        out[i] = __float2bfloat16_rn(v[0]);
+    }
+}
+
+// Blend for plans where at most two tiles cover any index on every axis
+// (always the case under the guard: a tile holds at least twice the
+// overlap, so tiles i and i+2 never meet).
+//
+// Persistent over a contiguous range of (frame, band, b, c) items with two
+// shared-memory stages: warp 0 stages the next item's tile rows while the
+// CTA blends the current one.  A thread owns U adjacent output columns for
+// the whole run (U = 2, or 1 when W is odd) and KT column-tile terms for
+// them; it walks the rows of its row group, where a per-row table lists the
+// (frame tile, row tile) pairs covering the row with w_fh = r_f * r_h.  Per
+// pair and column the thread forms inner = sum over column tiles of
+// r_w * value, then acc = fma(w_fh, inner, acc): the window product
+// r_f r_h r_w grouped as w_fh * (r_w * value), in fp32, summed in the order
+// (frame tile, row tile, column tile).
+template <typename Tin, typename Tout, int U, int KT>
+__global__ void __launch_bounds__(kThreads, 3) blend_fast_kernel(const __grid_constant__ tdp_plan_t pg,
+                                                              const BlendArgs a) {
+    __shared__ tdp_plan_t p;
+    load_plan(&p, pg);
+    __syncthreads();
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    Cov* fcov = reinterpret_cast<Cov*>(smem + a.off_fcov);
-    int* hcnt = reinterpret_cast<int*>(smem + a.off_hcnt);
-    Cov* hcov = reinterpret_cast<Cov*>(smem + a.off_hcov);
-    int* wcnt = reinterpret_cast<int*>(smem + a.off_wcnt);
-    Cov* wcov = reinterpret_cast<Cov*>(smem + a.off_wcov);
-    int2* wtile = reinterpret_cast<int2*>(smem + a.off_wtile);  // (start, size) per column tile
+    int* ncombo = reinterpret_cast<int*>(smem + a.off_a);
+    Combo* combo = reinterpret_cast<Combo*>(smem + a.off_b);
+    StageSlot* table = reinterpret_cast<StageSlot*>(smem + a.off_stage);
+    int* slotbase0 = reinterpret_cast<int*>(smem + a.off_slotbase);
+    unsigned char* data0 = smem + a.off_data;
+    const Tin* tiles = static_cast<const Tin*>(a.tiles);
+    Tout* out = static_cast<Tout*>(a.out);
+    const int F = p.dims[0], H = p.dims[1], W = p.dims[2], nw = p.num_tiles[2];
+    const int KC = a.kf * a.kh;
+    const int max_slots = a.max_slots;
+    const int data_elems = a.data_bytes / static_cast<int>(sizeof(Tin));
+    const uintptr_t limit = reinterpret_cast<uintptr_t>(tiles + a.tiles_numel) & ~uintptr_t(15);
+
+    int first, last;
+    cta_item_range(a.n_items, first, last);
+    if (first >= last) return;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+    }
+    __syncthreads();
+    // warp 0: stage table for the (frame, band) of the item it stages next
+    int table_fb = -1, table_n = 0;
+    ItemCursor ahead;
+    ahead.init(first, a.BC);
+    if (threadIdx.x < 32) {
+        const BlendBox c0 = blend_box(p, a, ahead.fb);
+        blend_build_stage_table<Tin>(p, a, c0, table);
+        table_fb = ahead.fb;
+        table_n = c0.nslots;
+        blend_stage_item(tiles, limit, table, table_n, ahead.bc, slotbase0, data0, &bar[0]);
+    }
+    ahead.next();
+
+    // This thread's columns and terms (fixed for the run).  A row group is
+    // the column units rounded up to whole warps, so a warp stays on one row
+    // and walks one (frame tile, row tile) list.
+    const int ncu = (W + U - 1) / U;
+    const int per_row = min(round_up(ncu, 32), static_cast<int>(blockDim.x));
+    const int RG = static_cast<int>(blockDim.x) / per_row;
+    const int rg = static_cast<int>(threadIdx.x) / per_row;
+    const int cu0 = static_cast<int>(threadIdx.x) - rg * per_row;
+    const int ncu_mine = (rg < RG && cu0 < ncu) ? (ncu - cu0 + per_row - 1) / per_row : 0;
+    Terms<U, KT> tm;
+    if (ncu_mine == 1) load_terms<U, KT>(p, cu0 * U, W, tm);
+
+    ItemCursor cur;
+    cur.init(first, a.BC);
+    int box_fb = -1;
+    BlendBox c{};
+    for (int k = 0, item = first; item < last; ++k, ++item, cur.next()) {
+        const int s = k & 1;
+        if (cur.fb != box_fb) c = blend_box(p, a, cur.fb);
+        if (threadIdx.x < 32) {
+            if (item + 1 < last) {
+                if (ahead.fb != table_fb) {
+                    const BlendBox cn = blend_box(p, a, ahead.fb);
+                    blend_build_stage_table<Tin>(p, a, cn, table);
+                    table_fb = ahead.fb;
+                    table_n = cn.nslots;
+                }
+                blend_stage_item(tiles, limit, table, table_n, ahead.bc, slotbase0 + (s ^ 1) * max_slots,
+                                 data0 + (s ^ 1) * a.data_bytes, &bar[s ^ 1]);
+                ahead.next();
+            }
+        } else if (cur.fb != box_fb) {
+            for (int r = threadIdx.x - 32; r < c.rows; r += blockDim.x - 32) {
+                const int h = c.hb0 + r;
+                int lo, hi;
+                tdp::axis_cover(p, 1, h, lo, hi);
+                int n = 0;
+                for (int fa = 0; fa < c.NF; ++fa) {
+                    const float wf = axis_weight(p, 0, c.if_lo + fa, c.f);
+                    for (int ih = lo; ih <= hi; ++ih)
+                        combo[r * KC + n++] =
+                            Combo{(fa * c.NH + ih - c.ih_lo) * nw, __fmul_rn(wf, axis_weight(p, 1, ih, h))};
+                }
+                ncombo[r] = n;
+            }
+        }
+        box_fb = cur.fb;
+        if (!cta_wait(&bar[s], (k >> 1) & 1)) {
+            if (threadIdx.x == 0) {
+                atomicOr(&g_device_error, kErrBlendWait);
+                mbar_wait_bounded(&bar[s], (k >> 1) & 1);
+                if (item + 1 < last) mbar_wait_bounded(&bar[s ^ 1], ((k + 1) >> 1) & 1);
+            }
+            return;
+        }
+        const Tin* sdata = reinterpret_cast<const Tin*>(data0) + s * data_elems;
+        const int* sbase = slotbase0 + s * max_slots;
+        const long long out0 = ((long long)cur.bc * F + c.f) * H * W + (long long)c.hb0 * W;
+        for (int m = 0; m < ncu_mine; ++m) {
+            const int cu = cu0 + m * per_row;
+            if (ncu_mine > 1) load_terms<U, KT>(p, cu * U, W, tm);
+            int rowoff[KT];
+#pragma unroll
+            for (int q = 0; q < KT; ++q) rowoff[q] = (c.hb0 + rg) * tm.sw[q] + tm.xo[q];
+            for (int r = rg; r < c.rows; r += RG) {
+                float acc[U];
+#pragma unroll
+                for (int v = 0; v < U; ++v) acc[v] = 0.0f;
+                const int nc = ncombo[r];
+                for (int kk = 0; kk < nc; ++kk) {
+                    const Combo cb = combo[r * KC + kk];
+                    float inner[U];
+#pragma unroll
+                    for (int v = 0; v < U; ++v) inner[v] = 0.0f;
+#pragma unroll
+                    for (int q = 0; q < KT; ++q) {
+                        const int i = sbase[cb.slot0 + tm.iw[q]] + rowoff[q];
+#pragma unroll
+                        for (int v = 0; v < U; ++v) {
+                            const float x = load_elem(sdata, i + v);
+                            inner[v] = fmaf(tm.w[q][v], tm.in[q][v] ? x : 0.0f, inner[v]);
+                        }
+                    }
+#pragma unroll
+                    for (int v = 0; v < U; ++v) acc[v] = fmaf(cb.w, inner[v], acc[v]);
+                }
+                store_cols<U>(out, out0 + (long long)r * W + cu * U, acc);
+#pragma unroll
+                for (int q = 0; q < KT; ++q) rowoff[q] += RG * tm.sw[q];
+            }
+        }
+        __syncthreads();  // stage s, its slot bases and the row table are free again
+    }
+}
+
+// Blend for any plan (guard-violating layouts can cover an index with more
+// than two tiles per axis): one item per CTA, per-CTA cover tables in
+// shared memory; same arithmetic grouping as the fast kernel.
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kThreads) blend_generic_kernel(const __grid_constant__ tdp_plan_t pg,
+                                                                 const BlendArgs a) {
+    __shared__ tdp_plan_t p;
+    load_plan(&p, pg);
+    __syncthreads();
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    Cov* fcov = reinterpret_cast<Cov*>(smem + a.off_a);
+    int* hcnt = reinterpret_cast<int*>(smem + a.off_b);
+    Cov* hcov = reinterpret_cast<Cov*>(smem + a.off_c);
+    int* wcnt = reinterpret_cast<int*>(smem + a.off_d);
+    Cov* wcov = reinterpret_cast<Cov*>(smem + a.off_e);
+    StageSlot* table = reinterpret_cast<StageSlot*>(smem + a.off_stage);
     int* slotbase = reinterpret_cast<int*>(smem + a.off_slotbase);
-    StageSlot* stage = reinterpret_cast<StageSlot*>(smem + a.off_stage);
     unsigned char* data = smem + a.off_data;
     const Tin* tiles = static_cast<const Tin*>(a.tiles);
     Tout* out = static_cast<Tout*>(a.out);
-
-    const int F = p.dims[0], H = p.dims[1], W = p.dims[2];
-    int cta = blockIdx.x;
-    const int bi = cta % a.nbands;
-    cta /= a.nbands;
-    const int f = cta % F;
-    const int bc = cta / F;
-    const int hb0 = bi * a.band_rows, hb1 = min(H, hb0 + a.band_rows);
-    const int rows = hb1 - hb0;
-
-    int if_lo, if_hi, ih_lo, ih_hi;
-    tdp::axis_cover(p, 0, f, if_lo, if_hi);
-    tdp::axis_range_cover(p, 1, hb0, hb1, ih_lo, ih_hi);
-    const int nw = p.num_tiles[2], NH = ih_hi - ih_lo + 1, NF = if_hi - if_lo + 1;
-    const int nslots = NF * NH * nw;
+    const int F = p.dims[0], H = p.dims[1], W = p.dims[2], nw = p.num_tiles[2];
+    const int fb = blockIdx.x / a.BC, bc = blockIdx.x - fb * a.BC;
+    const BlendBox c = blend_box(p, a, fb);
+    const uintptr_t limit = reinterpret_cast<uintptr_t>(tiles + a.tiles_numel) & ~uintptr_t(15);
 
     if (threadIdx.x == 0) mbar_init(bar, 1);
     __syncthreads();
-
     if (threadIdx.x < 32) {
-        // Warp 0: locate each slot's run of tile rows, lay the runs out in
-        // shared memory (exclusive scan of their padded sizes), then issue
-        // one bulk copy per run plus plain loads for its partial tail.
-        const int lane = threadIdx.x;
-        int carry = 0;
-        for (int s0 = 0; s0 < nslots; s0 += 32) {
-            const int s = s0 + lane;
-            int padded = 0;
-            StageSlot st;
-            int r0 = 0, sw = 1;
-            if (s < nslots) {
-                const int iw = s % nw, jh = (s / nw) % NH, i_f = if_lo + s / (nw * NH), i_h = ih_lo + jh;
-                const int sf = tdp::tile_size(p, 0, i_f), sh = tdp::tile_size(p, 1, i_h);
-                sw = tdp::tile_size(p, 2, iw);
-                r0 = max(p.start[1][i_h], hb0);
-                const int r1 = min(p.end[1][i_h], hb1);
-                const long long tile0 = (long long)a.BC * tdp::tile_prefix_volume(p, i_f, i_h, iw);
-                st.src = tile0 + (((long long)bc * sf + (f - p.start[0][i_f])) * sh + (r0 - p.start[1][i_h])) * sw;
-                st.len = (r1 - r0) * sw;
-                padded = round_up(st.len * (int)sizeof(Tin), 16) + 16;
-            }
-            const int incl = warp_incl_scan(padded);
-            if (s < nslots) {
-                st.smem_off = carry + incl - padded;
-                stage[s] = st;
-                const uintptr_t g0 = reinterpret_cast<uintptr_t>(tiles + st.src);
-                const uintptr_t lo = g0 & ~uintptr_t(15);
-                // shared element index of (row r0, column 0) of this slot, minus r0*sw
-                slotbase[s] = (st.smem_off + static_cast<int>(g0 - lo)) / (int)sizeof(Tin) - r0 * sw;
-            }
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        __syncwarp();
-        // Total bytes the bulk copies will deliver.
-        uint32_t mine = 0;
-        for (int s = lane; s < nslots; s += 32) {
-            const StageSlot st = stage[s];
-            const uintptr_t g0 = reinterpret_cast<uintptr_t>(tiles + st.src);
-            const uintptr_t g1 = reinterpret_cast<uintptr_t>(tiles + st.src + st.len);
-            const uintptr_t lo = g0 & ~uintptr_t(15), mid = g1 & ~uintptr_t(15);
-            if (mid > lo) mine += static_cast<uint32_t>(mid - lo);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-        if (lane == 0) mbar_arrive_expect_tx(bar, mine);
-        __syncwarp();
-        for (int s = lane; s < nslots; s += 32) {
-            const StageSlot st = stage[s];
-            const uintptr_t g0 = reinterpret_cast<uintptr_t>(tiles + st.src);
-            const uintptr_t g1 = reinterpret_cast<uintptr_t>(tiles + st.src + st.len);
-            const uintptr_t lo = g0 & ~uintptr_t(15), mid = g1 & ~uintptr_t(15);
-            if (mid > lo) bulk_copy_g2s(data + st.smem_off, reinterpret_cast<const void*>(lo),
-                                        static_cast<uint32_t>(mid - lo), bar);
-            Tin* dst = reinterpret_cast<Tin*>(data + st.smem_off + (g0 - lo));
-            const int t0 = mid > g0 ? static_cast<int>((mid - g0) / sizeof(Tin)) : 0;
-            for (int e = t0; e < st.len; ++e) dst[e] = tiles[st.src + e];
-        }
+        blend_build_stage_table<Tin>(p, a, c, table);
+        blend_stage_item(tiles, limit, table, c.nslots, bc, slotbase, data, bar);
     } else {
-        // Warps 1..: weight tables (ascending tile order on every axis).
         const int t = threadIdx.x - 32, nt = blockDim.x - 32;
-        if (t == 0) {
-            for (int i = if_lo; i <= if_hi; ++i) fcov[i - if_lo] = Cov{i, axis_weight(p, 0, i, f)};
-        }
-        for (int r = t; r < rows; r += nt) {
+        if (t == 0)
+            for (int i = c.if_lo; i <= c.if_hi; ++i) fcov[i - c.if_lo] = Cov{i, axis_weight(p, 0, i, c.f)};
+        for (int r = t; r < c.rows; r += nt) {
             int lo, hi;
-            tdp::axis_cover(p, 1, hb0 + r, lo, hi);
+            tdp::axis_cover(p, 1, c.hb0 + r, lo, hi);
             hcnt[r] = hi - lo + 1;
-            for (int i = lo; i <= hi; ++i) hcov[r * a.kh + (i - lo)] = Cov{i, axis_weight(p, 1, i, hb0 + r)};
+            for (int i = lo; i <= hi; ++i) hcov[r * a.kh + (i - lo)] = Cov{i, axis_weight(p, 1, i, c.hb0 + r)};
         }
-        for (int c = t; c < W; c += nt) {
+        for (int col = t; col < W; col += nt) {
             int lo, hi;
-            tdp::axis_cover(p, 2, c, lo, hi);
-            wcnt[c] = hi - lo + 1;
-            for (int i = lo; i <= hi; ++i) wcov[c * a.kw + (i - lo)] = Cov{i, axis_weight(p, 2, i, c)};
+            tdp::axis_cover(p, 2, col, lo, hi);
+            wcnt[col] = hi - lo + 1;
+            for (int i = lo; i <= hi; ++i) wcov[col * a.kw + (i - lo)] = Cov{i, axis_weight(p, 2, i, col)};
         }
-        for (int i = t; i < nw; i += nt) wtile[i] = make_int2(p.start[2][i], tdp::tile_size(p, 2, i));
     }
-    __syncthreads();
-    if (!mbar_wait_or_flag(bar, kErrBlendWait)) return;
+    if (!cta_wait(bar, 0)) {
+        if (threadIdx.x == 0) {
+            atomicOr(&g_device_error, kErrBlendWait);
+            mbar_wait_bounded(bar, 0);
+        }
+        return;
+    }
 
     const Tin* sdata = reinterpret_cast<const Tin*>(data);
-    const int ncu = W / U;
-    const long long out0 = ((long long)bc * F + f) * H * W + (long long)hb0 * W;
-    const int items = rows * ncu;
-    int r = static_cast<int>(threadIdx.x) / ncu, cu = static_cast<int>(threadIdx.x) - r * ncu;
-    const int dq = static_cast<int>(blockDim.x) / ncu, dr = static_cast<int>(blockDim.x) - dq * ncu;
-    for (int it = threadIdx.x; it < items; it += blockDim.x) {
-        const int h = hb0 + r;
-        float acc[U];
-#pragma unroll
-        for (int v = 0; v < U; ++v) acc[v] = 0.0f;
-        const int hc = hcnt[r];
-        for (int fa = 0; fa < NF; ++fa) {
+    const long long out0 = ((long long)bc * F + c.f) * H * W + (long long)c.hb0 * W;
+    for (int it = threadIdx.x; it < c.rows * W; it += blockDim.x) {
+        const int r = it / W, col = it - r * W, h = c.hb0 + r;
+        float acc = 0.0f;
+        for (int fa = 0; fa < c.NF; ++fa) {
             const float wf = fcov[fa].w;
-            for (int k = 0; k < hc; ++k) {
+            for (int k = 0; k < hcnt[r]; ++k) {
                 const Cov hk = hcov[r * a.kh + k];
                 const float wfh = __fmul_rn(wf, hk.w);
-                const int sbase = (fa * NH + (hk.i - ih_lo)) * nw;
-#pragma unroll
-                for (int v = 0; v < U; ++v) {
-                    const int col = cu * U + v;
-                    const int wc = wcnt[col];
-                    for (int q = 0; q < wc; ++q) {
-                        const Cov wq = wcov[col * a.kw + q];
-                        const int2 wt = wtile[wq.i];
-                        const int idx = slotbase[sbase + wq.i] + h * wt.y + (col - wt.x);
-                        acc[v] = fmaf(__fmul_rn(wfh, wq.w), load_f(sdata, idx), acc[v]);
-                    }
+                const int sb = (fa * c.NH + (hk.i - c.ih_lo)) * nw;
+                float inner = 0.0f;
+                for (int q = 0; q < wcnt[col]; ++q) {
+                    const Cov wq = wcov[col * a.kw + q];
+                    const int idx = slotbase[sb + wq.i] + h * tdp::tile_size(p, 2, wq.i) + (col - p.start[2][wq.i]);
+                    inner = fmaf(wq.w, load_elem(sdata, idx), inner);
                 }
+                acc = fmaf(wfh, inner, acc);
             }
         }
-        store_out(out, out0 + (long long)r * W + cu * U, acc);
-        cu += dr;
-        r += dq;
-        if (cu >= ncu) { cu -= ncu; ++r; }
+        const float v[1] = {acc};
+        store_cols<1>(out, out0 + it, v);
     }
 }
 
 // =================================================================== K3: window sum
-__global__ void __launch_bounds__(kThreads) window_sum_kernel(const __grid_constant__ tdp_plan_t p,
+__global__ void __launch_bounds__(kThreads, 1) window_sum_kernel(const __grid_constant__ tdp_plan_t pg,
                                                               float* max_abs_dev, float* sum_out) {
+    __shared__ tdp_plan_t p;
+    load_plan(&p, pg);
+    __syncthreads();
     const int F = p.dims[0], H = p.dims[1], W = p.dims[2];
     const long long N = (long long)F * H * W;
     float worst = 0.0f;
@@ -512,14 +844,17 @@ __global__ void __launch_bounds__(kThreads) window_sum_kernel(const __grid_const
         tdp::axis_cover(p, 0, f, f0, f1);
         tdp::axis_cover(p, 1, h, h0, h1);
         tdp::axis_cover(p, 2, w, w0, w1);
-        // Same weights, products and summation order as the blend kernel
-        // (products rounded on their own: never contracted into the sum).
+        // Same weights and grouping as the blend kernels applied to tiles of
+        // ones: per (frame tile, row tile) pair, inner = sum of r_w over the
+        // column tiles, then S = fma(r_f * r_h, inner, S).
         float S = 0.0f;
         for (int i = f0; i <= f1; ++i) {
             const float wf = axis_weight(p, 0, i, f);
             for (int j = h0; j <= h1; ++j) {
                 const float wfh = __fmul_rn(wf, axis_weight(p, 1, j, h));
-                for (int k = w0; k <= w1; ++k) S = __fadd_rn(S, __fmul_rn(wfh, axis_weight(p, 2, k, w)));
+                float inner = 0.0f;
+                for (int k = w0; k <= w1; ++k) inner = fmaf(axis_weight(p, 2, k, w), 1.0f, inner);
+                S = fmaf(wfh, inner, S);
             }
         }
         if (sum_out) sum_out[idx] = S;
@@ -628,8 +963,11 @@ struct PositionsArgs {
     int normalize;
 };
 
-__global__ void __launch_bounds__(kThreads) positions_kernel(const __grid_constant__ tdp_plan_t p,
+__global__ void __launch_bounds__(kThreads) positions_kernel(const __grid_constant__ tdp_plan_t pg,
                                                              const PositionsArgs a) {
+    __shared__ tdp_plan_t p;
+    load_plan(&p, pg);
+    __syncthreads();
     __shared__ int ext_sh[6];
     cg::cluster_group cluster = cg::this_cluster();
     const int tb = blockIdx.x / kCluster;
@@ -678,7 +1016,10 @@ __device__ __forceinline__ bool cond_keep(const int* cond, int b, int M, int m, 
     return ok;
 }
 
-__global__ void __launch_bounds__(kThreads) cond_kernel(const __grid_constant__ tdp_plan_t p, const CondArgs a) {
+__global__ void __launch_bounds__(kThreads) cond_kernel(const __grid_constant__ tdp_plan_t pg, const CondArgs a) {
+    __shared__ tdp_plan_t p;
+    load_plan(&p, pg);
+    __syncthreads();
     __shared__ int ext_sh[6];
     __shared__ int scan_sh[33];
     __shared__ int kept_sh;
@@ -784,21 +1125,38 @@ int max_slots_for(const tdp_plan_t& p, int band_rows, int nbands) {
     return best;
 }
 
-int extract_smem(const tdp_plan_t& p, int band_rows, int esz, int* data_off) {
+// Shared-memory layout of an extract CTA: two barriers, the slot table and
+// two staged bands.
+struct ExtractLayout {
+    int off_slots, off_data, stage_bytes, total;
+};
+
+ExtractLayout extract_layout(const tdp_plan_t& p, int band_rows, int esz) {
     const int nbands = (p.dims[1] + band_rows - 1) / band_rows;
-    const int slots = max_slots_for(p, band_rows, nbands);
-    *data_off = round_up(16 + slots * (int)sizeof(ExtractSlot), 16);
-    const long long bytes = (long long)*data_off + round_up(band_rows * p.dims[2] * esz, 16) + 16;
-    return bytes > INT_MAX ? INT_MAX : static_cast<int>(bytes);
+    ExtractLayout L;
+    L.off_slots = 16;
+    L.off_data = round_up(L.off_slots + max_slots_for(p, band_rows, nbands) * (int)sizeof(ExtractSlot), 16);
+    const long long stage = (long long)round_up(band_rows * p.dims[2] * esz, 16) + 16;
+    const long long total = L.off_data + 2 * stage;
+    L.stage_bytes = stage > INT_MAX ? INT_MAX : static_cast<int>(stage);
+    L.total = total > INT_MAX ? INT_MAX : static_cast<int>(total);
+    return L;
 }
 
-// Exact shared-memory need of the blend for a band height: tables plus the
-// largest sum of padded staged runs over all (frame, band) boxes.
-int blend_smem(const tdp_plan_t& p, int band_rows, int esz, BlendLayout* L) {
-    const int H = p.dims[1], W = p.dims[2], nw = p.num_tiles[2];
+// Shared-memory layout of a blend CTA: barriers, then the fast kernel's
+// per-row (frame tile, row tile) table or the generic kernel's per-axis
+// cover tables, then the slot tables and the staged tile rows -- two
+// stages for the (persistent) fast kernel, one for the generic kernel.
+struct BlendLayout {
+    int off_a, off_b, off_c, off_d, off_e, off_slotbase, off_stage, off_data;
+    int max_slots, data_bytes, total;
+    bool fast;
+};
+
+// Largest sum of padded staged runs over all (frame, band) boxes.
+long long blend_data_bytes(const tdp_plan_t& p, int band_rows, int esz) {
+    const int H = p.dims[1], nw = p.num_tiles[2];
     const int nbands = (H + band_rows - 1) / band_rows;
-    const int slots = max_slots_for(p, band_rows, nbands);
-    *L = blend_layout(p.max_cover[0], p.max_cover[1], p.max_cover[2], band_rows, W, nw, slots);
     long long worst = 0;
     for (int f = 0; f < p.dims[0]; ++f) {
         int flo, fhi;
@@ -810,14 +1168,60 @@ int blend_smem(const tdp_plan_t& p, int band_rows, int esz, BlendLayout* L) {
             long long sum = 0;
             for (int i_h = hlo; i_h <= hhi; ++i_h) {
                 const int rows = std::min(p.end[1][i_h], hb1) - std::max(p.start[1][i_h], hb0);
-                for (int iw = 0; iw < nw; ++iw)
-                    sum += round_up(rows * tdp::tile_size(p, 2, iw) * esz, 16) + 16;
+                for (int iw = 0; iw < nw; ++iw) sum += round_up(rows * tdp::tile_size(p, 2, iw) * esz, 16) + 16;
             }
             worst = std::max(worst, sum * (fhi - flo + 1));
         }
     }
-    const long long bytes = L->off_data + worst;
-    return bytes > INT_MAX ? INT_MAX : static_cast<int>(bytes);
+    return worst;
+}
+
+BlendLayout blend_layout(const tdp_plan_t& p, int band_rows, int esz) {
+    const int kf = p.max_cover[0], kh = p.max_cover[1], kw = p.max_cover[2], W = p.dims[2];
+    const int nbands = (p.dims[1] + band_rows - 1) / band_rows;
+    BlendLayout L;
+    L.fast = kf <= 2 && kh <= 2 && kw <= 2;
+    const int stages = L.fast ? 2 : 1;
+    L.max_slots = max_slots_for(p, band_rows, nbands);
+    int o = 16;  // two mbarriers
+    if (L.fast) {
+        L.off_a = o; o = round_up(o + band_rows * 4, 16);                             // ncombo
+        L.off_b = o; o = round_up(o + band_rows * kf * kh * (int)sizeof(Combo), 16);  // combo
+        L.off_c = L.off_d = L.off_e = o;
+    } else {
+        L.off_a = o; o = round_up(o + kf * (int)sizeof(Cov), 16);                     // fcov
+        L.off_b = o; o = round_up(o + band_rows * 4, 16);                             // hcnt
+        L.off_c = o; o = round_up(o + band_rows * kh * (int)sizeof(Cov), 16);         // hcov
+        L.off_d = o; o = round_up(o + W * 4, 16);                                     // wcnt
+        L.off_e = o; o = round_up(o + W * kw * (int)sizeof(Cov), 16);                 // wcov
+    }
+    L.off_stage = o; o = round_up(o + L.max_slots * (int)sizeof(StageSlot), 16);
+    L.off_slotbase = o; o = round_up(o + stages * L.max_slots * 4, 16);
+    L.off_data = o;
+    const long long data = blend_data_bytes(p, band_rows, esz);
+    const long long total = o + stages * data;
+    L.data_bytes = data > INT_MAX ? INT_MAX : static_cast<int>(data);
+    L.total = total > INT_MAX ? INT_MAX : static_cast<int>(total);
+    return L;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+// Grid of a persistent kernel: every resident CTA slot of the GPU, at most
+// one CTA per item.
+template <typename K>
+tdp_status persistent_grid(K kernel, int smem, long long items, unsigned* grid) {
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    const long long slots = (long long)std::max(1, per_sm) * std::max(1, sm_count());
+    *grid = static_cast<unsigned>(std::min(items, slots));
+    return TDP_OK;
 }
 
 template <typename K>
@@ -843,48 +1247,78 @@ tdp_status launch_cluster(K kernel, long long blocks, cudaStream_t stream, Args.
     return cuda_status(cudaLaunchKernelEx(&cfg, kernel, args...));
 }
 
+// Most column tiles that cover any of U adjacent output columns (the fast
+// blend's term count; at most 3 under the guard for U = 2).
+int max_terms(const tdp_plan_t& p, int U) {
+    int best = 1;
+    for (int c = 0; c < p.dims[2]; c += U) {
+        int lo, hi, l2, h2;
+        tdp::axis_cover(p, 2, c, lo, hi);
+        for (int v = 1; v < U && c + v < p.dims[2]; ++v) {
+            tdp::axis_cover(p, 2, c + v, l2, h2);
+            lo = std::min(lo, l2);
+            hi = std::max(hi, h2);
+        }
+        best = std::max(best, hi - lo + 1);
+    }
+    return best;
+}
+
 template <typename Tin, typename Tout>
-tdp_status launch_blend(const tdp_plan_t& p, int BC, const void* tiles, void* out, cudaStream_t stream) {
-    int band_rows = p.dims[1], smem = 0;
+tdp_status launch_blend(const tdp_plan_t& p, int BC, const void* tiles, long long tiles_numel, void* out,
+                        cudaStream_t stream) {
+    int band_rows = p.dims[1];
     BlendLayout L;
     for (;;) {
-        smem = blend_smem(p, band_rows, (int)sizeof(Tin), &L);
-        if (smem <= kBlendSmemBudget || band_rows == 1) break;
+        L = blend_layout(p, band_rows, (int)sizeof(Tin));
+        if (L.total <= kBlendSmemBudget || band_rows == 1) break;
         band_rows = std::max(1, band_rows / 2);
     }
-    if (smem > 200 * 1024) return TDP_ERR_UNSUPPORTED;
+    if (L.total > 200 * 1024) return TDP_ERR_UNSUPPORTED;
     const int nbands = (p.dims[1] + band_rows - 1) / band_rows;
-    const long long blocks = (long long)BC * p.dims[0] * nbands;
-    if (blocks > INT_MAX) return TDP_ERR_INVALID_ARG;
+    const long long items = (long long)BC * p.dims[0] * nbands;
+    if (items > INT_MAX) return TDP_ERR_INVALID_ARG;
     BlendArgs a;
     a.tiles = tiles;
     a.out = out;
+    a.tiles_numel = tiles_numel;
     a.BC = BC;
     a.band_rows = band_rows;
     a.nbands = nbands;
-    a.off_fcov = L.off_fcov;
-    a.off_hcnt = L.off_hcnt;
-    a.off_hcov = L.off_hcov;
-    a.off_wcnt = L.off_wcnt;
-    a.off_wcov = L.off_wcov;
-    a.off_wtile = L.off_wtile;
+    a.n_items = static_cast<int>(items);
+    a.off_a = L.off_a;
+    a.off_b = L.off_b;
+    a.off_c = L.off_c;
+    a.off_d = L.off_d;
+    a.off_e = L.off_e;
     a.off_slotbase = L.off_slotbase;
     a.off_stage = L.off_stage;
     a.off_data = L.off_data;
+    a.max_slots = L.max_slots;
+    a.data_bytes = L.data_bytes;
     a.kf = p.max_cover[0];
     a.kh = p.max_cover[1];
     a.kw = p.max_cover[2];
+    auto launch = [&](auto kernel, bool persistent) -> tdp_status {
+        tdp_status st = set_smem(kernel, L.total);
+        if (st != TDP_OK) return st;
+        unsigned grid = static_cast<unsigned>(items);
+        if (persistent && (st = persistent_grid(kernel, L.total, items, &grid)) != TDP_OK) return st;
+        kernel<<<grid, kThreads, L.total, stream>>>(p, a);
+        return cuda_status(cudaGetLastError());
+    };
     // Pair stores need every output row to start on a 4-byte (bf16) or
     // 8-byte (fp32) boundary: W even.
-    tdp_status st;
-    if (p.dims[2] % 2 == 0) {
-        if ((st = set_smem(blend_kernel<Tin, Tout, 2>, smem)) != TDP_OK) return st;
-        blend_kernel<Tin, Tout, 2><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p, a);
-    } else {
-        if ((st = set_smem(blend_kernel<Tin, Tout, 1>, smem)) != TDP_OK) return st;
-        blend_kernel<Tin, Tout, 1><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p, a);
+    const bool pairs = p.dims[2] % 2 == 0;
+    if (!L.fast) return launch(blend_generic_kernel<Tin, Tout>, false);
+    const int kt = max_terms(p, pairs ? 2 : 1);
+    if (pairs) {
+        if (kt == 1) return launch(blend_fast_kernel<Tin, Tout, 2, 1>, true);
+        if (kt == 2) return launch(blend_fast_kernel<Tin, Tout, 2, 2>, true);
+        return launch(blend_fast_kernel<Tin, Tout, 2, 3>, true);
     }
-    return cuda_status(cudaGetLastError());
+    if (kt == 1) return launch(blend_fast_kernel<Tin, Tout, 1, 1>, true);
+    return launch(blend_fast_kernel<Tin, Tout, 1, 2>, true);
 }
 
 }  // namespace
@@ -900,26 +1334,28 @@ tdp_status tdp_extract(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype d
     if (!latent || !tiles) return TDP_ERR_INVALID_ARG;
     if (!aligned16(latent) || !aligned16(tiles)) return TDP_ERR_ALIGNMENT;
     const tdp_plan_t& p = *plan;
-    int band_rows = p.dims[1], data_off = 0, smem = 0;
+    int band_rows = p.dims[1];
+    ExtractLayout L;
     for (;;) {
-        smem = extract_smem(p, band_rows, esz, &data_off);
-        if (smem <= kExtractSmemBudget || band_rows == 1) break;
+        L = extract_layout(p, band_rows, esz);
+        if (L.total <= kExtractSmemBudget || band_rows == 1) break;
         band_rows = std::max(1, band_rows / 2);
     }
-    if (smem > 200 * 1024) return TDP_ERR_UNSUPPORTED;
+    if (L.total > 200 * 1024) return TDP_ERR_UNSUPPORTED;
     const int nbands = (p.dims[1] + band_rows - 1) / band_rows;
-    const long long blocks = (long long)B * C * p.dims[0] * nbands;
-    if (blocks > INT_MAX || (long long)B * C > INT_MAX) return TDP_ERR_INVALID_ARG;
-    ExtractArgs a{latent, tiles, B * C, band_rows, nbands, data_off};
-    tdp_status st;
-    if (esz == 2) {
-        if ((st = set_smem(extract_kernel<uint16_t>, smem)) != TDP_OK) return st;
-        extract_kernel<uint16_t><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p, a);
-    } else {
-        if ((st = set_smem(extract_kernel<uint32_t>, smem)) != TDP_OK) return st;
-        extract_kernel<uint32_t><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p, a);
-    }
-    return cuda_status(cudaGetLastError());
+    const long long items = (long long)B * C * p.dims[0] * nbands;
+    if (items > INT_MAX || (long long)B * C > INT_MAX) return TDP_ERR_INVALID_ARG;
+    ExtractArgs a{latent, tiles, (long long)B * C * p.dims[0] * p.dims[1] * p.dims[2], B * C, band_rows, nbands,
+                  static_cast<int>(items), L.off_slots, L.off_data, L.stage_bytes};
+    auto launch = [&](auto kernel) -> tdp_status {
+        tdp_status st = set_smem(kernel, L.total);
+        if (st != TDP_OK) return st;
+        unsigned grid = 0;
+        if ((st = persistent_grid(kernel, L.total, items, &grid)) != TDP_OK) return st;
+        kernel<<<grid, kThreads, L.total, stream>>>(p, a);
+        return cuda_status(cudaGetLastError());
+    };
+    return esz == 2 ? launch(extract_kernel<uint16_t>) : launch(extract_kernel<uint32_t>);
 }
 
 tdp_status tdp_blend(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_dtype, const void* tiles,
@@ -931,13 +1367,14 @@ tdp_status tdp_blend(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_
     if (!aligned16(tiles) || !aligned16(out)) return TDP_ERR_ALIGNMENT;
     if ((long long)B * C > INT_MAX) return TDP_ERR_INVALID_ARG;
     const int BC = B * C;
+    const long long n = (long long)BC * tdp::total_volume(*plan);
     if (in_dtype == TDP_BF16 && out_dtype == TDP_BF16)
-        return launch_blend<__nv_bfloat16, __nv_bfloat16>(*plan, BC, tiles, out, stream);
+        return launch_blend<__nv_bfloat16, __nv_bfloat16>(*plan, BC, tiles, n, out, stream);
     if (in_dtype == TDP_BF16 && out_dtype == TDP_F32)
-        return launch_blend<__nv_bfloat16, float>(*plan, BC, tiles, out, stream);
+        return launch_blend<__nv_bfloat16, float>(*plan, BC, tiles, n, out, stream);
     if (in_dtype == TDP_F32 && out_dtype == TDP_BF16)
-        return launch_blend<float, __nv_bfloat16>(*plan, BC, tiles, out, stream);
-    return launch_blend<float, float>(*plan, BC, tiles, out, stream);
+        return launch_blend<float, __nv_bfloat16>(*plan, BC, tiles, n, out, stream);
+    return launch_blend<float, float>(*plan, BC, tiles, n, out, stream);
 }
 
 tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum_out, cudaStream_t stream) {
