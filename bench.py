@@ -237,6 +237,7 @@ def run_tdp(args, rank: int, world: int):
     import torch
     import torch.distributed as dist
     from overlap_add_blending_gb300 import tdp
+    from overlap_add_blending_gb300.replicas import combine
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the tdp path has no CPU fallback)")
@@ -355,11 +356,9 @@ def run_tdp(args, rank: int, world: int):
     torch.cuda.synchronize()
     e2e_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in e2e_evs]))
 
-    if world > 1:
-        t = torch.tensor([step_ms, e2e_ms] + list(per_kernel_ms), dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, e2e_ms = float(t[0]), float(t[1])
-        per_kernel_ms = t[2:].cpu().numpy()
+    # replicas: slowest rank's times, every rank's work
+    mx, job_bytes = combine([step_ms, e2e_ms] + [float(v) for v in per_kernel_ms], ab["total"], device=dev)
+    step_ms, e2e_ms, per_kernel_ms = mx[0], mx[1], np.array(mx[2:])
 
     if rank != 0:
         return 0
@@ -370,7 +369,7 @@ def run_tdp(args, rank: int, world: int):
     dom = "blend" if kern["blend"]["ms"] >= kern["extract"]["ms"] else "extract"
     achieved = kern[dom]["gbs"]
     traffic = recorded_traffic(dom)
-    value = world * ab["total"] / (step_ms * 1e-3) / 1e9
+    value = job_bytes / (step_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -384,7 +383,7 @@ def run_tdp(args, rank: int, world: int):
         "kernels": kern,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src},
-        "e2e": {"value": world * ab["total"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": job_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
         "gpu_launches": KERNELS_PER_STEP * K,
         "clocks": clocks,

@@ -39,7 +39,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kCluster = 8;                  // CTAs cooperating on one tile's token reduction
-constexpr uint64_t kWaitNs = 200ull * 1000 * 1000;  // give up on staged copies after 200 ms
+constexpr uint64_t kWaitNs = 1000ull * 1000 * 1000;  // give up on staged copies after 1 s
 constexpr uint32_t kSuspendHintNs = 20000;           // a polling thread sleeps up to 20 us per try
 constexpr uint32_t kErrExtractWait = 1u;
 constexpr uint32_t kErrBlendWait = 2u;
@@ -123,12 +123,6 @@ __device__ __forceinline__ void load_plan(tdp_plan_t* dst, const tdp_plan_t& src
 }
 
 // ------------------------------------------------------------------ element helpers
-__device__ __forceinline__ float load_f(const float* p, int i) { return p[i]; }
-__device__ __forceinline__ float load_f(const __nv_bfloat16* p, int i) {
-    const uint16_t bits = reinterpret_cast<const uint16_t*>(p)[i];
-    return __uint_as_float(static_cast<uint32_t>(bits) << 16);
-}
-__device__ __forceinline__ uint16_t to_bits(__nv_bfloat16 v) { return __bfloat16_as_ushort(v); }
 
 // 1-D trapezoid of tile i on axis d at coordinate x (x inside the tile):
 // rising ramp min(1, (x-a+1)/(o+1)) except on the first tile, falling ramp
@@ -196,6 +190,40 @@ __device__ __forceinline__ SpanCopy plan_span(const E* base, long long first, in
     c.shift = static_cast<int>((g0 - c.lo) / sizeof(E));
     c.tail0 = hi >= g1 ? len : (hi > g0 ? static_cast<int>((hi - g0) / sizeof(E)) : 0);
     return c;
+}
+
+// ------------------------------------------------------------------ shared loads by address
+// 32-bit shared-window byte addresses keep the hot loops' address math to
+// one add per access.
+__device__ __forceinline__ int lds_s32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+// One staged element as fp32 (bf16 is widened exactly).
+__device__ __forceinline__ float lds_elem(uint32_t addr, const __nv_bfloat16*) {
+    return __uint_as_float(lds_u16(addr) << 16);
+}
+__device__ __forceinline__ float lds_elem(uint32_t addr, const float*) { return lds_f32(addr); }
+// A staged element as fp32, or +0 where the tile does not reach the column:
+// a byte permute of the bf16 bits into the upper half (selector 0x1044) or
+// of zeros (0x4444); fp32 elements use a select.
+__device__ __forceinline__ float lds_masked(uint32_t addr, uint32_t sel, bool, const __nv_bfloat16*) {
+    return __uint_as_float(__byte_perm(lds_u16(addr), 0u, sel));
+}
+__device__ __forceinline__ float lds_masked(uint32_t addr, uint32_t, bool in, const float*) {
+    const float x = lds_f32(addr);
+    return in ? x : 0.0f;
 }
 
 // =================================================================== work split
@@ -418,7 +446,7 @@ struct Cov {
 };
 
 struct Combo {          // one (frame tile, row tile) pair covering a band row
-    int slot0;          // slot index of its column tile 0
+    int slot0b;         // byte offset of its column tile 0's entry in the run-base table
     float w;            // r_f * r_h, rounded
 };
 
@@ -504,7 +532,7 @@ __device__ void blend_build_stage_table(const tdp_plan_t& p, const BlendArgs& a,
 // Warp 0: stage item (box table, b*C + c) into a stage: arm its barrier
 // with the bulk bytes, issue one bulk copy per run (plain loads for a run
 // ending in the buffer's last partial 16 bytes) and record, per run, the
-// shared element index of (its row 0, column 0).
+// byte offset in the stage of (its row 0, column 0).
 template <typename Tin>
 __device__ void blend_stage_item(const Tin* tiles, uintptr_t limit, const StageSlot* table, int nslots, int bc,
                                  int* slotbase, unsigned char* data, uint64_t* bar) {
@@ -526,7 +554,7 @@ __device__ void blend_stage_item(const Tin* tiles, uintptr_t limit, const StageS
         if (cp.bulk) bulk_copy_g2s(data + st.smem_off, reinterpret_cast<const void*>(cp.lo), cp.bulk, bar);
         Tin* dst = reinterpret_cast<Tin*>(data + st.smem_off) + cp.shift;
         for (int e = cp.tail0; e < st.len; ++e) dst[e] = tiles[src + e];
-        slotbase[s] = st.smem_off / (int)sizeof(Tin) + cp.shift - st.r0sw;
+        slotbase[s] = st.smem_off + (cp.shift - st.r0sw) * (int)sizeof(Tin);   // bytes
     }
 }
 
@@ -541,6 +569,7 @@ struct Terms {
     int iw[KT], xo[KT], sw[KT];
     float w[KT][U];
     bool in[KT][U];
+    uint32_t sel[KT][U];   // byte-permute selector: bf16 -> fp32 bits, or +0 where the tile does not reach
 };
 
 template <int U, int KT>
@@ -568,15 +597,12 @@ __device__ __forceinline__ void load_terms(const tdp_plan_t& p, int c, int W, Te
         for (int v = 0; v < U; ++v) {
             const bool in = real && c + v >= w0 && c + v < w1;
             t.in[q][v] = in;
+            t.sel[q][v] = in ? 0x1044u : 0x4444u;
             t.w[q][v] = in ? axis_weight(p, 2, i, c + v) : 0.0f;
         }
     }
 }
 
-__device__ __forceinline__ float load_elem(const __nv_bfloat16* d, int i) {
-    return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(d)[i]) << 16);
-}
-__device__ __forceinline__ float load_elem(const float* d, int i) { return d[i]; }
 
 template <int U>
 __device__ __forceinline__ void store_cols(float* out, long long i, const float (&v)[U]) {
@@ -626,7 +652,6 @@ __global__ void __launch_bounds__(kThreads, 3) blend_fast_kernel(const __grid_co
     const int F = p.dims[0], H = p.dims[1], W = p.dims[2], nw = p.num_tiles[2];
     const int KC = a.kf * a.kh;
     const int max_slots = a.max_slots;
-    const int data_elems = a.data_bytes / static_cast<int>(sizeof(Tin));
     const uintptr_t limit = reinterpret_cast<uintptr_t>(tiles + a.tiles_numel) & ~uintptr_t(15);
 
     int first, last;
@@ -691,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 3) blend_fast_kernel(const __grid_co
                     const float wf = axis_weight(p, 0, c.if_lo + fa, c.f);
                     for (int ih = lo; ih <= hi; ++ih)
                         combo[r * KC + n++] =
-                            Combo{(fa * c.NH + ih - c.ih_lo) * nw, __fmul_rn(wf, axis_weight(p, 1, ih, h))};
+                            Combo{4 * (fa * c.NH + ih - c.ih_lo) * nw, __fmul_rn(wf, axis_weight(p, 1, ih, h))};
                 }
                 ncombo[r] = n;
             }
@@ -705,40 +730,58 @@ __global__ void __launch_bounds__(kThreads, 3) blend_fast_kernel(const __grid_co
             }
             return;
         }
-        const Tin* sdata = reinterpret_cast<const Tin*>(data0) + s * data_elems;
-        const int* sbase = slotbase0 + s * max_slots;
+        const uint32_t sdata = smem_u32(data0) + s * a.data_bytes;
+        const uint32_t sbase = smem_u32(slotbase0 + s * max_slots);
+        constexpr int esz = static_cast<int>(sizeof(Tin));
         const long long out0 = ((long long)cur.bc * F + c.f) * H * W + (long long)c.hb0 * W;
         for (int m = 0; m < ncu_mine; ++m) {
             const int cu = cu0 + m * per_row;
             if (ncu_mine > 1) load_terms<U, KT>(p, cu * U, W, tm);
-            int rowoff[KT];
+            // per term: byte offsets of the column pair in its tile row, of one
+            // row step, and of the term's entry in the run-base table
+            int rowb[KT], stepb[KT], iwb[KT];
 #pragma unroll
-            for (int q = 0; q < KT; ++q) rowoff[q] = (c.hb0 + rg) * tm.sw[q] + tm.xo[q];
+            for (int q = 0; q < KT; ++q) {
+                rowb[q] = ((c.hb0 + rg) * tm.sw[q] + tm.xo[q]) * esz;
+                stepb[q] = RG * tm.sw[q] * esz;
+                iwb[q] = 4 * tm.iw[q];
+            }
+            Tout* dst = out + out0 + (long long)rg * W + cu * U;
+            const long long dstep = (long long)RG * W;
+            uint32_t nca = smem_u32(ncombo) + 4 * rg;
+            uint32_t cba = smem_u32(combo) + 8 * KC * rg;
+            const uint32_t nca_step = 4 * RG, cba_step = 8 * KC * RG;
             for (int r = rg; r < c.rows; r += RG) {
                 float acc[U];
 #pragma unroll
                 for (int v = 0; v < U; ++v) acc[v] = 0.0f;
-                const int nc = ncombo[r];
-                for (int kk = 0; kk < nc; ++kk) {
-                    const Combo cb = combo[r * KC + kk];
+                const int nc = lds_s32(nca);
+                uint32_t ca = cba;
+                for (int kk = 0; kk < nc; ++kk, ca += 8) {
+                    const int slot0b = lds_s32(ca);
+                    const float wfh = lds_f32(ca + 4);
                     float inner[U];
 #pragma unroll
                     for (int v = 0; v < U; ++v) inner[v] = 0.0f;
 #pragma unroll
                     for (int q = 0; q < KT; ++q) {
-                        const int i = sbase[cb.slot0 + tm.iw[q]] + rowoff[q];
+                        const uint32_t ea = sdata + lds_s32(sbase + slot0b + iwb[q]) + rowb[q];
 #pragma unroll
                         for (int v = 0; v < U; ++v) {
-                            const float x = load_elem(sdata, i + v);
-                            inner[v] = fmaf(tm.w[q][v], tm.in[q][v] ? x : 0.0f, inner[v]);
+                            const float x = lds_masked(ea + v * esz, tm.sel[q][v], tm.in[q][v],
+                                                       static_cast<const Tin*>(nullptr));
+                            inner[v] = fmaf(tm.w[q][v], x, inner[v]);
                         }
                     }
 #pragma unroll
-                    for (int v = 0; v < U; ++v) acc[v] = fmaf(cb.w, inner[v], acc[v]);
+                    for (int v = 0; v < U; ++v) acc[v] = fmaf(wfh, inner[v], acc[v]);
                 }
-                store_cols<U>(out, out0 + (long long)r * W + cu * U, acc);
+                store_cols<U>(dst, 0, acc);
+                dst += dstep;
+                nca += nca_step;
+                cba += cba_step;
 #pragma unroll
-                for (int q = 0; q < KT; ++q) rowoff[q] += RG * tm.sw[q];
+                for (int q = 0; q < KT; ++q) rowb[q] += stepb[q];
             }
         }
         __syncthreads();  // stage s, its slot bases and the row table are free again
@@ -801,7 +844,7 @@ __global__ void __launch_bounds__(kThreads) blend_generic_kernel(const __grid_co
         return;
     }
 
-    const Tin* sdata = reinterpret_cast<const Tin*>(data);
+    const uint32_t sdata = smem_u32(data);
     const long long out0 = ((long long)bc * F + c.f) * H * W + (long long)c.hb0 * W;
     for (int it = threadIdx.x; it < c.rows * W; it += blockDim.x) {
         const int r = it / W, col = it - r * W, h = c.hb0 + r;
@@ -815,8 +858,9 @@ __global__ void __launch_bounds__(kThreads) blend_generic_kernel(const __grid_co
                 float inner = 0.0f;
                 for (int q = 0; q < wcnt[col]; ++q) {
                     const Cov wq = wcov[col * a.kw + q];
-                    const int idx = slotbase[sb + wq.i] + h * tdp::tile_size(p, 2, wq.i) + (col - p.start[2][wq.i]);
-                    inner = fmaf(wq.w, load_elem(sdata, idx), inner);
+                    const int off = slotbase[sb + wq.i] +
+                                    (h * tdp::tile_size(p, 2, wq.i) + (col - p.start[2][wq.i])) * (int)sizeof(Tin);
+                    inner = fmaf(wq.w, lds_elem(sdata + off, static_cast<const Tin*>(nullptr)), inner);
                 }
                 acc = fmaf(wfh, inner, acc);
             }
