@@ -4,10 +4,13 @@
 One step is one pass of every step of the path on the 4K-class workload
 (bf16 latent B=1, C=128, F=16, H=68, W=120; tiles 2x4x4 with overlaps
 2/8/12; 256 conditioning tokens, 64 with a negative time start):
-    tdp_extract -> tdp_positions -> tdp_cond_select -> tdp_blend -> tdp_window_sum
-(the per-tile op between extract and blend is the caller's; here identity,
+    tdp_extract, then tdp_blend concurrently with tdp_positions ->
+    tdp_cond_select -> tdp_window_sum on a second stream (they are
+    independent of extract and blend); the step ends when both are done.
+The per-tile op between extract and blend is the caller's (here identity,
 outside the path).  Inputs are resident in HBM when the timed region starts;
-L2 is flushed (a 256 MiB write) before every step and before the blend.
+L2 is flushed (a 256 MiB write) before every step and before the blend,
+outside the timed spans.
 
 Headline: algorithmic extract+blend bytes per step / step time (GB/s):
     latent read + tile write (extract) + tile read + latent write (blend).
@@ -62,7 +65,8 @@ def config_dict(wl, note: str) -> dict:
                         f"W={wl.dims[2]}, tiles (frames {wl.tiling[0][0]}/{wl.tiling[0][1]}, height "
                         f"{wl.tiling[1][0]}/{wl.tiling[1][1]}, width {wl.tiling[2][0]}/{wl.tiling[2][1]}), "
                         f"{wl.num_cond} conditioning tokens ({wl.num_cond_negative} with negative time)",
-            "step": "extract + positions + cond_select + blend + window_sum (per-tile op: identity, outside)",
+            "step": "extract, then blend || (positions, cond_select, window_sum on a second stream); "
+                    "per-tile op: identity, outside",
             "l2": note}
 
 
@@ -271,23 +275,33 @@ def run_tdp(args, rank: int, world: int):
         tdp.blend(p, tiles, wl.B, wl.C, out)
         tdp.window_sum(p, maxdev)
 
-    # Events bracket each kernel of the step, on the launching stream.  L2 is
-    # flushed before the step and again before the blend (outside the
-    # events): in use, the per-tile model runs between extract and blend.
-    def timed_step(ev):
+    # One step: extract, then the blend on the main stream while positions,
+    # conditioning selection and the window sum (independent of extract and
+    # blend) run on a side stream; the step ends when both are done.  Events bracket every
+    # kernel on the stream it is launched on.  L2 is flushed before the step
+    # and again before the blend, outside the timed spans: in use, the
+    # per-tile model runs between extract and blend.
+    side = torch.cuda.Stream(device=dev, priority=-1)   # short latency-bound kernels first
+
+    def timed_step(ev, es):
         ev[0].record(stream)
         tdp.extract(p, X, tiles)
         ev[1].record(stream)
-        tdp.positions(p, gen, True, tile_pos, offsets)
-        ev[2].record(stream)
-        tdp.cond_select(p, gen, cond, True, True, cond_out)
-        ev[3].record(stream)
         flush.zero_()
-        ev[4].record(stream)
+        ev[2].record(stream)
+        side.wait_event(ev[2])
+        with torch.cuda.stream(side):
+            es[0].record(side)
+            tdp.positions(p, gen, True, tile_pos, offsets, stream=side)
+            es[1].record(side)
+            tdp.cond_select(p, gen, cond, True, True, cond_out, stream=side)
+            es[2].record(side)
+            tdp.window_sum(p, maxdev, stream=side)
+            es[3].record(side)
         tdp.blend(p, tiles, wl.B, wl.C, out)
-        ev[5].record(stream)
-        tdp.window_sum(p, maxdev)
-        ev[6].record(stream)
+        ev[3].record(stream)
+        stream.wait_event(es[3])
+        ev[4].record(stream)
 
     # host enqueue time of one step, to size the head start given to the host
     path()
@@ -312,12 +326,13 @@ def run_tdp(args, rank: int, world: int):
     torch.cuda.synchronize()
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    ess = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     wall0 = time.perf_counter()
     for k in range(K):
         flush.zero_()
         torch.cuda._sleep(sleep_cycles)      # the host enqueues the whole step meanwhile
-        timed_step(evs[k])
+        timed_step(evs[k], ess[k])
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if world > 1:
@@ -325,9 +340,12 @@ def run_tdp(args, rank: int, world: int):
     torch.cuda.synchronize()
     clocks = sampler.stop()
 
-    pairs = ((0, 1), (1, 2), (2, 3), (4, 5), (5, 6))
-    seg = np.array([[evs[k][i].elapsed_time(evs[k][j]) for i, j in pairs] for k in range(K)])  # ms
-    step_ms = float(seg.sum(axis=1).mean())
+    # step = extract + fork .. join (blend || side stream)
+    step = np.array([evs[k][0].elapsed_time(evs[k][1]) + evs[k][2].elapsed_time(evs[k][4]) for k in range(K)])
+    seg = np.array([[evs[k][0].elapsed_time(evs[k][1]), ess[k][0].elapsed_time(ess[k][1]),
+                     ess[k][1].elapsed_time(ess[k][2]), evs[k][2].elapsed_time(evs[k][3]),
+                     ess[k][2].elapsed_time(ess[k][3])] for k in range(K)])  # ms
+    step_ms = float(step.mean())
     per_kernel_ms = seg.mean(axis=0)
     names = ["extract", "positions", "cond_select", "blend", "window_sum"]
 

@@ -871,12 +871,43 @@ __global__ void __launch_bounds__(kThreads) blend_generic_kernel(const __grid_co
 }
 
 // =================================================================== K3: window sum
-__global__ void __launch_bounds__(kThreads, 1) window_sum_kernel(const __grid_constant__ tdp_plan_t pg,
-                                                              float* max_abs_dev, float* sum_out) {
-    __shared__ tdp_plan_t p;
-    load_plan(&p, pg);
-    __syncthreads();
+// S(f,h,w) = sum over (frame tile, row tile) pairs of fma(r_f * r_h, inner(w), S)
+// with inner(w) = sum over column tiles of r_w: the blend kernels' weights
+// and grouping applied to tiles of ones, so S equals that blend bit for bit.
+// With `tables`, each CTA first tabulates r_f and r_h per covering tile and
+// inner(w) per column in shared memory (kf, kh: most tiles covering an index).
+__global__ void __launch_bounds__(kThreads) window_sum_kernel(const __grid_constant__ tdp_plan_t p, float* max_abs_dev,
+                                                              float* sum_out, int tables) {
+    extern __shared__ __align__(16) unsigned char wsm[];
     const int F = p.dims[0], H = p.dims[1], W = p.dims[2];
+    const int kf = p.max_cover[0], kh = p.max_cover[1];
+    float* wf = reinterpret_cast<float*>(wsm);          // [F][kf]
+    float* wh = wf + F * kf;                             // [H][kh]
+    float* winner = wh + H * kh;                         // [W]
+    int* fcnt = reinterpret_cast<int*>(winner + W);      // [F] covering frame tiles
+    int* hcnt = fcnt + F;                                // [H]
+    if (tables) {
+        for (int f = threadIdx.x; f < F; f += blockDim.x) {
+            int lo, hi;
+            tdp::axis_cover(p, 0, f, lo, hi);
+            fcnt[f] = hi - lo + 1;
+            for (int i = lo; i <= hi; ++i) wf[f * kf + (i - lo)] = axis_weight(p, 0, i, f);
+        }
+        for (int h = threadIdx.x; h < H; h += blockDim.x) {
+            int lo, hi;
+            tdp::axis_cover(p, 1, h, lo, hi);
+            hcnt[h] = hi - lo + 1;
+            for (int i = lo; i <= hi; ++i) wh[h * kh + (i - lo)] = axis_weight(p, 1, i, h);
+        }
+        for (int w = threadIdx.x; w < W; w += blockDim.x) {
+            int lo, hi;
+            tdp::axis_cover(p, 2, w, lo, hi);
+            float inner = 0.0f;
+            for (int k = lo; k <= hi; ++k) inner = fmaf(axis_weight(p, 2, k, w), 1.0f, inner);
+            winner[w] = inner;
+        }
+        __syncthreads();
+    }
     const long long N = (long long)F * H * W;
     float worst = 0.0f;
     for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < N;
@@ -884,21 +915,23 @@ __global__ void __launch_bounds__(kThreads, 1) window_sum_kernel(const __grid_co
         const int w = static_cast<int>(idx % W);
         const long long fh = idx / W;
         const int h = static_cast<int>(fh % H), f = static_cast<int>(fh / H);
-        int f0, f1, h0, h1, w0, w1;
-        tdp::axis_cover(p, 0, f, f0, f1);
-        tdp::axis_cover(p, 1, h, h0, h1);
-        tdp::axis_cover(p, 2, w, w0, w1);
-        // Same weights and grouping as the blend kernels applied to tiles of
-        // ones: per (frame tile, row tile) pair, inner = sum of r_w over the
-        // column tiles, then S = fma(r_f * r_h, inner, S).
         float S = 0.0f;
-        for (int i = f0; i <= f1; ++i) {
-            const float wf = axis_weight(p, 0, i, f);
-            for (int j = h0; j <= h1; ++j) {
-                const float wfh = __fmul_rn(wf, axis_weight(p, 1, j, h));
-                float inner = 0.0f;
-                for (int k = w0; k <= w1; ++k) inner = fmaf(axis_weight(p, 2, k, w), 1.0f, inner);
-                S = fmaf(wfh, inner, S);
+        if (tables) {
+            const float in_w = winner[w];
+            for (int i = 0; i < fcnt[f]; ++i) {
+                const float a_f = wf[f * kf + i];
+                for (int j = 0; j < hcnt[h]; ++j) S = fmaf(__fmul_rn(a_f, wh[h * kh + j]), in_w, S);
+            }
+        } else {
+            int f0, f1, h0, h1, w0, w1;
+            tdp::axis_cover(p, 0, f, f0, f1);
+            tdp::axis_cover(p, 1, h, h0, h1);
+            tdp::axis_cover(p, 2, w, w0, w1);
+            float inner = 0.0f;
+            for (int k = w0; k <= w1; ++k) inner = fmaf(axis_weight(p, 2, k, w), 1.0f, inner);
+            for (int i = f0; i <= f1; ++i) {
+                const float a_f = axis_weight(p, 0, i, f);
+                for (int j = h0; j <= h1; ++j) S = fmaf(__fmul_rn(a_f, axis_weight(p, 1, j, h)), inner, S);
             }
         }
         if (sum_out) sum_out[idx] = S;
@@ -906,8 +939,16 @@ __global__ void __launch_bounds__(kThreads, 1) window_sum_kernel(const __grid_co
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) worst = fmaxf(worst, __shfl_xor_sync(0xffffffffu, worst, o));
-    // Non-negative floats order like their bit patterns.
-    if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned int*>(max_abs_dev), __float_as_uint(worst));
+    // Block maximum, then one atomic per block into the pre-zeroed result
+    // (non-negative floats order like their bit patterns).
+    __shared__ float warp_worst[kThreads / 32];
+    if ((threadIdx.x & 31) == 0) warp_worst[threadIdx.x >> 5] = worst;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float m = 0.0f;
+        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) m = fmaxf(m, warp_worst[i]);
+        atomicMax(reinterpret_cast<unsigned int*>(max_abs_dev), __float_as_uint(m));
+    }
 }
 
 // =================================================================== K4 / K5: tokens
@@ -1007,34 +1048,93 @@ struct PositionsArgs {
     int normalize;
 };
 
-__global__ void __launch_bounds__(kThreads) positions_kernel(const __grid_constant__ tdp_plan_t pg,
+constexpr int kPosCache = 4;   // tokens per thread kept in registers between reduce and write
+
+// One 8-CTA cluster per (tile, batch).  Each CTA reads its chunk of the
+// tile's generated tokens once, keeping them in registers (up to kPosCache
+// per thread); the chunk minima meet through distributed shared memory; the
+// CTA then writes its chunk shifted by the tile's per-axis minimum start.
+// Chunks longer than the register cache are read a second time.  Every plan
+// read here is uniform across the CTA, so the plan stays a parameter.
+__global__ void __launch_bounds__(kThreads) positions_kernel(const __grid_constant__ tdp_plan_t p,
                                                              const PositionsArgs a) {
-    __shared__ tdp_plan_t p;
-    load_plan(&p, pg);
-    __syncthreads();
     __shared__ int ext_sh[6];
     cg::cluster_group cluster = cg::this_cluster();
     const int tb = blockIdx.x / kCluster;
     const int t = tb / a.B, b = tb % a.B;
     const long long N = (long long)p.dims[0] * p.dims[1] * p.dims[2];
     const TileTokens tt = tile_tokens(p, t);
-    int ext[6];
-    tile_extent_cluster(p, tt, a.gen, b, N, ext_sh, ext);
-    cluster.sync();  // every CTA has read its peers' partials
     const int rank = static_cast<int>(cluster.block_rank());
-    if (rank == 0 && threadIdx.x < 3) a.offsets[((long long)t * a.B + b) * 3 + threadIdx.x] = ext[2 * threadIdx.x];
     const int chunk = (tt.n + kCluster - 1) / kCluster;
     const int j0 = rank * chunk, j1 = min(tt.n, j0 + chunk);
-    int* dst = a.tile_pos + tt.prefix * 6 * a.B;
-    for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
-        const long long n = global_token(p, tt, j);
+    const int* gen_b = a.gen + (long long)b * 3 * N * 2;
+    const bool cached = chunk <= kPosCache * static_cast<int>(blockDim.x);
+    int2 v[kPosCache][3];
+    int mn[3] = {INT_MAX, INT_MAX, INT_MAX};
+    if (threadIdx.x < 6) ext_sh[threadIdx.x] = (threadIdx.x & 1) ? INT_MIN : INT_MAX;
+    if (cached) {
 #pragma unroll
-        for (int d = 0; d < 3; ++d) {
-            int2 v = *reinterpret_cast<const int2*>(a.gen + (((long long)b * 3 + d) * N + n) * 2);
-            if (a.normalize) { v.x -= ext[2 * d]; v.y -= ext[2 * d]; }
-            *reinterpret_cast<int2*>(dst + (((long long)b * 3 + d) * tt.n + j) * 2) = v;
+        for (int k = 0; k < kPosCache; ++k) {
+            const int j = j0 + static_cast<int>(threadIdx.x) + k * static_cast<int>(blockDim.x);
+            if (j < j1) {
+                const long long n = global_token(p, tt, j);
+#pragma unroll
+                for (int d = 0; d < 3; ++d) {
+                    v[k][d] = *reinterpret_cast<const int2*>(gen_b + ((long long)d * N + n) * 2);
+                    mn[d] = min(mn[d], v[k][d].x);
+                }
+            }
+        }
+    } else {
+        for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+            const long long n = global_token(p, tt, j);
+#pragma unroll
+            for (int d = 0; d < 3; ++d) mn[d] = min(mn[d], gen_b[((long long)d * N + n) * 2]);
         }
     }
+#pragma unroll
+    for (int d = 0; d < 3; ++d) mn[d] = warp_min(mn[d]);
+    __syncthreads();  // ext_sh initialised
+    if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+        for (int d = 0; d < 3; ++d) atomicMin(&ext_sh[2 * d], mn[d]);
+    }
+    cluster.sync();
+    int off[3] = {INT_MAX, INT_MAX, INT_MAX};
+    for (int r = 0; r < kCluster; ++r) {
+        const int* peer = cluster.map_shared_rank(ext_sh, r);
+#pragma unroll
+        for (int d = 0; d < 3; ++d) off[d] = min(off[d], peer[2 * d]);
+    }
+    // Arrive now (this CTA is done reading its peers), wait at the end: the
+    // barrier's latency overlaps the writes, and no CTA leaves while a peer
+    // may still read its minima.
+    cluster.barrier_arrive();
+    if (rank == 0 && threadIdx.x < 3) a.offsets[((long long)t * a.B + b) * 3 + threadIdx.x] = off[threadIdx.x];
+    if (!a.normalize) off[0] = off[1] = off[2] = 0;
+    int* dst = a.tile_pos + tt.prefix * 6 * a.B + (long long)b * 3 * tt.n * 2;
+    if (cached) {
+#pragma unroll
+        for (int k = 0; k < kPosCache; ++k) {
+            const int j = j0 + static_cast<int>(threadIdx.x) + k * static_cast<int>(blockDim.x);
+            if (j < j1) {
+#pragma unroll
+                for (int d = 0; d < 3; ++d)
+                    *reinterpret_cast<int2*>(dst + ((long long)d * tt.n + j) * 2) =
+                        make_int2(v[k][d].x - off[d], v[k][d].y - off[d]);
+            }
+        }
+    } else {
+        for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+            const long long n = global_token(p, tt, j);
+#pragma unroll
+            for (int d = 0; d < 3; ++d) {
+                const int2 x = *reinterpret_cast<const int2*>(gen_b + ((long long)d * N + n) * 2);
+                *reinterpret_cast<int2*>(dst + ((long long)d * tt.n + j) * 2) = make_int2(x.x - off[d], x.y - off[d]);
+            }
+        }
+    }
+    cluster.barrier_wait();
 }
 
 struct CondArgs {
@@ -1060,10 +1160,7 @@ __device__ __forceinline__ bool cond_keep(const int* cond, int b, int M, int m, 
     return ok;
 }
 
-__global__ void __launch_bounds__(kThreads) cond_kernel(const __grid_constant__ tdp_plan_t pg, const CondArgs a) {
-    __shared__ tdp_plan_t p;
-    load_plan(&p, pg);
-    __syncthreads();
+__global__ void __launch_bounds__(kThreads) cond_kernel(const __grid_constant__ tdp_plan_t p, const CondArgs a) {
     __shared__ int ext_sh[6];
     __shared__ int scan_sh[33];
     __shared__ int kept_sh;
@@ -1097,6 +1194,7 @@ __global__ void __launch_bounds__(kThreads) cond_kernel(const __grid_constant__ 
         if (r < rank) before += c;
         total += c;
     }
+    cluster.barrier_arrive();  // done reading peers; the matching wait ends the kernel
     // Pass 2: compacted indices and shifted positions, original order.
     if (a.kept_idx || a.tile_cond) {
         int base = before;
@@ -1132,7 +1230,7 @@ __global__ void __launch_bounds__(kThreads) cond_kernel(const __grid_constant__ 
         }
     }
     if (rank == 0 && threadIdx.x == 0 && a.num_kept) a.num_kept[row] = total;
-    cluster.sync();  // peers finished reading kept_sh
+    cluster.barrier_wait();  // peers finished reading kept_sh
 }
 
 __global__ void __launch_bounds__(kThreads) cond_count_kernel(const unsigned char* keep, int T, int BM,
@@ -1424,11 +1522,16 @@ tdp_status tdp_blend(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_
 tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum_out, cudaStream_t stream) {
     if (!tdp::plan_is_valid(plan) || !max_abs_dev) return TDP_ERR_INVALID_ARG;
     if (!aligned16(max_abs_dev) || (sum_out && !aligned16(sum_out))) return TDP_ERR_ALIGNMENT;
+    const tdp_plan_t& p = *plan;
+    const long long N = (long long)p.dims[0] * p.dims[1] * p.dims[2];
+    const long long tab = 4LL * ((long long)p.dims[0] * p.max_cover[0] + (long long)p.dims[1] * p.max_cover[1] +
+                                 p.dims[2] + p.dims[0] + p.dims[1]);
+    const int tables = tab <= 32 * 1024 ? 1 : 0;
+    const int smem = tables ? static_cast<int>(tab) : 0;
     tdp_status st = cuda_status(cudaMemsetAsync(max_abs_dev, 0, sizeof(float), stream));
     if (st != TDP_OK) return st;
-    const long long N = (long long)plan->dims[0] * plan->dims[1] * plan->dims[2];
-    const long long blocks = std::min<long long>((N + kThreads - 1) / kThreads, 152LL * 8);
-    window_sum_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(*plan, max_abs_dev, sum_out);
+    const long long blocks = std::min<long long>((N + 4LL * kThreads - 1) / (4LL * kThreads), 2LL * std::max(1, sm_count()));
+    window_sum_kernel<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p, max_abs_dev, sum_out, tables);
     return cuda_status(cudaGetLastError());
 }
 
