@@ -43,8 +43,12 @@ constexpr uint64_t kWaitNs = 1000ull * 1000 * 1000;  // give up on staged copies
 constexpr uint32_t kSuspendHintNs = 20000;           // a polling thread sleeps up to 20 us per try
 constexpr uint32_t kErrExtractWait = 1u;
 constexpr uint32_t kErrBlendWait = 2u;
-constexpr int kExtractSmemBudget = 64 * 1024;   // two staged bands + slot table
-constexpr int kBlendSmemBudget = 72 * 1024;     // two stages of tile rows + tables
+constexpr int kExtractStages = 4;               // staged bands per extract CTA (3 in flight)
+constexpr int kExtractSmemBudget = 64 * 1024;   // staged bands + slot table
+constexpr int kBlendSmemBudget = 64 * 1024;     // ring of staged tile rows + tables (3 CTAs per SM)
+constexpr int kBlendQueue = 4;                  // blend items staged ahead at most
+constexpr int kBlendConsumers = 256;            // blend threads that compute (8 warps)
+constexpr int kBlendThreads = kBlendConsumers + 32;   // + one producer warp
 
 __device__ unsigned int g_device_error = 0;
 
@@ -65,6 +69,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
@@ -341,11 +350,11 @@ __device__ __forceinline__ void extract_copy_slot_warp(E* __restrict__ dst, cons
 }
 
 // Persistent: each CTA walks its item range; an item is one (frame, row
-// band, b, c) box of the latent, staged as one contiguous span.  Two
-// shared-memory stages: thread 0 issues the next item's bulk copy before
-// the current one is written out.
+// band, b, c) box of the latent, staged as one contiguous span.  A ring of
+// `stages` shared-memory stages: thread 0 keeps the next stages - 1 items'
+// bulk copies in flight while the CTA writes out the current one.
 template <typename E>
-__global__ void __launch_bounds__(kThreads) extract_kernel(const __grid_constant__ tdp_plan_t pg,
+__global__ void __launch_bounds__(kThreads, 5) extract_kernel(const __grid_constant__ tdp_plan_t pg,
                                                            const ExtractArgs a) {
     __shared__ tdp_plan_t p;
     load_plan(&p, pg);
@@ -355,6 +364,7 @@ __global__ void __launch_bounds__(kThreads) extract_kernel(const __grid_constant
     ExtractSlot* slots = reinterpret_cast<ExtractSlot*>(smem + a.off_slots);
     E* stage0 = reinterpret_cast<E*>(smem + a.off_data);
     const int stage_elems = a.stage_bytes / static_cast<int>(sizeof(E));
+    constexpr int S = kExtractStages;
     const E* latent = static_cast<const E*>(a.latent);
     E* tiles = static_cast<E*>(a.tiles);
     const int F = p.dims[0], H = p.dims[1], W = p.dims[2], nw = p.num_tiles[2];
@@ -378,19 +388,20 @@ __global__ void __launch_bounds__(kThreads) extract_kernel(const __grid_constant
         for (int e = cp.tail0; e < len; ++e) band[cp.shift + e] = latent[span0 + e];
     };
     if (threadIdx.x == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        issue(0);
-        ahead.next();
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        for (int s = 0; s < S - 1 && first + s < last; ++s) {
+            issue(s);
+            ahead.next();
+        }
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
     ItemCursor cur;
     cur.init(first, a.BC);
     int cached_fb = -1, nslots = 0, band_len = 0, f = 0, hb0 = 0;
-    for (int k = 0, item = first; item < last; ++k, ++item, cur.next()) {
-        const int s = k & 1;
-        if (threadIdx.x == 0 && item + 1 < last) {
-            issue(s ^ 1);
+    for (int k = 0, item = first, s = 0; item < last; ++k, ++item, cur.next(), s = (s + 1 == S ? 0 : s + 1)) {
+        // stage (k - 1) mod S was freed by the barrier ending item k - 1
+        if (threadIdx.x == 0 && item + S - 1 < last) {
+            issue(s == 0 ? S - 1 : s - 1);
             ahead.next();
         }
         if (cur.fb != cached_fb) {
@@ -422,11 +433,10 @@ __global__ void __launch_bounds__(kThreads) extract_kernel(const __grid_constant
         }
         const long long span0 = ((long long)cur.bc * F + f) * H * W + (long long)hb0 * W;
         const int shift = plan_span(latent, span0, band_len, limit).shift;
-        if (!cta_wait(&bar[s], (k >> 1) & 1)) {
-            if (threadIdx.x == 0) {
+        if (!cta_wait(&bar[s], (k / S) & 1)) {
+            if (threadIdx.x == 0) {  // let every issued copy land before the CTA exits
                 atomicOr(&g_device_error, kErrExtractWait);
-                mbar_wait_bounded(&bar[s], (k >> 1) & 1);
-                if (item + 1 < last) mbar_wait_bounded(&bar[s ^ 1], ((k + 1) >> 1) & 1);
+                for (int j = k; j < k + S && first + j < last; ++j) mbar_wait_bounded(&bar[j % S], (j / S) & 1);
             }
             return;
         }
@@ -443,11 +453,6 @@ __global__ void __launch_bounds__(kThreads) extract_kernel(const __grid_constant
 struct Cov {
     int i;
     float w;
-};
-
-struct Combo {          // one (frame tile, row tile) pair covering a band row
-    int slot0b;         // byte offset of its column tile 0's entry in the run-base table
-    float w;            // r_f * r_h, rounded
 };
 
 struct StageSlot {      // one run of tile rows of a (frame, band) box
@@ -499,8 +504,8 @@ __device__ __forceinline__ BlendBox blend_box(const tdp_plan_t& p, const BlendAr
 // frame tile, row tile meeting the band, column tile) -- and their layout
 // in a stage's data region (exclusive scan of padded sizes).
 template <typename Tin>
-__device__ void blend_build_stage_table(const tdp_plan_t& p, const BlendArgs& a, const BlendBox& c,
-                                        StageSlot* table) {
+__device__ int blend_build_stage_table(const tdp_plan_t& p, const BlendArgs& a, const BlendBox& c,
+                                       StageSlot* table) {
     const int lane = threadIdx.x & 31, nw = p.num_tiles[2];
     int carry = 0;
     for (int s0 = 0; s0 < c.nslots; s0 += 32) {
@@ -527,34 +532,41 @@ __device__ void blend_build_stage_table(const tdp_plan_t& p, const BlendArgs& a,
         carry += __shfl_sync(0xffffffffu, incl, 31);
     }
     __syncwarp();
+    return carry;   // bytes of one staged item
 }
 
-// Warp 0: stage item (box table, b*C + c) into a stage: arm its barrier
-// with the bulk bytes, issue one bulk copy per run (plain loads for a run
-// ending in the buffer's last partial 16 bytes) and record, per run, the
-// byte offset in the stage of (its row 0, column 0).
+// One warp: stage item (box table, b*C + c) at byte `pos` of the data
+// region.  First the plain writes -- per run, the byte offset in the data
+// region of (its row 0, column 0), and plain loads for a run ending in the
+// buffer's last partial 16 bytes -- then the barrier is armed with the bulk
+// bytes (its release covers those writes) and one bulk copy per run is
+// issued.
 template <typename Tin>
 __device__ void blend_stage_item(const Tin* tiles, uintptr_t limit, const StageSlot* table, int nslots, int bc,
-                                 int* slotbase, unsigned char* data, uint64_t* bar) {
+                                 int* slotbase, unsigned char* data, int pos, uint64_t* bar) {
     const int lane = threadIdx.x & 31;
     uint32_t bytes = 0;
     for (int s = lane; s < nslots; s += 32) {
         const StageSlot st = table[s];
-        bytes += plan_span(tiles, st.src0 + (long long)bc * st.vol, st.len, limit).bulk;
+        const long long src = st.src0 + (long long)bc * st.vol;
+        const SpanCopy cp = plan_span(tiles, src, st.len, limit);
+        const int off = pos + st.smem_off;
+        bytes += cp.bulk;
+        Tin* dst = reinterpret_cast<Tin*>(data + off) + cp.shift;
+        for (int e = cp.tail0; e < st.len; ++e) dst[e] = tiles[src + e];
+        slotbase[s] = off + (cp.shift - st.r0sw) * (int)sizeof(Tin);   // bytes
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+    __threadfence_block();
+    __syncwarp();
     fence_proxy_async();
     if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
     __syncwarp();
     for (int s = lane; s < nslots; s += 32) {
         const StageSlot st = table[s];
-        const long long src = st.src0 + (long long)bc * st.vol;
-        const SpanCopy cp = plan_span(tiles, src, st.len, limit);
-        if (cp.bulk) bulk_copy_g2s(data + st.smem_off, reinterpret_cast<const void*>(cp.lo), cp.bulk, bar);
-        Tin* dst = reinterpret_cast<Tin*>(data + st.smem_off) + cp.shift;
-        for (int e = cp.tail0; e < st.len; ++e) dst[e] = tiles[src + e];
-        slotbase[s] = st.smem_off + (cp.shift - st.r0sw) * (int)sizeof(Tin);   // bytes
+        const SpanCopy cp = plan_span(tiles, st.src0 + (long long)bc * st.vol, st.len, limit);
+        if (cp.bulk) bulk_copy_g2s(data + pos + st.smem_off, reinterpret_cast<const void*>(cp.lo), cp.bulk, bar);
     }
 }
 
@@ -566,6 +578,7 @@ __device__ void blend_stage_item(const Tin* tiles, uintptr_t limit, const StageS
 // same KT terms.
 template <int U, int KT>
 struct Terms {
+    int n;                 // column tiles touching the columns (<= KT)
     int iw[KT], xo[KT], sw[KT];
     float w[KT][U];
     bool in[KT][U];
@@ -585,6 +598,7 @@ __device__ __forceinline__ void load_terms(const tdp_plan_t& p, int c, int W, Te
             hi = max(hi, h2);
         }
     }
+    t.n = hi - lo + 1;
 #pragma unroll
     for (int q = 0; q < KT; ++q) {
         const bool real = lo + q <= hi;
@@ -620,30 +634,143 @@ __device__ __forceinline__ void store_cols(__nv_bfloat16* out, long long i, cons
     }
 }
 
+// Column tiles touching the U output columns starting at c.
+template <int U>
+__device__ __forceinline__ int unit_terms(const tdp_plan_t& p, int c, int W) {
+    int lo, hi, l2, h2;
+    tdp::axis_cover(p, 2, c, lo, hi);
+#pragma unroll
+    for (int v = 1; v < U; ++v) {
+        if (c + v < W) {
+            tdp::axis_cover(p, 2, c + v, l2, h2);
+            lo = min(lo, l2);
+            hi = max(hi, h2);
+        }
+    }
+    return hi - lo + 1;
+}
+
+// Band rows [r0, r1) of one (frame, band) box that share their list of
+// (frame tile, row tile) pairs, in (frame tile, row tile) order.
+struct __align__(16) Run {
+    int r0, r1;
+    int nc;             // pairs (1, 2 or 4)
+    int ones;           // nc == 1 and r_f * r_h is exactly 1 on every row
+    int slot0b[4];      // per pair: byte offset of its column tile 0's entry in the run-base table
+};
+
+// Band rows [r, r1) of run R for one thread's U columns with its first KTW
+// column terms: per pair, inner = sum over terms of r_w * value, then
+// acc = fma(w_fh, inner, acc) (acc = inner when every weight is 1:
+// fma(1, inner, +0) is inner, which is never -0).  Shared addresses of
+// every (pair, term) live in registers for the whole run.
+template <int NC, int KTW, bool ONES, typename Tin, typename Tout, int U, int KT>
+__device__ __forceinline__ void blend_run(const Run& R, int r, int r1, uint32_t sdata, uint32_t sbase, uint32_t wrow,
+                                          int KC, const Terms<U, KT>& tm, const int (&colb)[KT],
+                                          const int (&swb)[KT], const int (&iwb)[KT], int hb0, Tout* dcol, int W) {
+    constexpr int esz = static_cast<int>(sizeof(Tin));
+    uint32_t ea[NC][KTW];
+#pragma unroll
+    for (int kk = 0; kk < NC; ++kk)
+#pragma unroll
+        for (int q = 0; q < KTW; ++q)
+            ea[kk][q] = sdata + lds_s32(sbase + R.slot0b[kk] + iwb[q]) + (hb0 + r) * swb[q] + colb[q];
+    uint32_t wa = wrow + 4 * KC * r;
+    Tout* dst = dcol + (long long)r * W;
+    for (; r < r1; ++r) {
+        float acc[U];
+#pragma unroll
+        for (int v = 0; v < U; ++v) acc[v] = 0.0f;
+#pragma unroll
+        for (int kk = 0; kk < NC; ++kk) {
+            float inner[U];
+#pragma unroll
+            for (int v = 0; v < U; ++v) inner[v] = 0.0f;
+#pragma unroll
+            for (int q = 0; q < KTW; ++q)
+#pragma unroll
+                for (int v = 0; v < U; ++v) {
+                    const float x =
+                        lds_masked(ea[kk][q] + v * esz, tm.sel[q][v], tm.in[q][v], static_cast<const Tin*>(nullptr));
+                    inner[v] = fmaf(tm.w[q][v], x, inner[v]);
+                }
+            if constexpr (ONES) {
+#pragma unroll
+                for (int v = 0; v < U; ++v) acc[v] = inner[v];
+            } else {
+                const float wfh = lds_f32(wa + 4 * kk);
+#pragma unroll
+                for (int v = 0; v < U; ++v) acc[v] = fmaf(wfh, inner[v], acc[v]);
+            }
+        }
+        store_cols<U>(dst, 0, acc);
+#pragma unroll
+        for (int kk = 0; kk < NC; ++kk)
+#pragma unroll
+            for (int q = 0; q < KTW; ++q) ea[kk][q] += swb[q];
+        wa += 4 * KC;
+        dst += W;
+    }
+}
+
+// A run of rows whose value is one tile's elements unchanged (one pair
+// with w_fh = 1 and, on every column of every thread of the warp, one
+// column tile with r_w = 1): the elements are copied.  The arithmetic path
+// gives the same values except that it turns -0 into +0.
+template <int U>
+__device__ __forceinline__ void copy_row(uint32_t ea, __nv_bfloat16* dst) {
+    if constexpr (U == 2) *reinterpret_cast<uint32_t*>(dst) = lds_u16(ea) | (lds_u16(ea + 2) << 16);
+    else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(lds_u16(ea));
+}
+template <int U>
+__device__ __forceinline__ void copy_row(uint32_t ea, float* dst) {
+    if constexpr (U == 2) *reinterpret_cast<float2*>(dst) = make_float2(lds_f32(ea), lds_f32(ea + 4));
+    else *dst = lds_f32(ea);
+}
+template <int U, typename T>
+__device__ __forceinline__ void copy_run(const Run& R, int r, int r1, uint32_t sdata, uint32_t sbase, int colb,
+                                         int swb, int iwb, int hb0, T* dcol, int W) {
+    uint32_t ea = sdata + lds_s32(sbase + R.slot0b[0] + iwb) + (hb0 + r) * swb + colb;
+    T* dst = dcol + (long long)r * W;
+    for (; r < r1; ++r) {
+        copy_row<U>(ea, dst);
+        ea += swb;
+        dst += W;
+    }
+}
+
 // Blend for plans where at most two tiles cover any index on every axis
 // (always the case under the guard: a tile holds at least twice the
 // overlap, so tiles i and i+2 never meet).
 //
-// Persistent over a contiguous range of (frame, band, b, c) items with two
-// shared-memory stages: warp 0 stages the next item's tile rows while the
-// CTA blends the current one.  A thread owns U adjacent output columns for
+// Persistent over a contiguous range of (frame, band, b, c) items, with
+// one producer warp and kBlendConsumers consumer threads.  The producer
+// keeps up to kBlendQueue items' tile rows in flight in a ring of shared
+// memory (items differ in size: frames covered by two frame tiles stage
+// twice the rows); per queue entry a "full" barrier completes when the
+// item's bulk copies land and an "empty" barrier when every consumer warp
+// is done with it.  A consumer thread owns U adjacent output columns for
 // the whole run (U = 2, or 1 when W is odd) and KT column-tile terms for
-// them; it walks the rows of its row group, where a per-row table lists the
-// (frame tile, row tile) pairs covering the row with w_fh = r_f * r_h.  Per
-// pair and column the thread forms inner = sum over column tiles of
-// r_w * value, then acc = fma(w_fh, inner, acc): the window product
-// r_f r_h r_w grouped as w_fh * (r_w * value), in fp32, summed in the order
-// (frame tile, row tile, column tile).
+// them.  The band's rows are split into runs that share their (frame tile,
+// row tile) pairs, and into one contiguous block per row group, balanced
+// by pair count.  Per pair and column the thread forms inner = sum over
+// column tiles of r_w * value, then acc = fma(w_fh, inner, acc): the window
+// product r_f r_h r_w grouped as w_fh * (r_w * value), in fp32, summed in
+// the order (frame tile, row tile, column tile).
 template <typename Tin, typename Tout, int U, int KT>
-__global__ void __launch_bounds__(kThreads, 3) blend_fast_kernel(const __grid_constant__ tdp_plan_t pg,
-                                                              const BlendArgs a) {
+__global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __grid_constant__ tdp_plan_t pg,
+                                                                   const BlendArgs a) {
     __shared__ tdp_plan_t p;
     load_plan(&p, pg);
     __syncthreads();
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    int* ncombo = reinterpret_cast<int*>(smem + a.off_a);
-    Combo* combo = reinterpret_cast<Combo*>(smem + a.off_b);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);                  // [kBlendQueue]
+    uint64_t* empty = full + kBlendQueue;                                // [kBlendQueue]
+    uint64_t* csync = empty + kBlendQueue;                               // consumers only
+    int* hdr = reinterpret_cast<int*>(smem + a.off_a);                   // run count, row-group bounds
+    int* qstart = hdr + 12;                                              // [kBlendQueue] ring offsets
+    Run* runs = reinterpret_cast<Run*>(smem + a.off_a + 64);
+    float* wts = reinterpret_cast<float*>(smem + a.off_b);
     StageSlot* table = reinterpret_cast<StageSlot*>(smem + a.off_stage);
     int* slotbase0 = reinterpret_cast<int*>(smem + a.off_slotbase);
     unsigned char* data0 = smem + a.off_data;
@@ -651,140 +778,268 @@ __global__ void __launch_bounds__(kThreads, 3) blend_fast_kernel(const __grid_co
     Tout* out = static_cast<Tout*>(a.out);
     const int F = p.dims[0], H = p.dims[1], W = p.dims[2], nw = p.num_tiles[2];
     const int KC = a.kf * a.kh;
-    const int max_slots = a.max_slots;
-    const uintptr_t limit = reinterpret_cast<uintptr_t>(tiles + a.tiles_numel) & ~uintptr_t(15);
+    const int max_slots = a.max_slots, ring = a.data_bytes;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kConsumerWarps = kBlendConsumers / 32;
 
     int first, last;
     cta_item_range(a.n_items, first, last);
     if (first >= last) return;
+    const int n = last - first;
     if (threadIdx.x == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int q = 0; q < kBlendQueue; ++q) {
+            mbar_init(&full[q], 1);
+            mbar_init(&empty[q], kConsumerWarps);
+        }
+        mbar_init(csync, kBlendConsumers);
     }
     __syncthreads();
-    // warp 0: stage table for the (frame, band) of the item it stages next
-    int table_fb = -1, table_n = 0;
-    ItemCursor ahead;
-    ahead.init(first, a.BC);
-    if (threadIdx.x < 32) {
-        const BlendBox c0 = blend_box(p, a, ahead.fb);
-        blend_build_stage_table<Tin>(p, a, c0, table);
-        table_fb = ahead.fb;
-        table_n = c0.nslots;
-        blend_stage_item(tiles, limit, table, table_n, ahead.bc, slotbase0, data0, &bar[0]);
-    }
-    ahead.next();
 
-    // This thread's columns and terms (fixed for the run).  A row group is
-    // the column units rounded up to whole warps, so a warp stays on one row
-    // and walks one (frame tile, row tile) list.
+    if (warp == kConsumerWarps) {
+        // ---- producer.  Item k (k = item - first) uses queue entry
+        // k mod kBlendQueue; items sit in the ring in order, item k at
+        // qstart[k mod kBlendQueue]; kfree items are known released.
+        const uintptr_t limit = reinterpret_cast<uintptr_t>(tiles + a.tiles_numel) & ~uintptr_t(15);
+        int table_fb = -1, table_n = 0, table_bytes = 0, head = 0, kfree = 0;
+        bool ok = true;
+        ItemCursor ahead;
+        ahead.init(first, a.BC);
+        auto release = [&]() -> bool {   // wait for the oldest staged item to be released
+            const bool r = mbar_wait_bounded(&empty[kfree % kBlendQueue], (kfree / kBlendQueue) & 1);
+            ++kfree;
+            return r;
+        };
+        int kst = 0;
+        for (; kst < n && ok; ++kst, ahead.next()) {
+            if (ahead.fb != table_fb) {
+                const BlendBox cn = blend_box(p, a, ahead.fb);
+                table_bytes = blend_build_stage_table<Tin>(p, a, cn, table);
+                table_fb = ahead.fb;
+                table_n = cn.nslots;
+            }
+            while (ok && kfree < kst - kBlendQueue + 1) ok = release();   // queue entry free
+            int pos = 0;
+            for (;;) {                                                     // ring room
+                if (!ok) break;
+                if (kfree == kst) { pos = 0; break; }                      // ring empty
+                const int tail = qstart[kfree % kBlendQueue];
+                if (head > tail) {
+                    if (head + table_bytes <= ring) { pos = head; break; }
+                    if (table_bytes <= tail) { pos = 0; break; }
+                } else if (head < tail && head + table_bytes <= tail) {
+                    pos = head;
+                    break;
+                }
+                ok = release();
+            }
+            if (!ok) break;
+            const int q = kst % kBlendQueue;
+            if (lane == 0) qstart[q] = pos;
+            __syncwarp();
+            blend_stage_item(tiles, limit, table, table_n, ahead.bc, slotbase0 + q * max_slots, data0, pos, &full[q]);
+            head = pos + table_bytes;
+        }
+        if (!ok) {
+            // a consumer stopped: let every issued copy land, then leave
+            if (lane == 0) atomicOr(&g_device_error, kErrBlendWait);
+            for (int j = kfree; j < kst; ++j) mbar_wait_bounded(&full[j % kBlendQueue], (j / kBlendQueue) & 1);
+        }
+        return;
+    }
+
+    // ---- consumers.  They meet (every thread arrives, then waits, bounded)
+    // on `csync`; a wait that runs out stops the consumer, and the others
+    // then run out too, since it never arrives again.
+    uint32_t cphase = 0;
+    auto consumer_sync = [&]() -> bool {
+        mbar_arrive(csync);
+        const bool r = mbar_wait_bounded(csync, cphase & 1);
+        ++cphase;
+        return r;
+    };
+    // A row group is the column units rounded up to whole
+    // warps, so a warp stays on one row.  Column units are sorted by how
+    // many column tiles they touch (fewest first) so that whole warps share
+    // one term count.
     const int ncu = (W + U - 1) / U;
-    const int per_row = min(round_up(ncu, 32), static_cast<int>(blockDim.x));
-    const int RG = static_cast<int>(blockDim.x) / per_row;
+    const int per_row = min(round_up(ncu, 32), kBlendConsumers);
+    const int RG = kBlendConsumers / per_row;   // 1 .. 8
     const int rg = static_cast<int>(threadIdx.x) / per_row;
     const int cu0 = static_cast<int>(threadIdx.x) - rg * per_row;
     const int ncu_mine = (rg < RG && cu0 < ncu) ? (ncu - cu0 + per_row - 1) / per_row : 0;
+    int* tcount = reinterpret_cast<int*>(smem + a.off_c);
+    int* sorted = tcount + ncu;
+    for (int u = threadIdx.x; u < ncu; u += kBlendConsumers) tcount[u] = unit_terms<U>(p, u * U, W);
+    if (!consumer_sync()) return (void)atomicOr(&g_device_error, kErrBlendWait);
+    for (int u = threadIdx.x; u < ncu; u += kBlendConsumers) {
+        const int ku = tcount[u];
+        int rank = 0;
+        for (int j = 0; j < ncu; ++j) {
+            const int kj = tcount[j];
+            rank += (kj < ku) || (kj == ku && j < u);
+        }
+        sorted[rank] = u;
+    }
+    if (!consumer_sync()) return (void)atomicOr(&g_device_error, kErrBlendWait);
     Terms<U, KT> tm;
-    if (ncu_mine == 1) load_terms<U, KT>(p, cu0 * U, W, tm);
+    tm.n = 0;
+    bool lane_copy = false;
+    if (ncu_mine == 1) {
+        load_terms<U, KT>(p, sorted[cu0] * U, W, tm);
+        lane_copy = tm.n == 1 && sizeof(Tin) == sizeof(Tout);
+#pragma unroll
+        for (int v = 0; v < U; ++v) lane_copy = lane_copy && tm.in[0][v] && tm.w[0][v] == 1.0f;
+    }
+    // warp-uniform: term count (idle lanes count 0), and whether every
+    // working lane may copy; wide rows take the general path
+    const int kt_warp = __reduce_max_sync(0xffffffffu, ncu_mine > 1 ? KT : (ncu_mine == 1 ? tm.n : 0));
+    const bool warp_copy = __all_sync(0xffffffffu, ncu_mine == 0 || (ncu_mine == 1 && lane_copy)) &&
+                           __any_sync(0xffffffffu, ncu_mine == 1);
 
     ItemCursor cur;
     cur.init(first, a.BC);
     int box_fb = -1;
     BlendBox c{};
-    for (int k = 0, item = first; item < last; ++k, ++item, cur.next()) {
-        const int s = k & 1;
-        if (cur.fb != box_fb) c = blend_box(p, a, cur.fb);
-        if (threadIdx.x < 32) {
-            if (item + 1 < last) {
-                if (ahead.fb != table_fb) {
-                    const BlendBox cn = blend_box(p, a, ahead.fb);
-                    blend_build_stage_table<Tin>(p, a, cn, table);
-                    table_fb = ahead.fb;
-                    table_n = cn.nslots;
-                }
-                blend_stage_item(tiles, limit, table, table_n, ahead.bc, slotbase0 + (s ^ 1) * max_slots,
-                                 data0 + (s ^ 1) * a.data_bytes, &bar[s ^ 1]);
-                ahead.next();
-            }
-        } else if (cur.fb != box_fb) {
-            for (int r = threadIdx.x - 32; r < c.rows; r += blockDim.x - 32) {
-                const int h = c.hb0 + r;
-                int lo, hi;
-                tdp::axis_cover(p, 1, h, lo, hi);
-                int n = 0;
-                for (int fa = 0; fa < c.NF; ++fa) {
-                    const float wf = axis_weight(p, 0, c.if_lo + fa, c.f);
-                    for (int ih = lo; ih <= hi; ++ih)
-                        combo[r * KC + n++] =
-                            Combo{4 * (fa * c.NH + ih - c.ih_lo) * nw, __fmul_rn(wf, axis_weight(p, 1, ih, h))};
-                }
-                ncombo[r] = n;
-            }
-        }
-        box_fb = cur.fb;
-        if (!cta_wait(&bar[s], (k >> 1) & 1)) {
-            if (threadIdx.x == 0) {
-                atomicOr(&g_device_error, kErrBlendWait);
-                mbar_wait_bounded(&bar[s], (k >> 1) & 1);
-                if (item + 1 < last) mbar_wait_bounded(&bar[s ^ 1], ((k + 1) >> 1) & 1);
-            }
-            return;
-        }
-        const uint32_t sdata = smem_u32(data0) + s * a.data_bytes;
-        const uint32_t sbase = smem_u32(slotbase0 + s * max_slots);
-        constexpr int esz = static_cast<int>(sizeof(Tin));
-        const long long out0 = ((long long)cur.bc * F + c.f) * H * W + (long long)c.hb0 * W;
-        for (int m = 0; m < ncu_mine; ++m) {
-            const int cu = cu0 + m * per_row;
-            if (ncu_mine > 1) load_terms<U, KT>(p, cu * U, W, tm);
-            // per term: byte offsets of the column pair in its tile row, of one
-            // row step, and of the term's entry in the run-base table
-            int rowb[KT], stepb[KT], iwb[KT];
-#pragma unroll
-            for (int q = 0; q < KT; ++q) {
-                rowb[q] = ((c.hb0 + rg) * tm.sw[q] + tm.xo[q]) * esz;
-                stepb[q] = RG * tm.sw[q] * esz;
-                iwb[q] = 4 * tm.iw[q];
-            }
-            Tout* dst = out + out0 + (long long)rg * W + cu * U;
-            const long long dstep = (long long)RG * W;
-            uint32_t nca = smem_u32(ncombo) + 4 * rg;
-            uint32_t cba = smem_u32(combo) + 8 * KC * rg;
-            const uint32_t nca_step = 4 * RG, cba_step = 8 * KC * RG;
-            for (int r = rg; r < c.rows; r += RG) {
-                float acc[U];
-#pragma unroll
-                for (int v = 0; v < U; ++v) acc[v] = 0.0f;
-                const int nc = lds_s32(nca);
-                uint32_t ca = cba;
-                for (int kk = 0; kk < nc; ++kk, ca += 8) {
-                    const int slot0b = lds_s32(ca);
-                    const float wfh = lds_f32(ca + 4);
-                    float inner[U];
-#pragma unroll
-                    for (int v = 0; v < U; ++v) inner[v] = 0.0f;
-#pragma unroll
-                    for (int q = 0; q < KT; ++q) {
-                        const uint32_t ea = sdata + lds_s32(sbase + slot0b + iwb[q]) + rowb[q];
-#pragma unroll
-                        for (int v = 0; v < U; ++v) {
-                            const float x = lds_masked(ea + v * esz, tm.sel[q][v], tm.in[q][v],
-                                                       static_cast<const Tin*>(nullptr));
-                            inner[v] = fmaf(tm.w[q][v], x, inner[v]);
-                        }
+    int nruns = 0, rb0 = 0, rb1 = 0;
+    for (int k = 0; k < n; ++k, cur.next()) {
+        if (cur.fb != box_fb) {
+            // new (frame, band): rebuild the row tables once every consumer
+            // is done with the old ones
+            c = blend_box(p, a, cur.fb);
+            box_fb = cur.fb;
+            if (!consumer_sync()) return (void)atomicOr(&g_device_error, kErrBlendWait);
+            if (warp == 1) {
+                // runs: a row opens one when its pair list or its all-ones
+                // flag differs from the previous row's
+                const float wf0 = axis_weight(p, 0, c.if_lo, c.f);
+                int carry = 0, prev_key = -1;
+                for (int r0 = 0; r0 < c.rows; r0 += 32) {
+                    const int r = r0 + lane;
+                    const bool valid = r < c.rows;
+                    int lo = 0, hi = 0, key = -1;
+                    bool ones = false;
+                    if (valid) {
+                        tdp::axis_cover(p, 1, c.hb0 + r, lo, hi);
+                        ones = c.NF == 1 && lo == hi && __fmul_rn(wf0, axis_weight(p, 1, lo, c.hb0 + r)) == 1.0f;
+                        key = lo | (hi << 8) | (int(ones) << 16);
                     }
-#pragma unroll
-                    for (int v = 0; v < U; ++v) acc[v] = fmaf(wfh, inner[v], acc[v]);
+                    int pk = __shfl_up_sync(0xffffffffu, key, 1);
+                    if (lane == 0) pk = prev_key;
+                    const bool start = valid && key != pk;
+                    const unsigned bal = __ballot_sync(0xffffffffu, start);
+                    if (start) {
+                        Run& R = runs[carry + __popc(bal & ((1u << lane) - 1u))];
+                        R.r0 = r;
+                        R.nc = c.NF * (hi - lo + 1);
+                        R.ones = ones;
+                        int m = 0;
+                        for (int fa = 0; fa < c.NF; ++fa)
+                            for (int ih = lo; ih <= hi; ++ih) R.slot0b[m++] = 4 * (fa * c.NH + ih - c.ih_lo) * nw;
+                        for (; m < 4; ++m) R.slot0b[m] = 0;
+                    }
+                    carry += __popc(bal);
+                    prev_key = __shfl_sync(0xffffffffu, key, 31);
                 }
-                store_cols<U>(dst, 0, acc);
-                dst += dstep;
-                nca += nca_step;
-                cba += cba_step;
+                __syncwarp();
+                for (int i = lane; i < carry; i += 32) runs[i].r1 = i + 1 < carry ? runs[i + 1].r0 : c.rows;
+                __syncwarp();
+                if (lane == 0) {
+                    // row-group blocks: contiguous rows, split where the
+                    // running pair count crosses g / RG of the band's total
+                    int total = 0;
+                    for (int i = 0; i < carry; ++i) total += runs[i].nc * (runs[i].r1 - runs[i].r0);
+                    hdr[0] = carry;
+                    hdr[1] = 0;
+                    int g = 1, acc = 0;
+                    for (int i = 0; i < carry && g < RG; ++i) {
+                        const int nc = runs[i].nc, len = runs[i].r1 - runs[i].r0;
+                        while (g < RG) {
+                            const int target = (total * g + RG / 2) / RG;
+                            if (acc + nc * len < target) break;
+                            hdr[1 + g] = runs[i].r0 + min(len, max(0, (target - acc + nc - 1) / nc));
+                            ++g;
+                        }
+                        acc += nc * len;
+                    }
+                    for (; g <= RG; ++g) hdr[1 + g] = c.rows;
+                }
+            } else if (warp >= 2) {
+                // per row and pair (frame tile major): w_fh = r_f * r_h
+                for (int r = threadIdx.x - 64; r < c.rows; r += kBlendConsumers - 64) {
+                    const int h = c.hb0 + r;
+                    int lo, hi;
+                    tdp::axis_cover(p, 1, h, lo, hi);
+                    int m = 0;
+                    for (int fa = 0; fa < c.NF; ++fa) {
+                        const float wf = axis_weight(p, 0, c.if_lo + fa, c.f);
+                        for (int ih = lo; ih <= hi; ++ih) wts[r * KC + m++] = __fmul_rn(wf, axis_weight(p, 1, ih, h));
+                    }
+                }
+            }
+            if (!consumer_sync()) return (void)atomicOr(&g_device_error, kErrBlendWait);
+            nruns = hdr[0];
+            rb0 = rg < RG ? hdr[1 + rg] : 0;
+            rb1 = rg < RG ? hdr[2 + rg] : 0;
+        }
+        const int q = k % kBlendQueue;
+        if (!mbar_wait_bounded(&full[q], (k / kBlendQueue) & 1)) {
+            if (lane == 0) atomicOr(&g_device_error, kErrBlendWait);
+            return;   // no further releases: the producer gives up and drains its copies
+        }
+        const uint32_t sdata = smem_u32(data0);
+        const uint32_t sbase = smem_u32(slotbase0 + q * max_slots);
+        const uint32_t wrow = smem_u32(wts);
+        constexpr int esz = static_cast<int>(sizeof(Tin));
+        Tout* const out_band = out + ((long long)cur.bc * F + c.f) * H * W + (long long)c.hb0 * W;
+        for (int m = 0; m < ncu_mine; ++m) {
+            const int cu = sorted[cu0 + m * per_row];
+            if (ncu_mine > 1) load_terms<U, KT>(p, cu * U, W, tm);
+            // per term: byte offsets of the columns in the tile row, of one
+            // tile row, and of the term's entry in the run-base table
+            int colb[KT], swb[KT], iwb[KT];
 #pragma unroll
-                for (int q = 0; q < KT; ++q) rowb[q] += stepb[q];
+            for (int t = 0; t < KT; ++t) {
+                colb[t] = tm.xo[t] * esz;
+                swb[t] = tm.sw[t] * esz;
+                iwb[t] = 4 * tm.iw[t];
+            }
+            Tout* const dcol = out_band + cu * U;
+            for (int ri = 0; ri < nruns; ++ri) {
+                const Run R = runs[ri];
+                const int r = max(R.r0, rb0), r1 = min(R.r1, rb1);
+                if (r >= r1) continue;
+                if (R.nc == 1) {
+                    if (R.ones) {
+                        if constexpr (sizeof(Tin) == sizeof(Tout)) {
+                            if (warp_copy) {
+                                copy_run<U>(R, r, r1, sdata, sbase, colb[0], swb[0], iwb[0], c.hb0, dcol, W);
+                                continue;
+                            }
+                        }
+                        if (kt_warp == 1)
+                            blend_run<1, 1, true, Tin>(R, r, r1, sdata, sbase, wrow, KC, tm, colb, swb, iwb, c.hb0, dcol, W);
+                        else
+                            blend_run<1, KT, true, Tin>(R, r, r1, sdata, sbase, wrow, KC, tm, colb, swb, iwb, c.hb0, dcol, W);
+                    } else if (kt_warp == 1) {
+                        blend_run<1, 1, false, Tin>(R, r, r1, sdata, sbase, wrow, KC, tm, colb, swb, iwb, c.hb0, dcol, W);
+                    } else {
+                        blend_run<1, KT, false, Tin>(R, r, r1, sdata, sbase, wrow, KC, tm, colb, swb, iwb, c.hb0, dcol, W);
+                    }
+                } else if (R.nc == 2) {
+                    if (kt_warp == 1)
+                        blend_run<2, 1, false, Tin>(R, r, r1, sdata, sbase, wrow, KC, tm, colb, swb, iwb, c.hb0, dcol, W);
+                    else
+                        blend_run<2, KT, false, Tin>(R, r, r1, sdata, sbase, wrow, KC, tm, colb, swb, iwb, c.hb0, dcol, W);
+                } else {
+                    if (kt_warp == 1)
+                        blend_run<4, 1, false, Tin>(R, r, r1, sdata, sbase, wrow, KC, tm, colb, swb, iwb, c.hb0, dcol, W);
+                    else
+                        blend_run<4, KT, false, Tin>(R, r, r1, sdata, sbase, wrow, KC, tm, colb, swb, iwb, c.hb0, dcol, W);
+                }
             }
         }
-        __syncthreads();  // stage s, its slot bases and the row table are free again
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[q]);   // this warp is done with item k's rows and slot bases
     }
 }
 
@@ -818,7 +1073,7 @@ __global__ void __launch_bounds__(kThreads) blend_generic_kernel(const __grid_co
     __syncthreads();
     if (threadIdx.x < 32) {
         blend_build_stage_table<Tin>(p, a, c, table);
-        blend_stage_item(tiles, limit, table, c.nslots, bc, slotbase, data, bar);
+        blend_stage_item(tiles, limit, table, c.nslots, bc, slotbase, data, 0, bar);
     } else {
         const int t = threadIdx.x - 32, nt = blockDim.x - 32;
         if (t == 0)
@@ -1267,8 +1522,8 @@ int max_slots_for(const tdp_plan_t& p, int band_rows, int nbands) {
     return best;
 }
 
-// Shared-memory layout of an extract CTA: two barriers, the slot table and
-// two staged bands.
+// Shared-memory layout of an extract CTA: one barrier per stage, the slot
+// table and the staged bands.
 struct ExtractLayout {
     int off_slots, off_data, stage_bytes, total;
 };
@@ -1276,10 +1531,10 @@ struct ExtractLayout {
 ExtractLayout extract_layout(const tdp_plan_t& p, int band_rows, int esz) {
     const int nbands = (p.dims[1] + band_rows - 1) / band_rows;
     ExtractLayout L;
-    L.off_slots = 16;
+    L.off_slots = round_up(8 * kExtractStages, 16);
     L.off_data = round_up(L.off_slots + max_slots_for(p, band_rows, nbands) * (int)sizeof(ExtractSlot), 16);
     const long long stage = (long long)round_up(band_rows * p.dims[2] * esz, 16) + 16;
-    const long long total = L.off_data + 2 * stage;
+    const long long total = L.off_data + kExtractStages * stage;
     L.stage_bytes = stage > INT_MAX ? INT_MAX : static_cast<int>(stage);
     L.total = total > INT_MAX ? INT_MAX : static_cast<int>(total);
     return L;
@@ -1323,13 +1578,13 @@ BlendLayout blend_layout(const tdp_plan_t& p, int band_rows, int esz) {
     const int nbands = (p.dims[1] + band_rows - 1) / band_rows;
     BlendLayout L;
     L.fast = kf <= 2 && kh <= 2 && kw <= 2;
-    const int stages = L.fast ? 2 : 1;
     L.max_slots = max_slots_for(p, band_rows, nbands);
-    int o = 16;  // two mbarriers
+    int o = L.fast ? round_up(16 * kBlendQueue + 8, 16) : 16;  // mbarriers
     if (L.fast) {
-        L.off_a = o; o = round_up(o + band_rows * 4, 16);                             // ncombo
-        L.off_b = o; o = round_up(o + band_rows * kf * kh * (int)sizeof(Combo), 16);  // combo
-        L.off_c = L.off_d = L.off_e = o;
+        L.off_a = o; o = round_up(o + 64 + band_rows * (int)sizeof(Run), 16);         // header, runs
+        L.off_b = o; o = round_up(o + band_rows * kf * kh * 4, 16);                   // w_fh per row and pair
+        L.off_c = o; o = round_up(o + 8 * W, 16);                                     // column order
+        L.off_d = L.off_e = o;
     } else {
         L.off_a = o; o = round_up(o + kf * (int)sizeof(Cov), 16);                     // fcov
         L.off_b = o; o = round_up(o + band_rows * 4, 16);                             // hcnt
@@ -1338,10 +1593,14 @@ BlendLayout blend_layout(const tdp_plan_t& p, int band_rows, int esz) {
         L.off_e = o; o = round_up(o + W * kw * (int)sizeof(Cov), 16);                 // wcov
     }
     L.off_stage = o; o = round_up(o + L.max_slots * (int)sizeof(StageSlot), 16);
-    L.off_slotbase = o; o = round_up(o + stages * L.max_slots * 4, 16);
+    L.off_slotbase = o; o = round_up(o + (L.fast ? kBlendQueue : 1) * L.max_slots * 4, 16);
     L.off_data = o;
-    const long long data = blend_data_bytes(p, band_rows, esz);
-    const long long total = o + stages * data;
+    // largest item; the fast kernel's ring holds at least two of them and
+    // takes the rest of the budget
+    const long long item = blend_data_bytes(p, band_rows, esz);
+    long long data = item;
+    if (L.fast) data = std::max(2 * item, (long long)(kBlendSmemBudget - o) / 16 * 16);
+    const long long total = o + data;
     L.data_bytes = data > INT_MAX ? INT_MAX : static_cast<int>(data);
     L.total = total > INT_MAX ? INT_MAX : static_cast<int>(total);
     return L;
@@ -1357,9 +1616,9 @@ int sm_count() {
 // Grid of a persistent kernel: every resident CTA slot of the GPU, at most
 // one CTA per item.
 template <typename K>
-tdp_status persistent_grid(K kernel, int smem, long long items, unsigned* grid) {
+tdp_status persistent_grid(K kernel, int smem, long long items, unsigned* grid, int threads = kThreads) {
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
     if (e != cudaSuccess) return cuda_status(e);
     const long long slots = (long long)std::max(1, per_sm) * std::max(1, sm_count());
     *grid = static_cast<unsigned>(std::min(items, slots));
@@ -1445,8 +1704,9 @@ tdp_status launch_blend(const tdp_plan_t& p, int BC, const void* tiles, long lon
         tdp_status st = set_smem(kernel, L.total);
         if (st != TDP_OK) return st;
         unsigned grid = static_cast<unsigned>(items);
-        if (persistent && (st = persistent_grid(kernel, L.total, items, &grid)) != TDP_OK) return st;
-        kernel<<<grid, kThreads, L.total, stream>>>(p, a);
+        const int threads = persistent ? kBlendThreads : kThreads;
+        if (persistent && (st = persistent_grid(kernel, L.total, items, &grid, threads)) != TDP_OK) return st;
+        kernel<<<grid, threads, L.total, stream>>>(p, a);
         return cuda_status(cudaGetLastError());
     };
     // Pair stores need every output row to start on a 4-byte (bf16) or
