@@ -41,12 +41,14 @@ constexpr int kThreads = 256;
 constexpr int kCluster = 8;                  // CTAs cooperating on one tile's token reduction
 constexpr uint64_t kWaitNs = 1000ull * 1000 * 1000;  // give up on staged copies after 1 s
 constexpr uint32_t kSuspendHintNs = 20000;           // a polling thread sleeps up to 20 us per try
+constexpr uint32_t kBackoffNs = 200;                 // sleep between polls of a waiter off the critical path
 constexpr uint32_t kErrExtractWait = 1u;
 constexpr uint32_t kErrBlendWait = 2u;
-constexpr int kExtractStages = 4;               // staged bands per extract CTA (3 in flight)
+constexpr int kExtractStages = 3;               // staged bands per extract CTA (2 in flight)
 constexpr int kExtractSmemBudget = 64 * 1024;   // staged bands + slot table
 constexpr int kBlendSmemBudget = 64 * 1024;     // ring of staged tile rows + tables (3 CTAs per SM)
-constexpr int kBlendQueue = 4;                  // blend items staged ahead at most
+constexpr int kBlendQueue = 4;                  // blend items staged ahead at most (the header holds 4 ring offsets)
+constexpr int kMaxOrdered = 256;                // column units ordered on the host
 constexpr int kBlendConsumers = 256;            // blend threads that compute (8 warps)
 constexpr int kBlendThreads = kBlendConsumers + 32;   // + one producer warp
 
@@ -106,6 +108,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     const uint64_t t0 = global_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
+    }
+}
+
+// As mbar_wait_bounded, for a waiter off the critical path (a producer
+// waiting for buffer space): it sleeps between polls so that it does not
+// take issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        __nanosleep(kBackoffNs);
         if (global_ns() - t0 > kWaitNs) return false;
     }
 }
@@ -239,10 +253,13 @@ __device__ __forceinline__ float lds_masked(uint32_t addr, uint32_t, bool in, co
 // Items are numbered (frame, band) major, then b * C + c, and every CTA of a
 // persistent kernel takes one contiguous range of them: consecutive items
 // share their frame and band, so the geometry built for one serves the
-// next, and ranges differ in length by at most one item.
+// next, and ranges differ in length by at most one item (the first
+// n mod G ranges are one longer).
 __device__ __forceinline__ void cta_item_range(int n_items, int& first, int& last) {
-    first = static_cast<int>(((long long)blockIdx.x * n_items) / gridDim.x);
-    last = static_cast<int>(((long long)(blockIdx.x + 1) * n_items) / gridDim.x);
+    const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    const int q = n_items / G, r = n_items - q * G;
+    first = b * q + min(b, r);
+    last = first + q + (b < r ? 1 : 0);
 }
 
 struct FrameBand {
@@ -455,12 +472,12 @@ struct Cov {
     float w;
 };
 
-struct StageSlot {      // one run of tile rows of a (frame, band) box
-    long long src0;     // packed element index for b*C + c = 0
-    long long vol;      // elements per (b, c) of the tile: src = src0 + (b*C + c) * vol
-    int len;            // elements
-    int smem_off;       // byte offset inside a stage's data region
-    int r0sw;           // first row of the run times the tile width
+struct StageSlot {      // one run of tile rows of a (frame, band) box, in bytes
+    long long src0;     // offset in the packed tiles for b*C + c = 0
+    long long vol;      // per (b, c) of the tile: offset = src0 + (b*C + c) * vol
+    int len;            // bytes of the run
+    int smem_off;       // offset inside an item's staged data
+    int r0sw;           // first row of the run times the tile row
     int pad;
 };
 
@@ -477,6 +494,11 @@ struct BlendArgs {
     int off_a, off_b, off_c, off_d, off_e, off_stage, off_slotbase, off_data;
     int max_slots, data_bytes;
     int kf, kh, kw;
+    // fast kernel: column units (U output columns each) in the order the
+    // consumer threads take them -- fewest column tiles first -- when there
+    // are at most kMaxOrdered units; otherwise the identity order
+    int ordered;
+    uint16_t order[kMaxOrdered];
 };
 
 __host__ __device__ inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
@@ -516,13 +538,14 @@ __device__ int blend_build_stage_table(const tdp_plan_t& p, const BlendArgs& a, 
             const int iw = s % nw, jh = (s / nw) % c.NH, i_f = c.if_lo + s / (nw * c.NH), i_h = c.ih_lo + jh;
             const int sf = tdp::tile_size(p, 0, i_f), sh = tdp::tile_size(p, 1, i_h), sw = tdp::tile_size(p, 2, iw);
             const int r0 = max(p.start[1][i_h], c.hb0), r1 = min(p.end[1][i_h], c.hb1);
-            st.vol = (long long)sf * sh * sw;
-            st.src0 = (long long)a.BC * tdp::tile_prefix_volume(p, i_f, i_h, iw) +
-                      ((long long)(c.f - p.start[0][i_f]) * sh + (r0 - p.start[1][i_h])) * sw;
-            st.len = (r1 - r0) * sw;
-            st.r0sw = r0 * sw;
+            constexpr int esz = static_cast<int>(sizeof(Tin));
+            st.vol = (long long)sf * sh * sw * esz;
+            st.src0 = ((long long)a.BC * tdp::tile_prefix_volume(p, i_f, i_h, iw) +
+                       ((long long)(c.f - p.start[0][i_f]) * sh + (r0 - p.start[1][i_h])) * sw) * esz;
+            st.len = (r1 - r0) * sw * esz;
+            st.r0sw = r0 * sw * esz;
             st.pad = 0;
-            padded = round_up(st.len * (int)sizeof(Tin), 16) + 16;
+            padded = round_up(st.len, 16) + 16;
         }
         const int incl = warp_incl_scan(padded);
         if (s < c.nslots) {
@@ -536,37 +559,43 @@ __device__ int blend_build_stage_table(const tdp_plan_t& p, const BlendArgs& a, 
 }
 
 // One warp: stage item (box table, b*C + c) at byte `pos` of the data
-// region.  First the plain writes -- per run, the byte offset in the data
-// region of (its row 0, column 0), and plain loads for a run ending in the
-// buffer's last partial 16 bytes -- then the barrier is armed with the bulk
-// bytes (its release covers those writes) and one bulk copy per run is
-// issued.
+// region.  Each lane takes runs s = lane, lane + 32, ...: it records the
+// byte offset in the data region of the run's (row 0, column 0), loads
+// with plain copies the part of a run in the buffer's last partial 16
+// bytes, arrives on the barrier with its bulk bytes (the arrival releases
+// those writes; the barrier counts 32 arrivals) and then issues its bulk
+// copies.
 template <typename Tin>
 __device__ void blend_stage_item(const Tin* tiles, uintptr_t limit, const StageSlot* table, int nslots, int bc,
                                  int* slotbase, unsigned char* data, int pos, uint64_t* bar) {
     const int lane = threadIdx.x & 31;
+    const uintptr_t base = reinterpret_cast<uintptr_t>(tiles);
     uint32_t bytes = 0;
     for (int s = lane; s < nslots; s += 32) {
         const StageSlot st = table[s];
-        const long long src = st.src0 + (long long)bc * st.vol;
-        const SpanCopy cp = plan_span(tiles, src, st.len, limit);
-        const int off = pos + st.smem_off;
-        bytes += cp.bulk;
-        Tin* dst = reinterpret_cast<Tin*>(data + off) + cp.shift;
-        for (int e = cp.tail0; e < st.len; ++e) dst[e] = tiles[src + e];
-        slotbase[s] = off + (cp.shift - st.r0sw) * (int)sizeof(Tin);   // bytes
+        const uintptr_t g0 = base + st.src0 + (uintptr_t)bc * st.vol, g1 = g0 + st.len;
+        const uintptr_t lo = g0 & ~uintptr_t(15);
+        uintptr_t hi = (g1 + 15) & ~uintptr_t(15);
+        if (hi > limit) {   // the tail past the last 16-byte boundary: plain copies
+            hi = g1 & ~uintptr_t(15);
+            const uintptr_t t0 = hi > g0 ? hi : g0;
+            Tin* dst = reinterpret_cast<Tin*>(data + pos + st.smem_off + (t0 - lo));
+            const Tin* src = reinterpret_cast<const Tin*>(t0);
+            for (int e = 0; e < static_cast<int>((g1 - t0) / sizeof(Tin)); ++e) dst[e] = src[e];
+        }
+        bytes += hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
+        slotbase[s] = pos + st.smem_off + static_cast<int>(g0 - lo) - st.r0sw;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-    __threadfence_block();
-    __syncwarp();
     fence_proxy_async();
-    if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-    __syncwarp();
+    mbar_arrive_expect_tx(bar, bytes);
     for (int s = lane; s < nslots; s += 32) {
         const StageSlot st = table[s];
-        const SpanCopy cp = plan_span(tiles, st.src0 + (long long)bc * st.vol, st.len, limit);
-        if (cp.bulk) bulk_copy_g2s(data + pos + st.smem_off, reinterpret_cast<const void*>(cp.lo), cp.bulk, bar);
+        const uintptr_t g0 = base + st.src0 + (uintptr_t)bc * st.vol, g1 = g0 + st.len;
+        const uintptr_t lo = g0 & ~uintptr_t(15);
+        uintptr_t hi = (g1 + 15) & ~uintptr_t(15);
+        if (hi > limit) hi = g1 & ~uintptr_t(15);
+        if (hi > lo)
+            bulk_copy_g2s(data + pos + st.smem_off, reinterpret_cast<const void*>(lo), static_cast<uint32_t>(hi - lo), bar);
     }
 }
 
@@ -632,22 +661,6 @@ __device__ __forceinline__ void store_cols(__nv_bfloat16* out, long long i, cons
     } else {
         out[i] = __float2bfloat16_rn(v[0]);
     }
-}
-
-// Column tiles touching the U output columns starting at c.
-template <int U>
-__device__ __forceinline__ int unit_terms(const tdp_plan_t& p, int c, int W) {
-    int lo, hi, l2, h2;
-    tdp::axis_cover(p, 2, c, lo, hi);
-#pragma unroll
-    for (int v = 1; v < U; ++v) {
-        if (c + v < W) {
-            tdp::axis_cover(p, 2, c + v, l2, h2);
-            lo = min(lo, l2);
-            hi = max(hi, h2);
-        }
-    }
-    return hi - lo + 1;
 }
 
 // Band rows [r0, r1) of one (frame, band) box that share their list of
@@ -781,6 +794,7 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
     const int max_slots = a.max_slots, ring = a.data_bytes;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int kConsumerWarps = kBlendConsumers / 32;
+    static_assert(kBlendQueue <= 4 && kConsumerWarps <= 8, "shared header: 12 ints of run count and row-group bounds, 4 ring offsets");
 
     int first, last;
     cta_item_range(a.n_items, first, last);
@@ -788,7 +802,7 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
     const int n = last - first;
     if (threadIdx.x == 0) {
         for (int q = 0; q < kBlendQueue; ++q) {
-            mbar_init(&full[q], 1);
+            mbar_init(&full[q], 32);
             mbar_init(&empty[q], kConsumerWarps);
         }
         mbar_init(csync, kBlendConsumers);
@@ -805,7 +819,7 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
         ItemCursor ahead;
         ahead.init(first, a.BC);
         auto release = [&]() -> bool {   // wait for the oldest staged item to be released
-            const bool r = mbar_wait_bounded(&empty[kfree % kBlendQueue], (kfree / kBlendQueue) & 1);
+            const bool r = mbar_wait_backoff(&empty[kfree % kBlendQueue], (kfree / kBlendQueue) & 1);
             ++kfree;
             return r;
         };
@@ -867,25 +881,12 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
     const int rg = static_cast<int>(threadIdx.x) / per_row;
     const int cu0 = static_cast<int>(threadIdx.x) - rg * per_row;
     const int ncu_mine = (rg < RG && cu0 < ncu) ? (ncu - cu0 + per_row - 1) / per_row : 0;
-    int* tcount = reinterpret_cast<int*>(smem + a.off_c);
-    int* sorted = tcount + ncu;
-    for (int u = threadIdx.x; u < ncu; u += kBlendConsumers) tcount[u] = unit_terms<U>(p, u * U, W);
-    if (!consumer_sync()) return (void)atomicOr(&g_device_error, kErrBlendWait);
-    for (int u = threadIdx.x; u < ncu; u += kBlendConsumers) {
-        const int ku = tcount[u];
-        int rank = 0;
-        for (int j = 0; j < ncu; ++j) {
-            const int kj = tcount[j];
-            rank += (kj < ku) || (kj == ku && j < u);
-        }
-        sorted[rank] = u;
-    }
-    if (!consumer_sync()) return (void)atomicOr(&g_device_error, kErrBlendWait);
+    auto unit_of = [&](int i) -> int { return a.ordered ? static_cast<int>(a.order[i]) : i; };
     Terms<U, KT> tm;
     tm.n = 0;
     bool lane_copy = false;
     if (ncu_mine == 1) {
-        load_terms<U, KT>(p, sorted[cu0] * U, W, tm);
+        load_terms<U, KT>(p, unit_of(cu0) * U, W, tm);
         lane_copy = tm.n == 1 && sizeof(Tin) == sizeof(Tout);
 #pragma unroll
         for (int v = 0; v < U; ++v) lane_copy = lane_copy && tm.in[0][v] && tm.w[0][v] == 1.0f;
@@ -908,73 +909,75 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
             c = blend_box(p, a, cur.fb);
             box_fb = cur.fb;
             if (!consumer_sync()) return (void)atomicOr(&g_device_error, kErrBlendWait);
-            if (warp == 1) {
-                // runs: a row opens one when its pair list or its all-ones
-                // flag differs from the previous row's
-                const float wf0 = axis_weight(p, 0, c.if_lo, c.f);
-                int carry = 0, prev_key = -1;
-                for (int r0 = 0; r0 < c.rows; r0 += 32) {
-                    const int r = r0 + lane;
-                    const bool valid = r < c.rows;
-                    int lo = 0, hi = 0, key = -1;
-                    bool ones = false;
-                    if (valid) {
-                        tdp::axis_cover(p, 1, c.hb0 + r, lo, hi);
-                        ones = c.NF == 1 && lo == hi && __fmul_rn(wf0, axis_weight(p, 1, lo, c.hb0 + r)) == 1.0f;
-                        key = lo | (hi << 8) | (int(ones) << 16);
-                    }
-                    int pk = __shfl_up_sync(0xffffffffu, key, 1);
-                    if (lane == 0) pk = prev_key;
-                    const bool start = valid && key != pk;
-                    const unsigned bal = __ballot_sync(0xffffffffu, start);
-                    if (start) {
-                        Run& R = runs[carry + __popc(bal & ((1u << lane) - 1u))];
-                        R.r0 = r;
-                        R.nc = c.NF * (hi - lo + 1);
-                        R.ones = ones;
-                        int m = 0;
-                        for (int fa = 0; fa < c.NF; ++fa)
-                            for (int ih = lo; ih <= hi; ++ih) R.slot0b[m++] = 4 * (fa * c.NH + ih - c.ih_lo) * nw;
-                        for (; m < 4; ++m) R.slot0b[m] = 0;
-                    }
-                    carry += __popc(bal);
-                    prev_key = __shfl_sync(0xffffffffu, key, 31);
+            // w_fh = r_f * r_h per band row and pair (frame tile major), one
+            // row per thread
+            for (int r = threadIdx.x; r < c.rows; r += kBlendConsumers) {
+                const int h = c.hb0 + r;
+                int lo, hi;
+                tdp::axis_cover(p, 1, h, lo, hi);
+                int m = 0;
+                for (int fa = 0; fa < c.NF; ++fa) {
+                    const float wf = axis_weight(p, 0, c.if_lo + fa, c.f);
+                    for (int ih = lo; ih <= hi; ++ih) wts[r * KC + m++] = __fmul_rn(wf, axis_weight(p, 1, ih, h));
                 }
-                __syncwarp();
-                for (int i = lane; i < carry; i += 32) runs[i].r1 = i + 1 < carry ? runs[i + 1].r0 : c.rows;
-                __syncwarp();
-                if (lane == 0) {
-                    // row-group blocks: contiguous rows, split where the
-                    // running pair count crosses g / RG of the band's total
-                    int total = 0;
-                    for (int i = 0; i < carry; ++i) total += runs[i].nc * (runs[i].r1 - runs[i].r0);
-                    hdr[0] = carry;
-                    hdr[1] = 0;
-                    int g = 1, acc = 0;
-                    for (int i = 0; i < carry && g < RG; ++i) {
-                        const int nc = runs[i].nc, len = runs[i].r1 - runs[i].r0;
-                        while (g < RG) {
-                            const int target = (total * g + RG / 2) / RG;
-                            if (acc + nc * len < target) break;
-                            hdr[1 + g] = runs[i].r0 + min(len, max(0, (target - acc + nc - 1) / nc));
-                            ++g;
-                        }
-                        acc += nc * len;
-                    }
-                    for (; g <= RG; ++g) hdr[1 + g] = c.rows;
-                }
-            } else if (warp >= 2) {
-                // per row and pair (frame tile major): w_fh = r_f * r_h
-                for (int r = threadIdx.x - 64; r < c.rows; r += kBlendConsumers - 64) {
-                    const int h = c.hb0 + r;
-                    int lo, hi;
-                    tdp::axis_cover(p, 1, h, lo, hi);
+            }
+            // runs: the rows between consecutive starts and ends of the row
+            // tiles meeting the band (where the covering tiles change)
+            if (threadIdx.x == 0) {
+                const int nh = p.num_tiles[1];
+                int lo, hi;
+                tdp::axis_cover(p, 1, c.hb0, lo, hi);
+                int h = c.hb0, nr = 0;
+                while (h < c.hb1) {
+                    int nxt = min(p.end[1][lo], c.hb1);
+                    if (hi + 1 < nh) nxt = min(nxt, p.start[1][hi + 1]);
+                    Run& R = runs[nr++];
+                    R.r0 = h - c.hb0;
+                    R.r1 = nxt - c.hb0;
+                    R.nc = c.NF * (hi - lo + 1);
+                    R.ones = 0;
                     int m = 0;
-                    for (int fa = 0; fa < c.NF; ++fa) {
-                        const float wf = axis_weight(p, 0, c.if_lo + fa, c.f);
-                        for (int ih = lo; ih <= hi; ++ih) wts[r * KC + m++] = __fmul_rn(wf, axis_weight(p, 1, ih, h));
-                    }
+                    for (int fa = 0; fa < c.NF; ++fa)
+                        for (int ih = lo; ih <= hi; ++ih) R.slot0b[m++] = 4 * (fa * c.NH + ih - c.ih_lo) * nw;
+                    for (; m < 4; ++m) R.slot0b[m] = 0;
+                    if (p.end[1][lo] == nxt) ++lo;
+                    if (hi + 1 < nh && p.start[1][hi + 1] == nxt) ++hi;
+                    h = nxt;
                 }
+                hdr[0] = nr;
+            }
+            if (!consumer_sync()) return (void)atomicOr(&g_device_error, kErrBlendWait);
+            if (warp == 0) {
+                const int nr = hdr[0];
+                // a one-pair run is all ones when w_fh is 1 on its first and
+                // last rows: r_h is a rising ramp times a falling one, each at
+                // most 1, so it is 1 in between too
+                for (int i = lane; i < nr; i += 32) {
+                    Run& R = runs[i];
+                    R.ones = R.nc == 1 && wts[R.r0 * KC] == 1.0f && wts[(R.r1 - 1) * KC] == 1.0f;
+                }
+                // row-group blocks: contiguous rows, split where the running
+                // pair count crosses g / RG of the band's total (RG and nc are
+                // powers of two)
+                if (lane < RG) {
+                    int b = lane == 0 ? 0 : c.rows;
+                    if (lane > 0) {
+                        int total = 0;
+                        for (int i = 0; i < nr; ++i) total += runs[i].nc * (runs[i].r1 - runs[i].r0);
+                        const int target = (total * lane + (RG >> 1)) >> (__ffs(RG) - 1);
+                        int acc = 0;
+                        for (int i = 0; i < nr; ++i) {
+                            const int nc = runs[i].nc, len = runs[i].r1 - runs[i].r0;
+                            if (acc + nc * len >= target) {
+                                b = runs[i].r0 + min(len, max(0, (target - acc + nc - 1) >> (__ffs(nc) - 1)));
+                                break;
+                            }
+                            acc += nc * len;
+                        }
+                    }
+                    hdr[1 + lane] = b;
+                }
+                if (lane == 0) hdr[1 + RG] = c.rows;
             }
             if (!consumer_sync()) return (void)atomicOr(&g_device_error, kErrBlendWait);
             nruns = hdr[0];
@@ -992,7 +995,7 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
         constexpr int esz = static_cast<int>(sizeof(Tin));
         Tout* const out_band = out + ((long long)cur.bc * F + c.f) * H * W + (long long)c.hb0 * W;
         for (int m = 0; m < ncu_mine; ++m) {
-            const int cu = sorted[cu0 + m * per_row];
+            const int cu = unit_of(cu0 + m * per_row);
             if (ncu_mine > 1) load_terms<U, KT>(p, cu * U, W, tm);
             // per term: byte offsets of the columns in the tile row, of one
             // tile row, and of the term's entry in the run-base table
@@ -1069,7 +1072,7 @@ __global__ void __launch_bounds__(kThreads) blend_generic_kernel(const __grid_co
     const BlendBox c = blend_box(p, a, fb);
     const uintptr_t limit = reinterpret_cast<uintptr_t>(tiles + a.tiles_numel) & ~uintptr_t(15);
 
-    if (threadIdx.x == 0) mbar_init(bar, 1);
+    if (threadIdx.x == 0) mbar_init(bar, 32);
     __syncthreads();
     if (threadIdx.x < 32) {
         blend_build_stage_table<Tin>(p, a, c, table);
@@ -1583,8 +1586,7 @@ BlendLayout blend_layout(const tdp_plan_t& p, int band_rows, int esz) {
     if (L.fast) {
         L.off_a = o; o = round_up(o + 64 + band_rows * (int)sizeof(Run), 16);         // header, runs
         L.off_b = o; o = round_up(o + band_rows * kf * kh * 4, 16);                   // w_fh per row and pair
-        L.off_c = o; o = round_up(o + 8 * W, 16);                                     // column order
-        L.off_d = L.off_e = o;
+        L.off_c = L.off_d = L.off_e = o;
     } else {
         L.off_a = o; o = round_up(o + kf * (int)sizeof(Cov), 16);                     // fcov
         L.off_b = o; o = round_up(o + band_rows * 4, 16);                             // hcnt
@@ -1700,6 +1702,30 @@ tdp_status launch_blend(const tdp_plan_t& p, int BC, const void* tiles, long lon
     a.kf = p.max_cover[0];
     a.kh = p.max_cover[1];
     a.kw = p.max_cover[2];
+    const bool pairs = p.dims[2] % 2 == 0;
+    {
+        // column units ordered by the number of column tiles they touch
+        // (stable), so that the consumer warps share one term count
+        const int U = pairs ? 2 : 1, W = p.dims[2], ncu = (W + U - 1) / U;
+        a.ordered = ncu <= kMaxOrdered ? 1 : 0;
+        if (a.ordered) {
+            uint8_t cls[kMaxOrdered];
+            int count[kMaxOrdered + 2] = {0};
+            for (int u = 0; u < ncu; ++u) {
+                int lo, hi, l2, h2;
+                tdp::axis_cover(p, 2, u * U, lo, hi);
+                for (int v = 1; v < U && u * U + v < W; ++v) {
+                    tdp::axis_cover(p, 2, u * U + v, l2, h2);
+                    lo = std::min(lo, l2);
+                    hi = std::max(hi, h2);
+                }
+                cls[u] = static_cast<uint8_t>(hi - lo + 1);
+                ++count[cls[u] + 1];
+            }
+            for (int k = 1; k <= kMaxOrdered + 1; ++k) count[k] += count[k - 1];   // first slot per class
+            for (int u = 0; u < ncu; ++u) a.order[count[cls[u]]++] = static_cast<uint16_t>(u);
+        }
+    }
     auto launch = [&](auto kernel, bool persistent) -> tdp_status {
         tdp_status st = set_smem(kernel, L.total);
         if (st != TDP_OK) return st;
@@ -1711,7 +1737,6 @@ tdp_status launch_blend(const tdp_plan_t& p, int BC, const void* tiles, long lon
     };
     // Pair stores need every output row to start on a 4-byte (bf16) or
     // 8-byte (fp32) boundary: W even.
-    const bool pairs = p.dims[2] % 2 == 0;
     if (!L.fast) return launch(blend_generic_kernel<Tin, Tout>, false);
     const int kt = max_terms(p, pairs ? 2 : 1);
     if (pairs) {
