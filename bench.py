@@ -4,9 +4,10 @@
 One step is one pass of every step of the path on the 4K-class workload
 (bf16 latent B=1, C=128, F=16, H=68, W=120; tiles 2x4x4 with overlaps
 2/8/12; 256 conditioning tokens, 64 with a negative time start):
-    tdp_extract, then tdp_blend concurrently with tdp_positions ->
-    tdp_cond_select -> tdp_window_sum on a second stream (they are
-    independent of extract and blend); the step ends when both are done.
+    tdp_extract, tdp_tokens (positions and conditioning selection in one
+    launch, plus the per-token count), tdp_window_sum, tdp_blend, in order
+    on one stream (the blend's persistent grid fills every SM, so the short
+    token kernels gain nothing from a second stream).
 The per-tile op between extract and blend is the caller's (here identity,
 outside the path).  Inputs are resident in HBM when the timed region starts;
 L2 is flushed (a 256 MiB write) before every step and before the blend,
@@ -44,7 +45,7 @@ from overlap_add_blending_gb300.workloads import WORKLOADS  # noqa: E402
 WORKLOAD = WORKLOADS["4k"]
 METRIC = "tile extract+blend HBM GB/s (fraction of GB300 peak) and latent elems/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_STEP = 6  # extract, positions, cond select (2), blend, window sum
+KERNELS_PER_STEP = 5  # extract, tokens (2: per-tile kernel, per-token count), window sum, blend
 
 
 def esz(dtype: str) -> int:
@@ -65,7 +66,7 @@ def config_dict(wl, note: str) -> dict:
                         f"W={wl.dims[2]}, tiles (frames {wl.tiling[0][0]}/{wl.tiling[0][1]}, height "
                         f"{wl.tiling[1][0]}/{wl.tiling[1][1]}, width {wl.tiling[2][0]}/{wl.tiling[2][1]}), "
                         f"{wl.num_cond} conditioning tokens ({wl.num_cond_negative} with negative time)",
-            "step": "extract, then blend || (positions, cond_select, window_sum on a second stream); "
+            "step": "extract, tokens (positions + cond select), window_sum, blend on one stream; "
                     "per-tile op: identity, outside",
             "l2": note}
 
@@ -261,46 +262,32 @@ def run_tdp(args, rank: int, world: int):
     cond = torch.from_numpy(cond_np).to(dev)
     tiles = torch.empty(p.tiles_numel(wl.B, wl.C), dtype=dt, device=dev)
     out = torch.empty_like(X)
-    tile_pos = torch.empty(6 * wl.B * p.tokens_numel(), dtype=torch.int32, device=dev)
-    offsets = torch.empty((p.T, wl.B, 3), dtype=torch.int32, device=dev)
-    cond_out = {}
+    tok_out = {}
     maxdev = torch.empty(4, dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     def path():
         tdp.extract(p, X, tiles)
-        tdp.positions(p, gen, True, tile_pos, offsets)
-        tdp.cond_select(p, gen, cond, True, True, cond_out)
-        tdp.blend(p, tiles, wl.B, wl.C, out)
+        tdp.tokens(p, gen, cond, True, True, tok_out)
         tdp.window_sum(p, maxdev)
+        tdp.blend(p, tiles, wl.B, wl.C, out)
 
-    # One step: extract, then the blend on the main stream while positions,
-    # conditioning selection and the window sum (independent of extract and
-    # blend) run on a side stream; the step ends when both are done.  Events bracket every
-    # kernel on the stream it is launched on.  L2 is flushed before the step
-    # and again before the blend, outside the timed spans: in use, the
-    # per-tile model runs between extract and blend.
-    side = torch.cuda.Stream(device=dev, priority=-1)   # short latency-bound kernels first
-
-    def timed_step(ev, es):
+    # One step: extract, tokens, window sum, blend, on one stream.  Events
+    # bracket extract, the token and window kernels (no event between them,
+    # so each may start while the previous one finishes) and the blend.  L2
+    # is flushed before the step and again after extract, outside the timed
+    # spans: in use, the per-tile model runs between extract and the rest.
+    def timed_step(ev):
         ev[0].record(stream)
         tdp.extract(p, X, tiles)
         ev[1].record(stream)
         flush.zero_()
         ev[2].record(stream)
-        side.wait_event(ev[2])
-        with torch.cuda.stream(side):
-            es[0].record(side)
-            tdp.positions(p, gen, True, tile_pos, offsets, stream=side)
-            es[1].record(side)
-            tdp.cond_select(p, gen, cond, True, True, cond_out, stream=side)
-            es[2].record(side)
-            tdp.window_sum(p, maxdev, stream=side)
-            es[3].record(side)
-        tdp.blend(p, tiles, wl.B, wl.C, out)
+        tdp.tokens(p, gen, cond, True, True, tok_out)
+        tdp.window_sum(p, maxdev)
         ev[3].record(stream)
-        stream.wait_event(es[3])
+        tdp.blend(p, tiles, wl.B, wl.C, out)
         ev[4].record(stream)
 
     # host enqueue time of one step, to size the head start given to the host
@@ -327,12 +314,11 @@ def run_tdp(args, rank: int, world: int):
 
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
-    ess = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     wall0 = time.perf_counter()
     for k in range(K):
         flush.zero_()
         torch.cuda._sleep(sleep_cycles)      # the host enqueues the whole step meanwhile
-        timed_step(evs[k], ess[k])
+        timed_step(evs[k])
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if world > 1:
@@ -340,14 +326,13 @@ def run_tdp(args, rank: int, world: int):
     torch.cuda.synchronize()
     clocks = sampler.stop()
 
-    # step = extract + fork .. join (blend || side stream)
+    # step = extract + (tokens, window sum, blend)
     step = np.array([evs[k][0].elapsed_time(evs[k][1]) + evs[k][2].elapsed_time(evs[k][4]) for k in range(K)])
-    seg = np.array([[evs[k][0].elapsed_time(evs[k][1]), ess[k][0].elapsed_time(ess[k][1]),
-                     ess[k][1].elapsed_time(ess[k][2]), evs[k][2].elapsed_time(evs[k][3]),
-                     ess[k][2].elapsed_time(ess[k][3])] for k in range(K)])  # ms
+    seg = np.array([[evs[k][0].elapsed_time(evs[k][1]), evs[k][2].elapsed_time(evs[k][3]),
+                     evs[k][3].elapsed_time(evs[k][4])] for k in range(K)])  # ms
     step_ms = float(step.mean())
     per_kernel_ms = seg.mean(axis=0)
-    names = ["extract", "positions", "cond_select", "blend", "window_sum"]
+    names = ["extract", "tokens_and_window_sum", "blend"]
 
     # e2e: host buffers in, blended latent out, through the same C-ABI calls
     X_h = X.cpu().pin_memory()

@@ -205,6 +205,26 @@ tdp_status tdp_cond_select(const tdp_plan_t* plan, int32_t B, const int32_t* gen
                            cudaStream_t stream);
 
 /*
+ * tdp_tokens -- steps 3 and 4 in one launch: tdp_positions and
+ * tdp_cond_select over the same tiles, sharing one pass over the generated
+ * positions (the tile extent is reduced once and serves both).
+ *
+ * Source: "Tiled Data Parallelism (TDP)", Position normalization and
+ * Shared negative (reference) positions, as for the two calls above.
+ * Arguments mean what they mean there.  tile_pos NULL skips the positions
+ * (offsets may then be NULL too); M == 0 skips the conditioning tokens
+ * (cond_pos, keep, count and weight may then be NULL); tile_extent, when
+ * not NULL, receives [TS, TE) per tile, batch and axis (required when
+ * M > 0).  Every result equals what the separate calls write.
+ * Bit-exact.  Asynchronous on `stream`.
+ */
+tdp_status tdp_tokens(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos,
+                      int32_t normalize, int32_t* tile_pos, int32_t* offsets, int32_t M,
+                      const int32_t* cond_pos, int32_t* tile_extent, uint8_t* keep,
+                      int32_t* count, float* weight, int32_t* kept_idx, int32_t* num_kept,
+                      int32_t* tile_cond_pos, cudaStream_t stream);
+
+/*
  * tdp_blend -- step 5, fused separable trapezoid window + overlap-add (K2).
  *
  * Source: "Tiled Data Parallelism (TDP)", What it is (overlapping regions

@@ -134,6 +134,15 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity) {
     return !__syncthreads_or(!ok);
 }
 
+// Programmatic dependent launch.  Every kernel here is launched so that it
+// may start while the previous kernel in the stream finishes; it lets its
+// own dependents start early, and waits for the previous kernel to complete
+// (and its memory to be visible) before the first global access that kernel
+// could have produced or could still be reading.  Launched without the
+// attribute, the wait returns at once.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // The plan is a __grid_constant__ kernel parameter; indexed reads of it with
@@ -374,8 +383,10 @@ template <typename E>
 __global__ void __launch_bounds__(kThreads, 5) extract_kernel(const __grid_constant__ tdp_plan_t pg,
                                                            const ExtractArgs a) {
     __shared__ tdp_plan_t p;
+    pdl_launch_dependents();
     load_plan(&p, pg);
     __syncthreads();
+    pdl_wait();   // latent (read) and tiles (written) may belong to the previous kernel
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     ExtractSlot* slots = reinterpret_cast<ExtractSlot*>(smem + a.off_slots);
@@ -774,6 +785,7 @@ template <typename Tin, typename Tout, int U, int KT>
 __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __grid_constant__ tdp_plan_t pg,
                                                                    const BlendArgs a) {
     __shared__ tdp_plan_t p;
+    pdl_launch_dependents();
     load_plan(&p, pg);
     __syncthreads();
     extern __shared__ __align__(128) unsigned char smem[];
@@ -824,6 +836,7 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
             return r;
         };
         int kst = 0;
+        pdl_wait();   // the tiles may come from the previous kernel
         for (; kst < n && ok; ++kst, ahead.next()) {
             if (ahead.fb != table_fb) {
                 const BlendBox cn = blend_box(p, a, ahead.fb);
@@ -902,6 +915,7 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
     int box_fb = -1;
     BlendBox c{};
     int nruns = 0, rb0 = 0, rb1 = 0;
+    pdl_wait();   // the previous kernel may still read `out`
     for (int k = 0; k < n; ++k, cur.next()) {
         if (cur.fb != box_fb) {
             // new (frame, band): rebuild the row tables once every consumer
@@ -1053,8 +1067,10 @@ template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(kThreads) blend_generic_kernel(const __grid_constant__ tdp_plan_t pg,
                                                                  const BlendArgs a) {
     __shared__ tdp_plan_t p;
+    pdl_launch_dependents();
     load_plan(&p, pg);
     __syncthreads();
+    pdl_wait();
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     Cov* fcov = reinterpret_cast<Cov*>(smem + a.off_a);
@@ -1136,6 +1152,8 @@ __global__ void __launch_bounds__(kThreads) blend_generic_kernel(const __grid_co
 // inner(w) per column in shared memory (kf, kh: most tiles covering an index).
 __global__ void __launch_bounds__(kThreads) window_sum_kernel(const __grid_constant__ tdp_plan_t p, float* max_abs_dev,
                                                               float* sum_out, int tables) {
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ __align__(16) unsigned char wsm[];
     const int F = p.dims[0], H = p.dims[1], W = p.dims[2];
     const int kf = p.max_cover[0], kh = p.max_cover[1];
@@ -1209,6 +1227,103 @@ __global__ void __launch_bounds__(kThreads) window_sum_kernel(const __grid_const
     }
 }
 
+// max |S - 1| alone (no per-element output), in one CTA.  S(f,h,w)
+// depends on (f, h, w) only through each axis's tuple of covering-tile
+// weights (for w: through inner(w)), and equal tuples give the same S bit
+// for bit, so the maximum over the whole volume is the maximum over the
+// triples of one representative index per run of equal tuples on each
+// axis.  The tables are those of window_sum_kernel; the representatives
+// follow them in shared memory.
+__device__ __forceinline__ bool same_tuple(const int* cnt, const float* w, int k, int x, int y) {
+    if (cnt[x] != cnt[y]) return false;
+    for (int i = 0; i < cnt[x]; ++i)
+        if (__float_as_uint(w[x * k + i]) != __float_as_uint(w[y * k + i])) return false;
+    return true;
+}
+
+// Compacts the first index of every run of equal tuples on an axis of n
+// indices into rep[]; returns the number of runs.  Whole CTA.
+template <typename Same>
+__device__ int axis_runs(int n, int* rep, int* scan_sh, Same same) {
+    int carry = 0;
+    for (int x0 = 0; x0 < n; x0 += blockDim.x) {
+        const int x = x0 + threadIdx.x;
+        const int start = (x < n) && (x == 0 || !same(x, x - 1)) ? 1 : 0;
+        int round_total;
+        const int at = carry + block_excl_scan(start, scan_sh, &round_total);
+        if (start) rep[at] = x;
+        carry += round_total;
+    }
+    __syncthreads();
+    return carry;
+}
+
+__global__ void __launch_bounds__(kThreads) window_max_kernel(const __grid_constant__ tdp_plan_t p, float* max_abs_dev) {
+    pdl_launch_dependents();
+    extern __shared__ __align__(16) unsigned char wsm[];
+    __shared__ int scan_sh[33];
+    __shared__ float warp_worst[kThreads / 32];
+    const int F = p.dims[0], H = p.dims[1], W = p.dims[2];
+    const int kf = p.max_cover[0], kh = p.max_cover[1];
+    float* wf = reinterpret_cast<float*>(wsm);          // [F][kf]
+    float* wh = wf + F * kf;                             // [H][kh]
+    float* winner = wh + H * kh;                         // [W]
+    int* fcnt = reinterpret_cast<int*>(winner + W);      // [F]
+    int* hcnt = fcnt + F;                                // [H]
+    int* frep = hcnt + H;                                // [F] run representatives
+    int* hrep = frep + F;                                // [H]
+    int* wrep = hrep + H;                                // [W]
+    for (int f = threadIdx.x; f < F; f += blockDim.x) {
+        int lo, hi;
+        tdp::axis_cover(p, 0, f, lo, hi);
+        fcnt[f] = hi - lo + 1;
+        for (int i = lo; i <= hi; ++i) wf[f * kf + (i - lo)] = axis_weight(p, 0, i, f);
+    }
+    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+        int lo, hi;
+        tdp::axis_cover(p, 1, h, lo, hi);
+        hcnt[h] = hi - lo + 1;
+        for (int i = lo; i <= hi; ++i) wh[h * kh + (i - lo)] = axis_weight(p, 1, i, h);
+    }
+    for (int w = threadIdx.x; w < W; w += blockDim.x) {
+        int lo, hi;
+        tdp::axis_cover(p, 2, w, lo, hi);
+        float inner = 0.0f;
+        for (int k = lo; k <= hi; ++k) inner = fmaf(axis_weight(p, 2, k, w), 1.0f, inner);
+        winner[w] = inner;
+    }
+    __syncthreads();
+    const int nf = axis_runs(F, frep, scan_sh, [&](int x, int y) { return same_tuple(fcnt, wf, kf, x, y); });
+    const int nh = axis_runs(H, hrep, scan_sh, [&](int x, int y) { return same_tuple(hcnt, wh, kh, x, y); });
+    const int nwc = axis_runs(W, wrep, scan_sh,
+                              [&](int x, int y) { return __float_as_uint(winner[x]) == __float_as_uint(winner[y]); });
+    float worst = 0.0f;
+    for (int idx = threadIdx.x; idx < nh * nwc; idx += blockDim.x) {   // (row class, column class)
+        const int hi = idx / nwc, h = hrep[hi];
+        const float in_w = winner[wrep[idx - hi * nwc]];
+        for (int fi = 0; fi < nf; ++fi) {
+            const int f = frep[fi];
+            float S = 0.0f;
+            for (int i = 0; i < fcnt[f]; ++i) {
+                const float a_f = wf[f * kf + i];
+                for (int j = 0; j < hcnt[h]; ++j) S = fmaf(__fmul_rn(a_f, wh[h * kh + j]), in_w, S);
+            }
+            worst = fmaxf(worst, fabsf(S - 1.0f));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) worst = fmaxf(worst, __shfl_xor_sync(0xffffffffu, worst, o));
+    if ((threadIdx.x & 31) == 0) warp_worst[threadIdx.x >> 5] = worst;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float m = 0.0f;
+        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) m = fmaxf(m, warp_worst[i]);
+        pdl_wait();   // the plan alone went in; the result may still be read by the previous kernel
+        *max_abs_dev = m;
+    }
+    pdl_wait();       // finish after the previous kernel, so that finishing implies it finished
+}
+
 // =================================================================== K4 / K5: tokens
 struct TileTokens {
     int f0, h0, w0, sf, sh, sw, n;
@@ -1230,14 +1345,6 @@ __device__ __forceinline__ TileTokens tile_tokens(const tdp_plan_t& p, int t) {
     return tt;
 }
 
-// Global token index of tile-local token j.
-__device__ __forceinline__ int global_token(const tdp_plan_t& p, const TileTokens& tt, int j) {
-    const int x = j % tt.sw;
-    const int r = j / tt.sw;
-    const int y = r % tt.sh, k = r / tt.sh;
-    return ((tt.f0 + k) * p.dims[1] + tt.h0 + y) * p.dims[2] + tt.w0 + x;
-}
-
 __device__ __forceinline__ int warp_min(int v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -1249,162 +1356,23 @@ __device__ __forceinline__ int warp_max(int v) {
     return v;
 }
 
-// Cluster-wide [min start, max end) of tile t's generated tokens, per axis.
-// Each CTA of the cluster reduces a chunk of the tile's tokens; the chunks
-// are combined through distributed shared memory.  ext_sh: 6 ints of this
-// CTA's shared memory.  Leaves the result in ext[6]; a final cluster.sync
-// by the caller must follow before any CTA exits.
-__device__ void tile_extent_cluster(const tdp_plan_t& p, const TileTokens& tt, const int* gen, int b, long long N,
-                                    int* ext_sh, int ext[6]) {
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rank = static_cast<int>(cluster.block_rank());
-    const int csize = static_cast<int>(cluster.num_blocks());
-    if (threadIdx.x < 3) { ext_sh[2 * threadIdx.x] = INT_MAX; ext_sh[2 * threadIdx.x + 1] = INT_MIN; }
-    __syncthreads();
-    const int chunk = (tt.n + csize - 1) / csize;
-    const int j0 = rank * chunk, j1 = min(tt.n, j0 + chunk);
-    int mn[3] = {INT_MAX, INT_MAX, INT_MAX}, mx[3] = {INT_MIN, INT_MIN, INT_MIN};
-    for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
-        const long long n = global_token(p, tt, j);
-#pragma unroll
-        for (int d = 0; d < 3; ++d) {
-            const int2 v = *reinterpret_cast<const int2*>(gen + (((long long)b * 3 + d) * N + n) * 2);
-            mn[d] = min(mn[d], v.x);
-            mx[d] = max(mx[d], v.y);
-        }
-    }
-#pragma unroll
-    for (int d = 0; d < 3; ++d) {
-        mn[d] = warp_min(mn[d]);
-        mx[d] = warp_max(mx[d]);
-    }
-    if ((threadIdx.x & 31) == 0) {
-#pragma unroll
-        for (int d = 0; d < 3; ++d) {
-            atomicMin(&ext_sh[2 * d], mn[d]);
-            atomicMax(&ext_sh[2 * d + 1], mx[d]);
-        }
-    }
-    cluster.sync();
-#pragma unroll
-    for (int d = 0; d < 3; ++d) { ext[2 * d] = INT_MAX; ext[2 * d + 1] = INT_MIN; }
-    for (int r = 0; r < csize; ++r) {
-        const int* peer = cluster.map_shared_rank(ext_sh, r);
-#pragma unroll
-        for (int d = 0; d < 3; ++d) {
-            ext[2 * d] = min(ext[2 * d], peer[2 * d]);
-            ext[2 * d + 1] = max(ext[2 * d + 1], peer[2 * d + 1]);
-        }
-    }
-}
-
-struct PositionsArgs {
+struct TokensArgs {
     const int* gen;
+    int B, normalize;
+    // positions (tile_pos NULL: not written)
     int* tile_pos;
     int* offsets;
-    int B;
-    int normalize;
-};
-
-constexpr int kPosCache = 4;   // tokens per thread kept in registers between reduce and write
-
-// One 8-CTA cluster per (tile, batch).  Each CTA reads its chunk of the
-// tile's generated tokens once, keeping them in registers (up to kPosCache
-// per thread); the chunk minima meet through distributed shared memory; the
-// CTA then writes its chunk shifted by the tile's per-axis minimum start.
-// Chunks longer than the register cache are read a second time.  Every plan
-// read here is uniform across the CTA, so the plan stays a parameter.
-__global__ void __launch_bounds__(kThreads) positions_kernel(const __grid_constant__ tdp_plan_t p,
-                                                             const PositionsArgs a) {
-    __shared__ int ext_sh[6];
-    cg::cluster_group cluster = cg::this_cluster();
-    const int tb = blockIdx.x / kCluster;
-    const int t = tb / a.B, b = tb % a.B;
-    const long long N = (long long)p.dims[0] * p.dims[1] * p.dims[2];
-    const TileTokens tt = tile_tokens(p, t);
-    const int rank = static_cast<int>(cluster.block_rank());
-    const int chunk = (tt.n + kCluster - 1) / kCluster;
-    const int j0 = rank * chunk, j1 = min(tt.n, j0 + chunk);
-    const int* gen_b = a.gen + (long long)b * 3 * N * 2;
-    const bool cached = chunk <= kPosCache * static_cast<int>(blockDim.x);
-    int2 v[kPosCache][3];
-    int mn[3] = {INT_MAX, INT_MAX, INT_MAX};
-    if (threadIdx.x < 6) ext_sh[threadIdx.x] = (threadIdx.x & 1) ? INT_MIN : INT_MAX;
-    if (cached) {
-#pragma unroll
-        for (int k = 0; k < kPosCache; ++k) {
-            const int j = j0 + static_cast<int>(threadIdx.x) + k * static_cast<int>(blockDim.x);
-            if (j < j1) {
-                const long long n = global_token(p, tt, j);
-#pragma unroll
-                for (int d = 0; d < 3; ++d) {
-                    v[k][d] = *reinterpret_cast<const int2*>(gen_b + ((long long)d * N + n) * 2);
-                    mn[d] = min(mn[d], v[k][d].x);
-                }
-            }
-        }
-    } else {
-        for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
-            const long long n = global_token(p, tt, j);
-#pragma unroll
-            for (int d = 0; d < 3; ++d) mn[d] = min(mn[d], gen_b[((long long)d * N + n) * 2]);
-        }
-    }
-#pragma unroll
-    for (int d = 0; d < 3; ++d) mn[d] = warp_min(mn[d]);
-    __syncthreads();  // ext_sh initialised
-    if ((threadIdx.x & 31) == 0) {
-#pragma unroll
-        for (int d = 0; d < 3; ++d) atomicMin(&ext_sh[2 * d], mn[d]);
-    }
-    cluster.sync();
-    int off[3] = {INT_MAX, INT_MAX, INT_MAX};
-    for (int r = 0; r < kCluster; ++r) {
-        const int* peer = cluster.map_shared_rank(ext_sh, r);
-#pragma unroll
-        for (int d = 0; d < 3; ++d) off[d] = min(off[d], peer[2 * d]);
-    }
-    // Arrive now (this CTA is done reading its peers), wait at the end: the
-    // barrier's latency overlaps the writes, and no CTA leaves while a peer
-    // may still read its minima.
-    cluster.barrier_arrive();
-    if (rank == 0 && threadIdx.x < 3) a.offsets[((long long)t * a.B + b) * 3 + threadIdx.x] = off[threadIdx.x];
-    if (!a.normalize) off[0] = off[1] = off[2] = 0;
-    int* dst = a.tile_pos + tt.prefix * 6 * a.B + (long long)b * 3 * tt.n * 2;
-    if (cached) {
-#pragma unroll
-        for (int k = 0; k < kPosCache; ++k) {
-            const int j = j0 + static_cast<int>(threadIdx.x) + k * static_cast<int>(blockDim.x);
-            if (j < j1) {
-#pragma unroll
-                for (int d = 0; d < 3; ++d)
-                    *reinterpret_cast<int2*>(dst + ((long long)d * tt.n + j) * 2) =
-                        make_int2(v[k][d].x - off[d], v[k][d].y - off[d]);
-            }
-        }
-    } else {
-        for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
-            const long long n = global_token(p, tt, j);
-#pragma unroll
-            for (int d = 0; d < 3; ++d) {
-                const int2 x = *reinterpret_cast<const int2*>(gen_b + ((long long)d * N + n) * 2);
-                *reinterpret_cast<int2*>(dst + ((long long)d * tt.n + j) * 2) = make_int2(x.x - off[d], x.y - off[d]);
-            }
-        }
-    }
-    cluster.barrier_wait();
-}
-
-struct CondArgs {
-    const int* gen;
+    // conditioning selection (M = 0: none)
+    int M;
     const int* cond;
     int* extent;
     unsigned char* keep;
     int* kept_idx;
     int* num_kept;
     int* tile_cond;
-    int B, M, normalize;
 };
+
+constexpr int kPosCache = 4;   // tokens per thread kept in registers between reduce and write
 
 __device__ __forceinline__ bool cond_keep(const int* cond, int b, int M, int m, const int ext[6]) {
     const int2 t = *reinterpret_cast<const int2*>(cond + (((long long)b * 3 + 0) * M + m) * 2);
@@ -1418,67 +1386,242 @@ __device__ __forceinline__ bool cond_keep(const int* cond, int b, int M, int m, 
     return ok;
 }
 
-__global__ void __launch_bounds__(kThreads) cond_kernel(const __grid_constant__ tdp_plan_t p, const CondArgs a) {
+// Tile-local token j = (z, y, x) in a tile of sh rows of sw tokens, walked
+// in steps of `step` tokens without a division per token.
+struct TokenWalk {
+    int x, y, z, sx, sy, sz;
+    __device__ __forceinline__ void init(const TileTokens& tt, int j, int step) {
+        x = j % tt.sw;
+        const int r = j / tt.sw;
+        y = r % tt.sh;
+        z = r / tt.sh;
+        sx = step % tt.sw;
+        const int q = step / tt.sw;
+        sy = q % tt.sh;
+        sz = q / tt.sh;
+    }
+    __device__ __forceinline__ void next(const TileTokens& tt) {
+        x += sx;
+        y += sy;
+        z += sz;
+        if (x >= tt.sw) { x -= tt.sw; ++y; }
+        if (y >= tt.sh) { y -= tt.sh; ++z; }
+    }
+    __device__ __forceinline__ long long token(const tdp_plan_t& p, const TileTokens& tt) const {
+        return ((long long)(tt.f0 + z) * p.dims[1] + tt.h0 + y) * p.dims[2] + tt.w0 + x;
+    }
+};
+
+// Keep test of a conditioning token already in registers (c[d] = [start,
+// end) on axis d): a negative time start keeps it everywhere, else it must
+// overlap the extent on every axis.
+__device__ __forceinline__ bool keep_token(const int2 (&c)[3], const int ext[6]) {
+    if (c[0].x < 0) return true;
+    bool ok = true;
+#pragma unroll
+    for (int d = 0; d < 3; ++d) ok = ok && (c[d].x < ext[2 * d + 1]) && (c[d].y > ext[2 * d]);
+    return ok;
+}
+
+// One 8-CTA cluster per (tile, batch) does both token steps of the tile.
+// Each CTA reads its chunk of the tile's generated tokens once (kept in
+// registers, up to kPosCache per thread, when the positions are written),
+// and the chunk minima of the starts and maxima of the ends meet through
+// distributed shared memory: the tile's extent [TS, TE) per axis.  Then
+// (positions) the CTA writes its chunk shifted by TS, and (conditioning)
+// it tests its chunk of the conditioning tokens -- loaded before the
+// reduction when the chunk fits one pass of the CTA -- against the extent,
+// the chunks' kept counts meet through distributed shared memory, and it
+// writes its kept tokens, compacted in their original order.  Every plan
+// read here is uniform across the CTA, so the plan stays a parameter.
+__global__ void __launch_bounds__(kThreads) tokens_kernel(const __grid_constant__ tdp_plan_t p, const TokensArgs a) {
     __shared__ int ext_sh[6];
     __shared__ int scan_sh[33];
     __shared__ int kept_sh;
+    pdl_launch_dependents();
+    pdl_wait();   // positions may come from the previous kernel
     cg::cluster_group cluster = cg::this_cluster();
     const int tb = blockIdx.x / kCluster;
     const int t = tb / a.B, b = tb % a.B;
+    const int nthr = static_cast<int>(blockDim.x);
     const long long N = (long long)p.dims[0] * p.dims[1] * p.dims[2];
     const TileTokens tt = tile_tokens(p, t);
-    int ext[6];
-    tile_extent_cluster(p, tt, a.gen, b, N, ext_sh, ext);
     const int rank = static_cast<int>(cluster.block_rank());
-    if (rank == 0 && threadIdx.x < 6) a.extent[((long long)t * a.B + b) * 6 + threadIdx.x] = ext[threadIdx.x];
+    const int chunk = (tt.n + kCluster - 1) / kCluster;
+    const int j0 = min(tt.n, rank * chunk), j1 = min(tt.n, j0 + chunk);
+    const int* gen_b = a.gen + (long long)b * 3 * N * 2;
+    const bool pos = a.tile_pos != nullptr;
+    const bool cached = pos && chunk <= kPosCache * nthr;
+    if (threadIdx.x < 6) ext_sh[threadIdx.x] = (threadIdx.x & 1) ? INT_MIN : INT_MAX;
 
-    const long long row = (long long)t * a.B + b;  // (t, b) row of keep / kept_idx
-    const int chunk = (a.M + kCluster - 1) / kCluster;
-    const int m0 = min(a.M, rank * chunk), m1 = min(a.M, m0 + chunk);
-    // Pass 1: keep flags and this CTA's kept count.
-    int mine = 0;
-    for (int m = m0 + threadIdx.x; m < m1; m += blockDim.x) {
-        const bool k = cond_keep(a.cond, b, a.M, m, ext);
-        a.keep[row * a.M + m] = k ? 1 : 0;
-        mine += k;
-    }
-    int total_cta;
-    block_excl_scan(mine, scan_sh, &total_cta);
-    if (threadIdx.x == 0) kept_sh = total_cta;
-    cluster.sync();  // kept counts visible cluster-wide (also ends the extent reads)
-    int before = 0, total = 0;
-    for (int r = 0; r < kCluster; ++r) {
-        const int c = *cluster.map_shared_rank(&kept_sh, r);
-        if (r < rank) before += c;
-        total += c;
-    }
-    cluster.barrier_arrive();  // done reading peers; the matching wait ends the kernel
-    // Pass 2: compacted indices and shifted positions, original order.
-    if (a.kept_idx || a.tile_cond) {
-        int base = before;
-        for (int m00 = m0; m00 < m1; m00 += blockDim.x) {
-            const int m = m00 + threadIdx.x;
-            const bool k = (m < m1) && cond_keep(a.cond, b, a.M, m, ext);
-            int round_total;
-            const int pos = base + block_excl_scan(k ? 1 : 0, scan_sh, &round_total);
-            if (k) {
-                if (a.kept_idx) a.kept_idx[row * a.M + pos] = m;
-                if (a.tile_cond) {
+    // this CTA's conditioning tokens, loaded early when they fit one pass
+    const int mchunk = (a.M + kCluster - 1) / kCluster;
+    const int m0 = min(a.M, rank * mchunk), m1 = min(a.M, m0 + mchunk);
+    const bool one_pass = m1 - m0 <= nthr;
+    const int mm = m0 + static_cast<int>(threadIdx.x);
+    const bool have_c = one_pass && mm < m1;
+    int2 cv[3];
+    if (have_c) {
 #pragma unroll
-                    for (int d = 0; d < 3; ++d) {
-                        int2 v = *reinterpret_cast<const int2*>(a.cond + (((long long)b * 3 + d) * a.M + m) * 2);
-                        if (a.normalize) { v.x -= ext[2 * d]; v.y -= ext[2 * d]; }
-                        *reinterpret_cast<int2*>(a.tile_cond + ((row * 3 + d) * a.M + pos) * 2) = v;
-                    }
+        for (int d = 0; d < 3; ++d) cv[d] = *reinterpret_cast<const int2*>(a.cond + (((long long)b * 3 + d) * a.M + mm) * 2);
+    }
+
+    int2 v[kPosCache][3];
+    int mn[3] = {INT_MAX, INT_MAX, INT_MAX}, mx[3] = {INT_MIN, INT_MIN, INT_MIN};
+    TokenWalk tw;
+    tw.init(tt, j0 + static_cast<int>(threadIdx.x), nthr);
+    if (cached) {
+#pragma unroll
+        for (int k = 0; k < kPosCache; ++k) {
+            const int j = j0 + static_cast<int>(threadIdx.x) + k * nthr;
+            if (j < j1) {
+                const long long n = tw.token(p, tt);
+#pragma unroll
+                for (int d = 0; d < 3; ++d) {
+                    v[k][d] = *reinterpret_cast<const int2*>(gen_b + ((long long)d * N + n) * 2);
+                    mn[d] = min(mn[d], v[k][d].x);
+                    mx[d] = max(mx[d], v[k][d].y);
                 }
             }
-            base += round_total;
+            tw.next(tt);
         }
-        // Fill the slots after the last kept token: -1 indices, zero positions.
+    } else {
+        for (int j = j0 + threadIdx.x; j < j1; j += nthr, tw.next(tt)) {
+            const long long n = tw.token(p, tt);
+#pragma unroll
+            for (int d = 0; d < 3; ++d) {
+                const int2 x = *reinterpret_cast<const int2*>(gen_b + ((long long)d * N + n) * 2);
+                mn[d] = min(mn[d], x.x);
+                mx[d] = max(mx[d], x.y);
+            }
+        }
+    }
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        mn[d] = warp_min(mn[d]);
+        mx[d] = warp_max(mx[d]);
+    }
+    __syncthreads();  // ext_sh initialised
+    if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            atomicMin(&ext_sh[2 * d], mn[d]);
+            atomicMax(&ext_sh[2 * d + 1], mx[d]);
+        }
+    }
+    cluster.sync();
+    int ext[6];
+#pragma unroll
+    for (int d = 0; d < 3; ++d) { ext[2 * d] = INT_MAX; ext[2 * d + 1] = INT_MIN; }
+    for (int r = 0; r < kCluster; ++r) {
+        const int* peer = cluster.map_shared_rank(ext_sh, r);
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            ext[2 * d] = min(ext[2 * d], peer[2 * d]);
+            ext[2 * d + 1] = max(ext[2 * d + 1], peer[2 * d + 1]);
+        }
+    }
+    const long long row = (long long)t * a.B + b;  // (t, b) row of the per-tile outputs
+    if (rank == 0 && threadIdx.x < 3 && a.offsets) a.offsets[row * 3 + threadIdx.x] = ext[2 * threadIdx.x];
+    if (rank == 0 && threadIdx.x < 6 && a.extent) a.extent[row * 6 + threadIdx.x] = ext[threadIdx.x];
+
+    // Conditioning pass 1: keep flags and this CTA's kept count, which meet
+    // the other chunks' counts through distributed shared memory.
+    int before = 0, total = 0, at_in = 0;
+    bool kc = false;
+    if (a.M > 0) {
+        int total_cta;
+        if (one_pass) {
+            kc = have_c && keep_token(cv, ext);
+            if (have_c) a.keep[row * a.M + mm] = kc ? 1 : 0;
+            at_in = block_excl_scan(kc ? 1 : 0, scan_sh, &total_cta);
+        } else {
+            int mine = 0;
+            for (int m = m0 + threadIdx.x; m < m1; m += nthr) {
+                const bool k = cond_keep(a.cond, b, a.M, m, ext);
+                a.keep[row * a.M + m] = k ? 1 : 0;
+                mine += k;
+            }
+            block_excl_scan(mine, scan_sh, &total_cta);
+        }
+        if (threadIdx.x == 0) kept_sh = total_cta;
+        cluster.sync();  // kept counts visible cluster-wide
+        for (int r = 0; r < kCluster; ++r) {
+            const int c = *cluster.map_shared_rank(&kept_sh, r);
+            if (r < rank) before += c;
+            total += c;
+        }
+    }
+    // Done reading the peers' shared memory; the matching wait ends the
+    // kernel, so its latency overlaps the writes below.
+    cluster.barrier_arrive();
+
+    if (pos) {
+        int off[3] = {ext[0], ext[2], ext[4]};
+        if (!a.normalize) off[0] = off[1] = off[2] = 0;
+        int* dst = a.tile_pos + tt.prefix * 6 * a.B + (long long)b * 3 * tt.n * 2;
+        if (cached) {
+#pragma unroll
+            for (int k = 0; k < kPosCache; ++k) {
+                const int j = j0 + static_cast<int>(threadIdx.x) + k * nthr;
+                if (j < j1) {
+#pragma unroll
+                    for (int d = 0; d < 3; ++d)
+                        *reinterpret_cast<int2*>(dst + ((long long)d * tt.n + j) * 2) =
+                            make_int2(v[k][d].x - off[d], v[k][d].y - off[d]);
+                }
+            }
+        } else {
+            tw.init(tt, j0 + static_cast<int>(threadIdx.x), nthr);
+            for (int j = j0 + threadIdx.x; j < j1; j += nthr, tw.next(tt)) {
+                const long long n = tw.token(p, tt);
+#pragma unroll
+                for (int d = 0; d < 3; ++d) {
+                    const int2 x = *reinterpret_cast<const int2*>(gen_b + ((long long)d * N + n) * 2);
+                    *reinterpret_cast<int2*>(dst + ((long long)d * tt.n + j) * 2) =
+                        make_int2(x.x - off[d], x.y - off[d]);
+                }
+            }
+        }
+    }
+
+    // Conditioning pass 2: compacted indices and shifted positions, in the
+    // original order; the slots after the last kept token get -1 / zeros.
+    if (a.M > 0 && (a.kept_idx || a.tile_cond)) {
+        auto put = [&](int m, int at, int2 (&c)[3]) {
+            if (a.kept_idx) a.kept_idx[row * a.M + at] = m;
+            if (a.tile_cond) {
+#pragma unroll
+                for (int d = 0; d < 3; ++d) {
+                    int2 q = c[d];
+                    if (a.normalize) { q.x -= ext[2 * d]; q.y -= ext[2 * d]; }
+                    *reinterpret_cast<int2*>(a.tile_cond + ((row * 3 + d) * a.M + at) * 2) = q;
+                }
+            }
+        };
+        if (one_pass) {
+            if (kc) put(mm, before + at_in, cv);
+        } else {
+            int base = before;
+            for (int m00 = m0; m00 < m1; m00 += nthr) {
+                const int m = m00 + threadIdx.x;
+                const bool k = (m < m1) && cond_keep(a.cond, b, a.M, m, ext);
+                int round_total;
+                const int at = base + block_excl_scan(k ? 1 : 0, scan_sh, &round_total);
+                if (k) {
+                    int2 c[3];
+#pragma unroll
+                    for (int d = 0; d < 3; ++d)
+                        c[d] = *reinterpret_cast<const int2*>(a.cond + (((long long)b * 3 + d) * a.M + m) * 2);
+                    put(m, at, c);
+                }
+                base += round_total;
+            }
+        }
         const int fill = a.M - total;
         const int fchunk = (fill + kCluster - 1) / kCluster;
         const int q0 = total + min(fill, rank * fchunk), q1 = total + min(fill, (rank + 1) * fchunk);
-        for (int q = q0 + threadIdx.x; q < q1; q += blockDim.x) {
+        for (int q = q0 + threadIdx.x; q < q1; q += nthr) {
             if (a.kept_idx) a.kept_idx[row * a.M + q] = -1;
             if (a.tile_cond) {
 #pragma unroll
@@ -1487,16 +1630,26 @@ __global__ void __launch_bounds__(kThreads) cond_kernel(const __grid_constant__ 
             }
         }
     }
-    if (rank == 0 && threadIdx.x == 0 && a.num_kept) a.num_kept[row] = total;
-    cluster.barrier_wait();  // peers finished reading kept_sh
+    if (rank == 0 && threadIdx.x == 0 && a.num_kept) a.num_kept[row] = total;   // 0 when M = 0
+    cluster.barrier_wait();  // no CTA leaves while a peer may read its shared memory
 }
 
 __global__ void __launch_bounds__(kThreads) cond_count_kernel(const unsigned char* keep, int T, int BM,
                                                               int* count, float* weight) {
+    pdl_launch_dependents();
+    pdl_wait();   // the keep flags of the previous kernel
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= BM) return;
-    int c = 0;
-    for (int t = 0; t < T; ++t) c += keep[(long long)t * BM + i];
+    int c0 = 0, c1 = 0, c2 = 0, c3 = 0;   // independent loads in flight
+    int t = 0;
+    for (; t + 4 <= T; t += 4) {
+        c0 += keep[(long long)t * BM + i];
+        c1 += keep[(long long)(t + 1) * BM + i];
+        c2 += keep[(long long)(t + 2) * BM + i];
+        c3 += keep[(long long)(t + 3) * BM + i];
+    }
+    for (; t < T; ++t) c0 += keep[(long long)t * BM + i];
+    const int c = (c0 + c1) + (c2 + c3);
     count[i] = c;
     weight[i] = c ? 1.0f / static_cast<float>(c) : 0.0f;
 }
@@ -1633,21 +1786,35 @@ tdp_status set_smem(K kernel, int bytes) {
     return cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
 }
 
+// Launch with programmatic stream serialization (the kernel may start while
+// its predecessor in the stream finishes; see pdl_wait) and, with
+// cluster > 1, clusters of that many CTAs.
 template <typename K, typename... Args>
-tdp_status launch_cluster(K kernel, long long blocks, cudaStream_t stream, Args... args) {
+tdp_status launch(K kernel, long long blocks, int threads, int smem, cudaStream_t stream, int cluster, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    unsigned n = 1;
+    if (cluster > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n = 2;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n;
     return cuda_status(cudaLaunchKernelEx(&cfg, kernel, args...));
+}
+
+template <typename K, typename... Args>
+tdp_status launch_cluster(K kernel, long long blocks, cudaStream_t stream, Args... args) {
+    return launch(kernel, blocks, kThreads, 0, stream, kCluster, args...);
 }
 
 // Most column tiles that cover any of U adjacent output columns (the fast
@@ -1726,26 +1893,25 @@ tdp_status launch_blend(const tdp_plan_t& p, int BC, const void* tiles, long lon
             for (int u = 0; u < ncu; ++u) a.order[count[cls[u]]++] = static_cast<uint16_t>(u);
         }
     }
-    auto launch = [&](auto kernel, bool persistent) -> tdp_status {
+    auto go = [&](auto kernel, bool persistent) -> tdp_status {
         tdp_status st = set_smem(kernel, L.total);
         if (st != TDP_OK) return st;
         unsigned grid = static_cast<unsigned>(items);
         const int threads = persistent ? kBlendThreads : kThreads;
         if (persistent && (st = persistent_grid(kernel, L.total, items, &grid, threads)) != TDP_OK) return st;
-        kernel<<<grid, threads, L.total, stream>>>(p, a);
-        return cuda_status(cudaGetLastError());
+        return launch(kernel, grid, threads, L.total, stream, 1, p, a);
     };
     // Pair stores need every output row to start on a 4-byte (bf16) or
     // 8-byte (fp32) boundary: W even.
-    if (!L.fast) return launch(blend_generic_kernel<Tin, Tout>, false);
+    if (!L.fast) return go(blend_generic_kernel<Tin, Tout>, false);
     const int kt = max_terms(p, pairs ? 2 : 1);
     if (pairs) {
-        if (kt == 1) return launch(blend_fast_kernel<Tin, Tout, 2, 1>, true);
-        if (kt == 2) return launch(blend_fast_kernel<Tin, Tout, 2, 2>, true);
-        return launch(blend_fast_kernel<Tin, Tout, 2, 3>, true);
+        if (kt == 1) return go(blend_fast_kernel<Tin, Tout, 2, 1>, true);
+        if (kt == 2) return go(blend_fast_kernel<Tin, Tout, 2, 2>, true);
+        return go(blend_fast_kernel<Tin, Tout, 2, 3>, true);
     }
-    if (kt == 1) return launch(blend_fast_kernel<Tin, Tout, 1, 1>, true);
-    return launch(blend_fast_kernel<Tin, Tout, 1, 2>, true);
+    if (kt == 1) return go(blend_fast_kernel<Tin, Tout, 1, 1>, true);
+    return go(blend_fast_kernel<Tin, Tout, 1, 2>, true);
 }
 
 }  // namespace
@@ -1774,15 +1940,14 @@ tdp_status tdp_extract(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype d
     if (items > INT_MAX || (long long)B * C > INT_MAX) return TDP_ERR_INVALID_ARG;
     ExtractArgs a{latent, tiles, (long long)B * C * p.dims[0] * p.dims[1] * p.dims[2], B * C, band_rows, nbands,
                   static_cast<int>(items), L.off_slots, L.off_data, L.stage_bytes};
-    auto launch = [&](auto kernel) -> tdp_status {
+    auto go = [&](auto kernel) -> tdp_status {
         tdp_status st = set_smem(kernel, L.total);
         if (st != TDP_OK) return st;
         unsigned grid = 0;
         if ((st = persistent_grid(kernel, L.total, items, &grid)) != TDP_OK) return st;
-        kernel<<<grid, kThreads, L.total, stream>>>(p, a);
-        return cuda_status(cudaGetLastError());
+        return launch(kernel, grid, kThreads, L.total, stream, 1, p, a);
     };
-    return esz == 2 ? launch(extract_kernel<uint16_t>) : launch(extract_kernel<uint32_t>);
+    return esz == 2 ? go(extract_kernel<uint16_t>) : go(extract_kernel<uint32_t>);
 }
 
 tdp_status tdp_blend(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_dtype, const void* tiles,
@@ -1813,45 +1978,58 @@ tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum
                                  p.dims[2] + p.dims[0] + p.dims[1]);
     const int tables = tab <= 32 * 1024 ? 1 : 0;
     const int smem = tables ? static_cast<int>(tab) : 0;
+    if (!sum_out && tables) {
+        // the maximum alone: one CTA over the runs of equal weight tuples
+        const long long reps = tab + 4LL * ((long long)p.dims[0] + p.dims[1] + p.dims[2]);
+        if (reps <= 40 * 1024) {
+            tdp_status st = set_smem(window_max_kernel, static_cast<int>(reps));
+            if (st != TDP_OK) return st;
+            return launch(window_max_kernel, 1, kThreads, static_cast<int>(reps), stream, 1, p, max_abs_dev);
+        }
+    }
     tdp_status st = cuda_status(cudaMemsetAsync(max_abs_dev, 0, sizeof(float), stream));
     if (st != TDP_OK) return st;
     const long long blocks = std::min<long long>((N + 4LL * kThreads - 1) / (4LL * kThreads), 2LL * std::max(1, sm_count()));
-    window_sum_kernel<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p, max_abs_dev, sum_out, tables);
-    return cuda_status(cudaGetLastError());
+    return launch(window_sum_kernel, blocks, kThreads, smem, stream, 1, p, max_abs_dev, sum_out, tables);
+}
+
+tdp_status tdp_tokens(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos, int32_t normalize,
+                      int32_t* tile_pos, int32_t* offsets, int32_t M, const int32_t* cond_pos,
+                      int32_t* tile_extent, uint8_t* keep, int32_t* count, float* weight, int32_t* kept_idx,
+                      int32_t* num_kept, int32_t* tile_cond_pos, cudaStream_t stream) {
+    if (!tdp::plan_is_valid(plan) || B < 0 || M < 0) return TDP_ERR_INVALID_ARG;
+    if (B == 0) return TDP_OK;
+    if (!gen_pos || (tile_pos && !offsets)) return TDP_ERR_INVALID_ARG;
+    if (M > 0 && (!cond_pos || !tile_extent || !keep || !count || !weight)) return TDP_ERR_INVALID_ARG;
+    const void* ptrs[] = {gen_pos, tile_pos, offsets, cond_pos, tile_extent, keep,
+                          count, weight, kept_idx, num_kept, tile_cond_pos};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return TDP_ERR_ALIGNMENT;
+    const long long blocks = (long long)kCluster * plan->total_tiles * B;
+    if (blocks > INT_MAX || (long long)B * M > INT_MAX) return TDP_ERR_INVALID_ARG;
+    TokensArgs a{gen_pos, B, normalize ? 1 : 0, tile_pos, offsets, M, cond_pos, tile_extent, keep, kept_idx,
+                 num_kept, tile_cond_pos};
+    tdp_status st = launch_cluster(tokens_kernel, blocks, stream, *plan, a);
+    if (st != TDP_OK || M == 0) return st;
+    const int BM = B * M;
+    return launch(cond_count_kernel, (BM + kThreads - 1) / kThreads, kThreads, 0, stream, 1,
+                  static_cast<const unsigned char*>(keep), plan->total_tiles, BM, count, weight);
 }
 
 tdp_status tdp_positions(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos, int32_t normalize,
                          int32_t* tile_pos, int32_t* offsets, cudaStream_t stream) {
-    if (!tdp::plan_is_valid(plan) || B < 0) return TDP_ERR_INVALID_ARG;
-    if (B == 0) return TDP_OK;
-    if (!gen_pos || !tile_pos || !offsets) return TDP_ERR_INVALID_ARG;
-    if (!aligned16(gen_pos) || !aligned16(tile_pos) || !aligned16(offsets)) return TDP_ERR_ALIGNMENT;
-    const long long blocks = (long long)kCluster * plan->total_tiles * B;
-    if (blocks > INT_MAX) return TDP_ERR_INVALID_ARG;
-    PositionsArgs a{gen_pos, tile_pos, offsets, B, normalize ? 1 : 0};
-    return launch_cluster(positions_kernel, blocks, stream, *plan, a);
+    if (!tile_pos || !offsets) return TDP_ERR_INVALID_ARG;
+    return tdp_tokens(plan, B, gen_pos, normalize, tile_pos, offsets, 0, nullptr, nullptr, nullptr, nullptr,
+                      nullptr, nullptr, nullptr, nullptr, stream);
 }
 
 tdp_status tdp_cond_select(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos, int32_t M,
                            const int32_t* cond_pos, int32_t normalize, int32_t* tile_extent, uint8_t* keep,
                            int32_t* count, float* weight, int32_t* kept_idx, int32_t* num_kept,
                            int32_t* tile_cond_pos, cudaStream_t stream) {
-    if (!tdp::plan_is_valid(plan) || B < 0 || M < 0) return TDP_ERR_INVALID_ARG;
-    if (B == 0) return TDP_OK;
-    if (!gen_pos || !tile_extent) return TDP_ERR_INVALID_ARG;
-    if (M > 0 && (!cond_pos || !keep || !count || !weight)) return TDP_ERR_INVALID_ARG;
-    const void* ptrs[] = {gen_pos, tile_extent, cond_pos, keep, count, weight, kept_idx, num_kept, tile_cond_pos};
-    for (const void* q : ptrs)
-        if (q && !aligned16(q)) return TDP_ERR_ALIGNMENT;
-    const long long blocks = (long long)kCluster * plan->total_tiles * B;
-    if (blocks > INT_MAX || (long long)B * M > INT_MAX) return TDP_ERR_INVALID_ARG;
-    CondArgs a{gen_pos, cond_pos, tile_extent, keep, kept_idx, num_kept, tile_cond_pos, B, M, normalize ? 1 : 0};
-    tdp_status st = launch_cluster(cond_kernel, blocks, stream, *plan, a);
-    if (st != TDP_OK || M == 0) return st;
-    const int BM = B * M;
-    cond_count_kernel<<<(BM + kThreads - 1) / kThreads, kThreads, 0, stream>>>(keep, plan->total_tiles, BM, count,
-                                                                              weight);
-    return cuda_status(cudaGetLastError());
+    if (!tile_extent) return TDP_ERR_INVALID_ARG;
+    return tdp_tokens(plan, B, gen_pos, normalize, nullptr, nullptr, M, cond_pos, tile_extent, keep, count, weight,
+                      kept_idx, num_kept, tile_cond_pos, stream);
 }
 
 tdp_status tdp_device_error(uint32_t* code, int32_t clear) {

@@ -108,6 +108,10 @@ _lib.tdp_cond_select.argtypes = [_P(Plan), C.c_int32, C.c_void_p, C.c_int32, C.c
                                  C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                  C.c_void_p, C.c_void_p]
 _lib.tdp_cond_select.restype = C.c_int
+_lib.tdp_tokens.argtypes = [_P(Plan), C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32,
+                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                            C.c_void_p, C.c_void_p]
+_lib.tdp_tokens.restype = C.c_int
 _lib.tdp_device_error.argtypes = [_P(C.c_uint32), C.c_int32]
 _lib.tdp_device_error.restype = C.c_int
 _lib.tdp_status_str.argtypes = [C.c_int]
@@ -121,7 +125,7 @@ if _lib.tdp_plan_struct_size() != C.sizeof(Plan):
     raise ImportError("tdp_plan_t layout mismatch between libtdp.so and the binding")
 
 EXPORTS = ("tdp_plan", "tdp_tile_offset", "tdp_tiles_numel", "tdp_tile_box", "tdp_plan_stats",
-           "tdp_extract", "tdp_positions", "tdp_cond_select", "tdp_blend", "tdp_window_sum",
+           "tdp_extract", "tdp_positions", "tdp_cond_select", "tdp_tokens", "tdp_blend", "tdp_window_sum",
            "tdp_device_error", "tdp_status_str", "tdp_last_cuda_error", "tdp_plan_struct_size")
 
 
@@ -285,6 +289,43 @@ def cond_select(p: Plan, gen_pos: torch.Tensor, cond_pos: torch.Tensor, normaliz
                                 _dev(o["count"], "count", torch.int32), _dev(o["weight"], "weight", torch.float32),
                                 opt("kept_idx", torch.int32), opt("num_kept", torch.int32),
                                 opt("tile_cond_pos", torch.int32), _stream(stream)), "tdp_cond_select")
+    return o
+
+
+def tokens(p: Plan, gen_pos: torch.Tensor, cond_pos: torch.Tensor, normalize: bool = True,
+           with_lists: bool = True, out: Optional[dict] = None,
+           stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """tdp_tokens: positions and conditioning selection in one launch.  Returns
+    the cond_select dict plus "tile_pos" (packed) and "offsets" [T, B, 3]."""
+    B = int(gen_pos.shape[0])
+    M = int(cond_pos.shape[2])
+    N = p.dims[0] * p.dims[1] * p.dims[2]
+    if tuple(gen_pos.shape) != (B, 3, N, 2) or tuple(cond_pos.shape) != (B, 3, M, 2):
+        raise ValueError("gen_pos must be [B, 3, F*H*W, 2] and cond_pos [B, 3, M, 2]")
+    dev = gen_pos.device
+    T = p.T
+    o = out if out is not None else {}
+    if not o:
+        o["tile_pos"] = torch.empty(6 * B * p.tokens_numel(), dtype=torch.int32, device=dev)
+        o["offsets"] = torch.empty((T, B, 3), dtype=torch.int32, device=dev)
+        o["extent"] = torch.empty((T, B, 3, 2), dtype=torch.int32, device=dev)
+        o["keep"] = torch.empty((T, B, M), dtype=torch.uint8, device=dev)
+        o["count"] = torch.empty((B, M), dtype=torch.int32, device=dev)
+        o["weight"] = torch.empty((B, M), dtype=torch.float32, device=dev)
+        if with_lists:
+            o["kept_idx"] = torch.empty((T, B, M), dtype=torch.int32, device=dev)
+            o["num_kept"] = torch.empty((T, B), dtype=torch.int32, device=dev)
+            o["tile_cond_pos"] = torch.empty((T, B, 3, M, 2), dtype=torch.int32, device=dev)
+
+    def opt(name, dtype):
+        return _dev(o[name], name, dtype) if name in o else None
+
+    _check(_lib.tdp_tokens(C.byref(p), B, _dev(gen_pos, "gen_pos", torch.int32), 1 if normalize else 0,
+                           opt("tile_pos", torch.int32), opt("offsets", torch.int32), M,
+                           _dev(cond_pos, "cond_pos", torch.int32) if M > 0 else None,
+                           opt("extent", torch.int32), opt("keep", torch.uint8), opt("count", torch.int32),
+                           opt("weight", torch.float32), opt("kept_idx", torch.int32), opt("num_kept", torch.int32),
+                           opt("tile_cond_pos", torch.int32), _stream(stream)), "tdp_tokens")
     return o
 
 

@@ -252,3 +252,66 @@ def test_cond_select_random_gen_positions(T):
     gen = inputs.random_positions(2, int(np.prod(dims)), seed=4, lo=-100, hi=400)
     cond = inputs.random_positions(2, 300, seed=5, lo=-150, hi=450)
     check_cond(T, dims, tiling, gen, cond)
+
+
+# ----------------------------------------------------------------- positions + conditioning in one launch
+@pytest.mark.parametrize("case", ["4k", "ragged", "random", "no_cond", "big_chunks"])
+def test_tokens_matches_separate_calls_and_oracle(T, case):
+    if case in ("4k", "no_cond"):
+        wl = WORKLOADS["4k"]
+        dims, tiling, B = wl.dims, wl.tiling, 2
+        gen = inputs.grid_positions(B, *dims)
+        M = 0 if case == "no_cond" else wl.num_cond
+        cond = inputs.cond_positions(B, M, *dims, n_negative=M // 4, seed=2)
+    elif case == "ragged":
+        dims, tiling, B = (5, 37, 53), ((2, 1), (3, 5), (4, 6)), 3
+        gen = inputs.grid_positions(B, *dims)
+        cond = inputs.cond_positions(B, 37, *dims, n_negative=7, seed=3)
+    elif case == "random":
+        dims, tiling, B = (3, 10, 12), ((1, 0), (2, 3), (3, 3)), 2
+        gen = inputs.random_positions(B, int(np.prod(dims)), seed=4, lo=-100, hi=400)
+        cond = inputs.random_positions(B, 300, seed=5, lo=-150, hi=450)
+    else:   # tiles whose chunks exceed the per-thread register cache (read twice)
+        dims, tiling, B = (8, 160, 160), ((1, 0), (2, 8), (2, 8)), 1
+        gen = inputs.grid_positions(B, *dims)
+        cond = inputs.cond_positions(B, 64, *dims, n_negative=8, seed=6)
+    p = T.plan(dims, tiling)
+    rp = O.make_plan(dims, tiling)
+    o = T.tokens(p, _dev(gen, torch.int32), _dev(cond, torch.int32))
+    tp, off = T.positions(p, _dev(gen, torch.int32))
+    torch.cuda.synchronize()
+    ref_tp, ref_off = O.positions(rp, gen)
+    assert np.array_equal(o["offsets"].cpu().numpy(), ref_off)
+    assert np.array_equal(o["tile_pos"].cpu().numpy(), np.concatenate([x.reshape(-1) for x in ref_tp]))
+    assert torch.equal(o["tile_pos"], tp) and torch.equal(o["offsets"], off)
+    M = cond.shape[2]
+    if M:
+        ref = O.cond_select(rp, gen, cond)
+        assert np.array_equal(o["extent"].cpu().numpy(), ref.extent)
+        assert np.array_equal(o["keep"].cpu().numpy(), ref.keep.astype(np.uint8))
+        assert np.array_equal(o["count"].cpu().numpy(), ref.count)
+        assert np.array_equal(o["weight"].cpu().numpy().view(np.uint32), ref.weight.view(np.uint32))
+        sep = T.cond_select(p, _dev(gen, torch.int32), _dev(cond, torch.int32))
+        for k in ("extent", "keep", "count", "weight", "kept_idx", "num_kept", "tile_cond_pos"):
+            assert torch.equal(o[k], sep[k]), k
+    assert T.device_error() == 0
+
+
+# ----------------------------------------------------------------- window maximum without the per-element sums
+@pytest.mark.parametrize("case", list(WORKLOADS) + ["mold3", "mold4", "triple", "ragged"])
+def test_window_max_alone_equals_full_sum(T, case):
+    if case in WORKLOADS:
+        wl = WORKLOADS[case]
+        dims, tiling, compat = wl.dims, wl.tiling, False
+    else:
+        dims, tiling, compat = {"mold3": ((1, 1, 21), ((1, 0), (1, 0), (3, 8)), True),
+                                "mold4": ((1, 1, 21), ((1, 0), (1, 0), (4, 8)), True),
+                                "triple": ((6, 21, 21), ((3, 2), (4, 8), (3, 8)), True),
+                                "ragged": ((5, 37, 53), ((2, 1), (3, 5), (4, 6)), False)}[case]
+    p = T.plan(dims, tiling, compat=compat)
+    dev_full, S = T.window_sum(p, want_sum=True)
+    full = dev_full.item()
+    dev_alone, none = T.window_sum(p)             # no per-element output: the one-CTA path
+    assert none is None
+    assert dev_alone.item() == full               # bit-identical maximum
+    assert abs(full - float(np.max(np.abs(_np64(S) - 1.0)))) == 0.0
