@@ -49,6 +49,7 @@ constexpr int kExtractSmemBudget = 64 * 1024;   // staged bands + slot table
 constexpr int kBlendSmemBudget = 64 * 1024;     // ring of staged tile rows + tables (3 CTAs per SM)
 constexpr int kBlendQueue = 4;                  // blend items staged ahead at most (the header holds 4 ring offsets)
 constexpr int kMaxOrdered = 256;                // column units ordered on the host
+constexpr int kBlendTabBudget = 6 * 1024;       // shared bytes for the per-CTA axis entries
 constexpr int kBlendConsumers = 256;            // blend threads that compute (8 warps)
 constexpr int kBlendThreads = kBlendConsumers + 32;   // + one producer warp
 
@@ -505,6 +506,7 @@ struct BlendArgs {
     int off_a, off_b, off_c, off_d, off_e, off_stage, off_slotbase, off_data;
     int max_slots, data_bytes;
     int kf, kh, kw;
+    int off_tab;   // fast kernel: axis entries (F + H + W of them), or -1: computed on demand
     // fast kernel: column units (U output columns each) in the order the
     // consumer threads take them -- fewest column tiles first -- when there
     // are at most kMaxOrdered units; otherwise the identity order
@@ -658,6 +660,70 @@ __device__ __forceinline__ void load_terms(const tdp_plan_t& p, int c, int W, Te
 }
 
 
+// Covering tiles of one index of an axis (at most two in the fast blend):
+// the first one, their count, and their weights r(x).
+struct AxisEnt {
+    uint8_t lo, n, pad0, pad1;
+    float w[2];
+};
+
+__device__ __forceinline__ AxisEnt axis_ent(const tdp_plan_t& p, int d, int x) {
+    int lo, hi;
+    tdp::axis_cover(p, d, x, lo, hi);
+    AxisEnt e;
+    e.lo = static_cast<uint8_t>(lo);
+    e.n = static_cast<uint8_t>(hi - lo + 1);
+    e.pad0 = e.pad1 = 0;
+    e.w[0] = axis_weight(p, d, lo, x);
+    e.w[1] = hi > lo ? axis_weight(p, d, lo + 1, x) : 0.0f;
+    return e;
+}
+
+// The three axes' entries, tabulated once per CTA in shared memory (frames,
+// then rows, then columns) when they fit; otherwise computed on demand.
+struct AxisTabs {
+    const AxisEnt* tab;   // nullptr: compute
+    int hbase, wbase;
+    __device__ __forceinline__ AxisEnt get(const tdp_plan_t& p, int d, int x) const {
+        if (tab) return tab[(d == 0 ? 0 : (d == 1 ? hbase : wbase)) + x];
+        return axis_ent(p, d, x);
+    }
+};
+
+// load_terms from the column entries (same values: the entries hold the
+// same axis_weight results).
+template <int U, int KT>
+__device__ __forceinline__ void load_terms_tab(const tdp_plan_t& p, const AxisTabs& at, int c, int W, Terms<U, KT>& t) {
+    AxisEnt e[U];
+#pragma unroll
+    for (int v = 0; v < U; ++v) e[v] = at.get(p, 2, c + v < W ? c + v : c);
+    int lo = e[0].lo, hi = e[0].lo + e[0].n - 1;
+#pragma unroll
+    for (int v = 1; v < U; ++v) {
+        if (c + v < W) {
+            lo = min(lo, static_cast<int>(e[v].lo));
+            hi = max(hi, e[v].lo + e[v].n - 1);
+        }
+    }
+    t.n = hi - lo + 1;
+#pragma unroll
+    for (int q = 0; q < KT; ++q) {
+        const bool real = lo + q <= hi;
+        const int i = min(lo + q, hi);
+        const int w0 = p.start[2][i], w1 = p.end[2][i];
+        t.iw[q] = i;
+        t.sw[q] = w1 - w0;
+        t.xo[q] = c - w0;
+#pragma unroll
+        for (int v = 0; v < U; ++v) {
+            const bool in = real && c + v < W && c + v >= w0 && c + v < w1;
+            t.in[q][v] = in;
+            t.sel[q][v] = in ? 0x1044u : 0x4444u;
+            t.w[q][v] = in ? e[v].w[i - e[v].lo] : 0.0f;
+        }
+    }
+}
+
 template <int U>
 __device__ __forceinline__ void store_cols(float* out, long long i, const float (&v)[U]) {
     if constexpr (U == 2) *reinterpret_cast<float2*>(out + i) = make_float2(v[0], v[1]);
@@ -701,7 +767,8 @@ __device__ __forceinline__ void blend_run(const Run& R, int r, int r1, uint32_t 
             ea[kk][q] = sdata + lds_s32(sbase + R.slot0b[kk] + iwb[q]) + (hb0 + r) * swb[q] + colb[q];
     uint32_t wa = wrow + 4 * KC * r;
     Tout* dst = dcol + (long long)r * W;
-    for (; r < r1; ++r) {
+    // One output row, `s` rows past the current pointers.
+    auto row = [&](int s) {
         float acc[U];
 #pragma unroll
         for (int v = 0; v < U; ++v) acc[v] = 0.0f;
@@ -714,27 +781,36 @@ __device__ __forceinline__ void blend_run(const Run& R, int r, int r1, uint32_t 
             for (int q = 0; q < KTW; ++q)
 #pragma unroll
                 for (int v = 0; v < U; ++v) {
-                    const float x =
-                        lds_masked(ea[kk][q] + v * esz, tm.sel[q][v], tm.in[q][v], static_cast<const Tin*>(nullptr));
+                    const float x = lds_masked(ea[kk][q] + s * swb[q] + v * esz, tm.sel[q][v], tm.in[q][v],
+                                               static_cast<const Tin*>(nullptr));
                     inner[v] = fmaf(tm.w[q][v], x, inner[v]);
                 }
             if constexpr (ONES) {
 #pragma unroll
                 for (int v = 0; v < U; ++v) acc[v] = inner[v];
             } else {
-                const float wfh = lds_f32(wa + 4 * kk);
+                const float wfh = lds_f32(wa + 4 * (s * KC + kk));
 #pragma unroll
                 for (int v = 0; v < U; ++v) acc[v] = fmaf(wfh, inner[v], acc[v]);
             }
         }
-        store_cols<U>(dst, 0, acc);
+        store_cols<U>(dst, (long long)s * W, acc);
+    };
+    // Two rows per pass, written out (the loop itself stays rolled: an
+    // unrolled form of the one-row loop gave wrong shared addresses on its
+    // second iteration in some builds, found by the row-band parity test).
+#pragma unroll 1
+    for (; r + 1 < r1; r += 2) {
+        row(0);
+        row(1);
 #pragma unroll
         for (int kk = 0; kk < NC; ++kk)
 #pragma unroll
-            for (int q = 0; q < KTW; ++q) ea[kk][q] += swb[q];
-        wa += 4 * KC;
-        dst += W;
+            for (int q = 0; q < KTW; ++q) ea[kk][q] += 2 * swb[q];
+        wa += 8 * KC;
+        dst += 2LL * W;
     }
+    if (r < r1) row(0);
 }
 
 // A run of rows whose value is one tile's elements unchanged (one pair
@@ -756,6 +832,7 @@ __device__ __forceinline__ void copy_run(const Run& R, int r, int r1, uint32_t s
                                          int swb, int iwb, int hb0, T* dcol, int W) {
     uint32_t ea = sdata + lds_s32(sbase + R.slot0b[0] + iwb) + (hb0 + r) * swb + colb;
     T* dst = dcol + (long long)r * W;
+#pragma unroll 1
     for (; r < r1; ++r) {
         copy_row<U>(ea, dst);
         ea += swb;
@@ -895,11 +972,21 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
     const int cu0 = static_cast<int>(threadIdx.x) - rg * per_row;
     const int ncu_mine = (rg < RG && cu0 < ncu) ? (ncu - cu0 + per_row - 1) / per_row : 0;
     auto unit_of = [&](int i) -> int { return a.ordered ? static_cast<int>(a.order[i]) : i; };
+    AxisTabs at;
+    at.tab = a.off_tab >= 0 ? reinterpret_cast<const AxisEnt*>(smem + a.off_tab) : nullptr;
+    at.hbase = F;
+    at.wbase = F + H;
+    if (at.tab) {
+        AxisEnt* tab = reinterpret_cast<AxisEnt*>(smem + a.off_tab);
+        for (int i = threadIdx.x; i < F + H + W; i += kBlendConsumers)
+            tab[i] = i < F ? axis_ent(p, 0, i) : (i < F + H ? axis_ent(p, 1, i - F) : axis_ent(p, 2, i - F - H));
+        if (!consumer_sync()) return (void)atomicOr(&g_device_error, kErrBlendWait);
+    }
     Terms<U, KT> tm;
     tm.n = 0;
     bool lane_copy = false;
     if (ncu_mine == 1) {
-        load_terms<U, KT>(p, unit_of(cu0) * U, W, tm);
+        load_terms_tab<U, KT>(p, at, unit_of(cu0) * U, W, tm);
         lane_copy = tm.n == 1 && sizeof(Tin) == sizeof(Tout);
 #pragma unroll
         for (int v = 0; v < U; ++v) lane_copy = lane_copy && tm.in[0][v] && tm.w[0][v] == 1.0f;
@@ -925,14 +1012,13 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
             if (!consumer_sync()) return (void)atomicOr(&g_device_error, kErrBlendWait);
             // w_fh = r_f * r_h per band row and pair (frame tile major), one
             // row per thread
-            for (int r = threadIdx.x; r < c.rows; r += kBlendConsumers) {
-                const int h = c.hb0 + r;
-                int lo, hi;
-                tdp::axis_cover(p, 1, h, lo, hi);
-                int m = 0;
-                for (int fa = 0; fa < c.NF; ++fa) {
-                    const float wf = axis_weight(p, 0, c.if_lo + fa, c.f);
-                    for (int ih = lo; ih <= hi; ++ih) wts[r * KC + m++] = __fmul_rn(wf, axis_weight(p, 1, ih, h));
+            {
+                const AxisEnt ef = at.get(p, 0, c.f);   // ef.lo == c.if_lo, ef.n == c.NF
+                for (int r = threadIdx.x; r < c.rows; r += kBlendConsumers) {
+                    const AxisEnt eh = at.get(p, 1, c.hb0 + r);
+                    int m = 0;
+                    for (int fa = 0; fa < c.NF; ++fa)
+                        for (int j = 0; j < eh.n; ++j) wts[r * KC + m++] = __fmul_rn(ef.w[fa], eh.w[j]);
                 }
             }
             // runs: the rows between consecutive starts and ends of the row
@@ -1010,7 +1096,7 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
         Tout* const out_band = out + ((long long)cur.bc * F + c.f) * H * W + (long long)c.hb0 * W;
         for (int m = 0; m < ncu_mine; ++m) {
             const int cu = unit_of(cu0 + m * per_row);
-            if (ncu_mine > 1) load_terms<U, KT>(p, cu * U, W, tm);
+            if (ncu_mine > 1) load_terms_tab<U, KT>(p, at, cu * U, W, tm);
             // per term: byte offsets of the columns in the tile row, of one
             // tile row, and of the term's entry in the run-base table
             int colb[KT], swb[KT], iwb[KT];
@@ -1373,6 +1459,7 @@ struct TokensArgs {
 };
 
 constexpr int kPosCache = 4;   // tokens per thread kept in registers between reduce and write
+constexpr int kCondOneCta = 2048;   // at most this many conditioning tokens: one CTA per tile tests them all
 
 __device__ __forceinline__ bool cond_keep(const int* cond, int b, int M, int m, const int ext[6]) {
     const int2 t = *reinterpret_cast<const int2*>(cond + (((long long)b * 3 + 0) * M + m) * 2);
@@ -1454,9 +1541,13 @@ __global__ void __launch_bounds__(kThreads) tokens_kernel(const __grid_constant_
     const bool cached = pos && chunk <= kPosCache * nthr;
     if (threadIdx.x < 6) ext_sh[threadIdx.x] = (threadIdx.x & 1) ? INT_MIN : INT_MAX;
 
-    // this CTA's conditioning tokens, loaded early when they fit one pass
-    const int mchunk = (a.M + kCluster - 1) / kCluster;
-    const int m0 = min(a.M, rank * mchunk), m1 = min(a.M, m0 + mchunk);
+    // Conditioning tokens: with at most kCondOneCta of them, cluster rank 0
+    // tests all of them (no exchange of kept counts between the CTAs);
+    // otherwise each CTA takes a chunk.  A CTA's tokens are loaded before
+    // the extent reduction when they fit one pass of its threads.
+    const bool solo = a.M <= kCondOneCta;
+    const int mchunk = solo ? a.M : (a.M + kCluster - 1) / kCluster;
+    const int m0 = solo ? 0 : min(a.M, rank * mchunk), m1 = solo ? (rank == 0 ? a.M : 0) : min(a.M, m0 + mchunk);
     const bool one_pass = m1 - m0 <= nthr;
     const int mm = m0 + static_cast<int>(threadIdx.x);
     const bool have_c = one_pass && mm < m1;
@@ -1544,12 +1635,16 @@ __global__ void __launch_bounds__(kThreads) tokens_kernel(const __grid_constant_
             }
             block_excl_scan(mine, scan_sh, &total_cta);
         }
-        if (threadIdx.x == 0) kept_sh = total_cta;
-        cluster.sync();  // kept counts visible cluster-wide
-        for (int r = 0; r < kCluster; ++r) {
-            const int c = *cluster.map_shared_rank(&kept_sh, r);
-            if (r < rank) before += c;
-            total += c;
+        if (solo) {
+            total = total_cta;   // rank 0 holds every token; the other ranks hold none
+        } else {
+            if (threadIdx.x == 0) kept_sh = total_cta;
+            cluster.sync();  // kept counts visible cluster-wide
+            for (int r = 0; r < kCluster; ++r) {
+                const int c = *cluster.map_shared_rank(&kept_sh, r);
+                if (r < rank) before += c;
+                total += c;
+            }
         }
     }
     // Done reading the peers' shared memory; the matching wait ends the
@@ -1620,7 +1715,8 @@ __global__ void __launch_bounds__(kThreads) tokens_kernel(const __grid_constant_
         }
         const int fill = a.M - total;
         const int fchunk = (fill + kCluster - 1) / kCluster;
-        const int q0 = total + min(fill, rank * fchunk), q1 = total + min(fill, (rank + 1) * fchunk);
+        int q0 = total + min(fill, rank * fchunk), q1 = total + min(fill, (rank + 1) * fchunk);
+        if (solo) { q0 = total; q1 = rank == 0 ? a.M : total; }
         for (int q = q0 + threadIdx.x; q < q1; q += nthr) {
             if (a.kept_idx) a.kept_idx[row * a.M + q] = -1;
             if (a.tile_cond) {
@@ -1630,7 +1726,7 @@ __global__ void __launch_bounds__(kThreads) tokens_kernel(const __grid_constant_
             }
         }
     }
-    if (rank == 0 && threadIdx.x == 0 && a.num_kept) a.num_kept[row] = total;   // 0 when M = 0
+    if (rank == 0 && threadIdx.x == 0 && a.num_kept) a.num_kept[row] = total;   // 0 when M = 0 (rank 0 knows it)
     cluster.barrier_wait();  // no CTA leaves while a peer may read its shared memory
 }
 
@@ -1640,16 +1736,16 @@ __global__ void __launch_bounds__(kThreads) cond_count_kernel(const unsigned cha
     pdl_wait();   // the keep flags of the previous kernel
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= BM) return;
-    int c0 = 0, c1 = 0, c2 = 0, c3 = 0;   // independent loads in flight
+    int c = 0;
     int t = 0;
-    for (; t + 4 <= T; t += 4) {
-        c0 += keep[(long long)t * BM + i];
-        c1 += keep[(long long)(t + 1) * BM + i];
-        c2 += keep[(long long)(t + 2) * BM + i];
-        c3 += keep[(long long)(t + 3) * BM + i];
+    for (; t + 16 <= T; t += 16) {   // 16 independent loads in flight
+        int k[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) k[u] = keep[(long long)(t + u) * BM + i];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) c += k[u];
     }
-    for (; t < T; ++t) c0 += keep[(long long)t * BM + i];
-    const int c = (c0 + c1) + (c2 + c3);
+    for (; t < T; ++t) c += keep[(long long)t * BM + i];
     count[i] = c;
     weight[i] = c ? 1.0f / static_cast<float>(c) : 0.0f;
 }
@@ -1701,7 +1797,7 @@ ExtractLayout extract_layout(const tdp_plan_t& p, int band_rows, int esz) {
 // cover tables, then the slot tables and the staged tile rows -- two
 // stages for the (persistent) fast kernel, one for the generic kernel.
 struct BlendLayout {
-    int off_a, off_b, off_c, off_d, off_e, off_slotbase, off_stage, off_data;
+    int off_a, off_b, off_c, off_d, off_e, off_slotbase, off_stage, off_data, off_tab;
     int max_slots, data_bytes, total;
     bool fast;
 };
@@ -1747,6 +1843,9 @@ BlendLayout blend_layout(const tdp_plan_t& p, int band_rows, int esz) {
         L.off_d = o; o = round_up(o + W * 4, 16);                                     // wcnt
         L.off_e = o; o = round_up(o + W * kw * (int)sizeof(Cov), 16);                 // wcov
     }
+    L.off_tab = -1;
+    const long long tab_bytes = (long long)sizeof(AxisEnt) * ((long long)p.dims[0] + p.dims[1] + W);
+    if (L.fast && tab_bytes <= kBlendTabBudget) { L.off_tab = o; o = round_up(o + static_cast<int>(tab_bytes), 16); }
     L.off_stage = o; o = round_up(o + L.max_slots * (int)sizeof(StageSlot), 16);
     L.off_slotbase = o; o = round_up(o + (L.fast ? kBlendQueue : 1) * L.max_slots * 4, 16);
     L.off_data = o;
@@ -1864,6 +1963,7 @@ tdp_status launch_blend(const tdp_plan_t& p, int BC, const void* tiles, long lon
     a.off_slotbase = L.off_slotbase;
     a.off_stage = L.off_stage;
     a.off_data = L.off_data;
+    a.off_tab = L.off_tab;
     a.max_slots = L.max_slots;
     a.data_bytes = L.data_bytes;
     a.kf = p.max_cover[0];

@@ -238,7 +238,7 @@ def test_cond_select_workloads(T, name):
     assert np.all(ref.count[neg] == WORKLOADS[name].tiling[0][0] * wl.tiling[1][0] * wl.tiling[2][0])
 
 
-@pytest.mark.parametrize("M", [0, 1, 37, 1000])
+@pytest.mark.parametrize("M", [0, 1, 37, 1000, 3000])   # 3000: chunks over the cluster's CTAs
 @pytest.mark.parametrize("normalize", [True, False])
 def test_cond_select_sizes(T, M, normalize):
     dims, tiling = (5, 37, 53), ((2, 1), (3, 5), (4, 6))
