@@ -348,17 +348,49 @@ __device__ __forceinline__ void extract_copy_slot_warp(E* __restrict__ dst, cons
         const int e0 = head + 2 * lane;
         const int r0 = small_div(e0, e.inv_sw);
         int x = e0 - r0 * sw;
-        int a = r0 * W + x;                          // source index of the pair's first element
         const int dq = small_div(64, e.inv_sw), dr = 64 - dq * sw;
-        const int step = dq * W + dr;
-        uint32_t* d32 = reinterpret_cast<uint32_t*>(dst + head);
-#pragma unroll 4
-        for (int j = lane; j < npairs; j += 32) {
-            const int a2 = a + 1 + ((x + 1 < sw) ? 0 : wrap);   // second element may open the next row
-            d32[j] = static_cast<uint32_t>(src[a]) | (static_cast<uint32_t>(src[a2]) << 16);
-            x += dr;
-            a += step;
-            if (x >= sw) { x -= sw; a += wrap; }
+        // shared byte address of the pair's first element, and its steps
+        uint32_t sa = smem_u32(src) + 2u * static_cast<uint32_t>(r0 * W + x);
+        const uint32_t sstep = 2u * static_cast<uint32_t>(dq * W + dr), swrap = 2u * static_cast<uint32_t>(wrap);
+        uint32_t* dp = reinterpret_cast<uint32_t*>(dst + head) + lane;
+        const int nit = npairs > lane ? (npairs - lane + 31) >> 5 : 0;
+        // one pass step on (x, sa), and one pair's word (its second element
+        // may open the next row)
+        auto advance = [&](int& xx, uint32_t& aa) {
+            xx += dr;
+            aa += sstep;
+            if (xx >= sw) { xx -= sw; aa += swrap; }
+        };
+        auto pair = [&](int xx, uint32_t aa) {
+            return lds_u16(aa) | (lds_u16(aa + (xx + 1 < sw ? 2u : 2u + swrap)) << 16);
+        };
+        int it = 0;
+        // four passes per trip, positions stepped explicitly so that the
+        // eight loads are in flight together (the loop itself stays rolled)
+#pragma unroll 1
+        for (; it + 3 < nit; it += 4) {
+            int x1 = x, x2, x3;
+            uint32_t a1 = sa, a2, a3;
+            advance(x1, a1);
+            x2 = x1; a2 = a1;
+            advance(x2, a2);
+            x3 = x2; a3 = a2;
+            advance(x3, a3);
+            const uint32_t w0 = pair(x, sa), w1 = pair(x1, a1), w2 = pair(x2, a2), w3 = pair(x3, a3);
+            dp[0] = w0;
+            dp[32] = w1;
+            dp[64] = w2;
+            dp[96] = w3;
+            dp += 128;
+            x = x3;
+            sa = a3;
+            advance(x, sa);
+        }
+#pragma unroll 1
+        for (; it < nit; ++it) {
+            *dp = pair(x, sa);
+            dp += 32;
+            advance(x, sa);
         }
     } else {
         const int r0 = small_div(lane, e.inv_sw);
