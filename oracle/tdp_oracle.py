@@ -298,6 +298,39 @@ def cond_select(plan: Plan, gen_pos: np.ndarray, cond_pos: np.ndarray, normalize
     return CondSelection(extent, keep, count, weight, kept, tcp)
 
 
+def cond_combine(sel: CondSelection, tile_cond_out: np.ndarray) -> np.ndarray:
+    """Blend of the conditioning tokens' per-tile outputs (TDP §Shared negative
+    (reference) positions: a token kept by k tiles has blend weight 1/k).
+    tile_cond_out[t, b, j] is tile t's output for its j-th kept token of batch
+    b (kept order = original order); rows past a tile's kept count are ignored.
+    Returns out[b, m] = sum over the tiles t keeping m of (1/k) *
+    tile_cond_out[t, b, j_t(m)], in float64 (a token kept by no tile gives 0)."""
+    T, B, M = sel.keep.shape
+    D = tile_cond_out.shape[-1]
+    out = np.zeros((B, M, D), dtype=np.float64)
+    for b in range(B):
+        for m in range(M):
+            k = int(sel.count[b, m])
+            if k == 0:
+                continue
+            for t in range(T):
+                hits = np.nonzero(sel.kept[t][b] == m)[0]
+                if len(hits):
+                    out[b, m] += tile_cond_out[t, b, int(hits[0])].astype(np.float64) / k
+    return out
+
+
+def cond_slots(sel: CondSelection) -> np.ndarray:
+    """slot[t, b, m] = the position of token m in tile t's kept list, or -1."""
+    T, B, M = sel.keep.shape
+    slot = np.full((T, B, M), -1, dtype=np.int64)
+    for t in range(T):
+        for b in range(B):
+            for j, m in enumerate(sel.kept[t][b]):
+                slot[t, b, m] = j
+    return slot
+
+
 # ---------------------------------------------------------------------------
 # Plan statistics (DistVAE "Choosing a tile window": decoded area, seams,
 # per-tile activations, heaviest-rank imbalance; TDP §What it is: tiles go to

@@ -363,3 +363,65 @@ def test_distvae_strip_figures():
     assert st.seams == int(g["seams"][0])
     grid = O.make_plan((1, 128, 128), ((1, 0), (int(g["grid_rows"][0]), 8), (int(g["grid_cols"][0]), 8)))
     assert O.layout_stats(grid.intervals, grid.dims, 4).seams == int(g["grid_seams"][0])
+
+
+# --------------------------------------------------------------------------
+# Conditioning-token combine (TDP §Shared negative (reference) positions: a
+# token kept by k tiles has blend weight 1/k).
+def _cond_case(seed=0, D=5):
+    dims, cfg = (5, 37, 53), ((2, 1), (3, 5), (4, 6))
+    plan = O.make_plan(dims, cfg)
+    gen = inputs.grid_positions(2, *dims)
+    cond = inputs.cond_positions(2, 60, *dims, n_negative=9, seed=seed)
+    sel = O.cond_select(plan, gen, cond)
+    rng = np.random.default_rng(seed)
+    T, B, M = sel.keep.shape
+    tile_out = rng.standard_normal((T, B, M, D))
+    return sel, tile_out
+
+
+def test_cond_combine_matches_cumsum_slots():
+    # independent slot derivation: slot = (number of kept tokens up to m) - 1
+    sel, x = _cond_case(3)
+    T, B, M = sel.keep.shape
+    slot = np.cumsum(sel.keep, axis=2) - 1
+    ref = np.zeros((B, M, x.shape[-1]))
+    for t in range(T):
+        k = sel.keep[t]                                   # [B, M]
+        gathered = np.take_along_axis(x[t], np.where(k, slot[t], 0)[..., None], axis=1)
+        ref += np.where(k[..., None], gathered / np.maximum(sel.count, 1)[..., None], 0.0)
+    assert np.array_equal(O.cond_slots(sel), np.where(sel.keep, slot, -1))
+    assert np.allclose(O.cond_combine(sel, x), ref, rtol=0, atol=1e-12)
+
+
+def test_cond_combine_single_keeper_is_a_copy_and_unkept_is_zero():
+    sel, x = _cond_case(4)
+    out = O.cond_combine(sel, x)
+    slot = O.cond_slots(sel)
+    one = sel.count == 1
+    none = sel.count == 0
+    assert one.any() and none.any()
+    for b, m in zip(*np.nonzero(one)):
+        t = int(np.nonzero(sel.keep[:, b, m])[0][0])
+        assert np.array_equal(out[b, m], x[t, b, slot[t, b, m]])   # weight exactly 1
+    assert np.all(out[none] == 0.0)
+
+
+def test_cond_combine_partition_of_unity_and_reference_tokens():
+    sel, _ = _cond_case(5)
+    T, B, M = sel.keep.shape
+    rng = np.random.default_rng(9)
+    v = rng.standard_normal((B, M, 3))
+    slot = O.cond_slots(sel)
+    x = np.zeros((T, B, M, 3))
+    for t in range(T):
+        for b in range(B):
+            for m in range(M):
+                if slot[t, b, m] >= 0:
+                    x[t, b, slot[t, b, m]] = v[b, m]       # every keeper returns the same value
+    out = O.cond_combine(sel, x)
+    kept = sel.count > 0
+    assert np.allclose(out[kept], v[kept], rtol=1e-12, atol=1e-12)
+    # reference (negative time) tokens are kept by every tile, weight 1/T each
+    cond_neg = sel.keep.all(axis=0)
+    assert cond_neg.any() and np.all(sel.count[cond_neg] == T)
