@@ -334,6 +334,20 @@ def run_tdp(args, rank: int, world: int):
     per_kernel_ms = seg.mean(axis=0)
     names = ["extract", "tokens_and_window_sum", "blend"]
 
+    # The next row after the step (not part of it): the conditioning-token
+    # combine, on the step's selection, with D = C features per token.
+    comb_in = torch.randn((p.T, wl.B, wl.num_cond, wl.C), device=dev).to(dt)
+    comb_out = torch.empty((wl.B, wl.num_cond, wl.C), dtype=dt, device=dev)
+    for _ in range(3):
+        tdp.cond_combine(p, comb_in, tok_out["slot_of"], tok_out["weight"], out=comb_out)
+    cev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(20)]
+    for e in cev:
+        e[0].record(stream)
+        tdp.cond_combine(p, comb_in, tok_out["slot_of"], tok_out["weight"], out=comb_out)
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    comb_ms = float(np.median([e[0].elapsed_time(e[1]) for e in cev]))
+
     # e2e: host buffers in, blended latent out, through the same C-ABI calls
     X_h = X.cpu().pin_memory()
     gen_h = gen.cpu().pin_memory()
@@ -389,6 +403,8 @@ def run_tdp(args, rank: int, world: int):
         "e2e": {"value": job_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
         "gpu_launches": KERNELS_PER_STEP * K,
+        "next_rows": {"cond_combine": {"ms": comb_ms, "workload": f"T={p.T} tiles, B={wl.B}, M={wl.num_cond} "
+                                       f"conditioning tokens, D={wl.C} bf16 features; median of 20, not in the step"}},
         "clocks": clocks,
         "timed_wall_s": wall,
     }

@@ -215,14 +215,41 @@ tdp_status tdp_cond_select(const tdp_plan_t* plan, int32_t B, const int32_t* gen
  * (offsets may then be NULL too); M == 0 skips the conditioning tokens
  * (cond_pos, keep, count and weight may then be NULL); tile_extent, when
  * not NULL, receives [TS, TE) per tile, batch and axis (required when
- * M > 0).  Every result equals what the separate calls write.
+ * M > 0).  slot_of, when not NULL, receives int32 [T, B, M]: the token's
+ * position in tile t's kept list, or -1 (the index tdp_cond_combine
+ * gathers by).  Every result equals what the separate calls write.
  * Bit-exact.  Asynchronous on `stream`.
  */
 tdp_status tdp_tokens(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos,
                       int32_t normalize, int32_t* tile_pos, int32_t* offsets, int32_t M,
                       const int32_t* cond_pos, int32_t* tile_extent, uint8_t* keep,
                       int32_t* count, float* weight, int32_t* kept_idx, int32_t* num_kept,
-                      int32_t* tile_cond_pos, cudaStream_t stream);
+                      int32_t* tile_cond_pos, int32_t* slot_of, cudaStream_t stream);
+
+/*
+ * tdp_cond_combine -- the blend of the conditioning tokens' per-tile
+ * outputs (the step after tdp_cond_select).
+ *
+ * Source: "Tiled Data Parallelism (TDP)", Shared negative (reference)
+ * positions: a token kept by several tiles is not counted twice; its blend
+ * weight is 1 / (number of tiles that kept it).
+ *   out[b,m,:] = sum over tiles t with slot_of[t,b,m] >= 0, in increasing t,
+ *                of weight[b,m] * tile_cond_out[t,b,slot_of[t,b,m],:]
+ * accumulated in fp32 (fmaf) and stored once in `out_dtype` (round to
+ * nearest even for bf16); a token kept by no tile gets zeros.
+ * tile_cond_out: device [T, B, M, D] in `in_dtype`: tile t's outputs for
+ *                its kept tokens in kept order (rows past the tile's kept
+ *                count are not read).
+ * slot_of:       device int32 [T, B, M] from tdp_tokens: the token's
+ *                position in tile t's kept list, or -1.
+ * weight:        device float [B, M] from tdp_cond_select / tdp_tokens.
+ * out:           device [B, M, D] in `out_dtype`.
+ * B, M or D == 0: nothing to do.  Asynchronous on `stream`.
+ */
+tdp_status tdp_cond_combine(const tdp_plan_t* plan, int32_t B, int32_t M, int32_t D,
+                            tdp_dtype in_dtype, const void* tile_cond_out, const int32_t* slot_of,
+                            const float* weight, tdp_dtype out_dtype, void* out,
+                            cudaStream_t stream);
 
 /*
  * tdp_blend -- step 5, fused separable trapezoid window + overlap-add (K2).

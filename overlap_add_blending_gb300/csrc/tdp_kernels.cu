@@ -225,6 +225,13 @@ __device__ __forceinline__ SpanCopy plan_span(const E* base, long long first, in
     return c;
 }
 
+// ------------------------------------------------------------------ element conversions
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
 // ------------------------------------------------------------------ shared loads by address
 // 32-bit shared-window byte addresses keep the hot loops' address math to
 // one add per access.
@@ -1488,9 +1495,11 @@ struct TokensArgs {
     int* kept_idx;
     int* num_kept;
     int* tile_cond;
+    int* slot_of;      // [T, B, M]: position in the tile's kept list, or -1 (NULL: not written)
 };
 
 constexpr int kPosCache = 4;   // tokens per thread kept in registers between reduce and write
+constexpr int kCombineCols = 4;   // feature columns per lane per pass of the conditioning combine
 constexpr int kCondOneCta = 2048;   // at most this many conditioning tokens: one CTA per tile tests them all
 
 __device__ __forceinline__ bool cond_keep(const int* cond, int b, int M, int m, const int ext[6]) {
@@ -1714,7 +1723,7 @@ __global__ void __launch_bounds__(kThreads) tokens_kernel(const __grid_constant_
 
     // Conditioning pass 2: compacted indices and shifted positions, in the
     // original order; the slots after the last kept token get -1 / zeros.
-    if (a.M > 0 && (a.kept_idx || a.tile_cond)) {
+    if (a.M > 0 && (a.kept_idx || a.tile_cond || a.slot_of)) {
         auto put = [&](int m, int at, int2 (&c)[3]) {
             if (a.kept_idx) a.kept_idx[row * a.M + at] = m;
             if (a.tile_cond) {
@@ -1728,6 +1737,7 @@ __global__ void __launch_bounds__(kThreads) tokens_kernel(const __grid_constant_
         };
         if (one_pass) {
             if (kc) put(mm, before + at_in, cv);
+            if (have_c && a.slot_of) a.slot_of[row * a.M + mm] = kc ? before + at_in : -1;
         } else {
             int base = before;
             for (int m00 = m0; m00 < m1; m00 += nthr) {
@@ -1735,6 +1745,7 @@ __global__ void __launch_bounds__(kThreads) tokens_kernel(const __grid_constant_
                 const bool k = (m < m1) && cond_keep(a.cond, b, a.M, m, ext);
                 int round_total;
                 const int at = base + block_excl_scan(k ? 1 : 0, scan_sh, &round_total);
+                if (m < m1 && a.slot_of) a.slot_of[row * a.M + m] = k ? at : -1;
                 if (k) {
                     int2 c[3];
 #pragma unroll
@@ -1780,6 +1791,63 @@ __global__ void __launch_bounds__(kThreads) cond_count_kernel(const unsigned cha
     for (; t < T; ++t) c += keep[(long long)t * BM + i];
     count[i] = c;
     weight[i] = c ? 1.0f / static_cast<float>(c) : 0.0f;
+}
+
+// =================================================================== K6: conditioning combine
+// out[b, m, :] = sum over tiles t keeping token m (slot_of[t, b, m] >= 0),
+// in increasing t, of weight[b, m] * tile_out[t, b, slot, :]: the 1/k blend
+// of a conditioning token's per-tile outputs, fp32 accumulation, one store.
+// One warp per (b, m); its lanes look up the tiles' slots 32 at a time and
+// then walk the feature dimension.
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kThreads) cond_combine_kernel(int T, int BM, int M, int D, const Tin* tile_out,
+                                                                const int* slot_of, const float* weight, Tout* out) {
+    pdl_launch_dependents();
+    pdl_wait();   // slots, weights and tile outputs may come from the previous kernel
+    const int lane = threadIdx.x & 31;
+    const int bm = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (bm >= BM) return;
+    const float w = weight[bm];
+    for (int d0 = 0; d0 < D; d0 += 32 * kCombineCols) {
+        float acc[kCombineCols];
+#pragma unroll
+        for (int i = 0; i < kCombineCols; ++i) acc[i] = 0.0f;
+        for (int t0 = 0; t0 < T; t0 += 32) {
+            const int t = t0 + lane;
+            const int slot = t < T ? slot_of[(long long)t * BM + bm] : -1;
+            unsigned kept = __ballot_sync(0xffffffffu, slot >= 0);
+            while (kept) {
+                // up to four kept tiles per round, lowest first: their loads
+                // are issued together, then added in increasing tile order
+                float v[4][kCombineCols];
+                bool has[4];   // warp-uniform: `kept` is a ballot
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    has[j] = kept != 0;
+                    const int src = has[j] ? __ffs(kept) - 1 : 0;
+                    kept &= kept - 1;
+                    const int st = __shfl_sync(0xffffffffu, slot, src);
+                    const long long row = ((long long)(t0 + src) * BM + (bm - bm % M) + st) * D;   // (t, b, st)
+#pragma unroll
+                    for (int i = 0; i < kCombineCols; ++i) {
+                        const int d = d0 + i * 32 + lane;
+                        v[j][i] = (has[j] && d < D) ? to_f32(tile_out[row + d]) : 0.0f;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (has[j]) {
+#pragma unroll
+                        for (int i = 0; i < kCombineCols; ++i) acc[i] = fmaf(w, v[j][i], acc[i]);
+                    }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kCombineCols; ++i) {
+            const int d = d0 + i * 32 + lane;
+            if (d < D) out[(long long)bm * D + d] = from_f32<Tout>(acc[i]);
+        }
+    }
 }
 
 // =================================================================== host helpers
@@ -2128,19 +2196,19 @@ tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum
 tdp_status tdp_tokens(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos, int32_t normalize,
                       int32_t* tile_pos, int32_t* offsets, int32_t M, const int32_t* cond_pos,
                       int32_t* tile_extent, uint8_t* keep, int32_t* count, float* weight, int32_t* kept_idx,
-                      int32_t* num_kept, int32_t* tile_cond_pos, cudaStream_t stream) {
+                      int32_t* num_kept, int32_t* tile_cond_pos, int32_t* slot_of, cudaStream_t stream) {
     if (!tdp::plan_is_valid(plan) || B < 0 || M < 0) return TDP_ERR_INVALID_ARG;
     if (B == 0) return TDP_OK;
     if (!gen_pos || (tile_pos && !offsets)) return TDP_ERR_INVALID_ARG;
     if (M > 0 && (!cond_pos || !tile_extent || !keep || !count || !weight)) return TDP_ERR_INVALID_ARG;
     const void* ptrs[] = {gen_pos, tile_pos, offsets, cond_pos, tile_extent, keep,
-                          count, weight, kept_idx, num_kept, tile_cond_pos};
+                          count, weight, kept_idx, num_kept, tile_cond_pos, slot_of};
     for (const void* q : ptrs)
         if (q && !aligned16(q)) return TDP_ERR_ALIGNMENT;
     const long long blocks = (long long)kCluster * plan->total_tiles * B;
     if (blocks > INT_MAX || (long long)B * M > INT_MAX) return TDP_ERR_INVALID_ARG;
     TokensArgs a{gen_pos, B, normalize ? 1 : 0, tile_pos, offsets, M, cond_pos, tile_extent, keep, kept_idx,
-                 num_kept, tile_cond_pos};
+                 num_kept, tile_cond_pos, slot_of};
     tdp_status st = launch_cluster(tokens_kernel, blocks, stream, *plan, a);
     if (st != TDP_OK || M == 0) return st;
     const int BM = B * M;
@@ -2152,7 +2220,7 @@ tdp_status tdp_positions(const tdp_plan_t* plan, int32_t B, const int32_t* gen_p
                          int32_t* tile_pos, int32_t* offsets, cudaStream_t stream) {
     if (!tile_pos || !offsets) return TDP_ERR_INVALID_ARG;
     return tdp_tokens(plan, B, gen_pos, normalize, tile_pos, offsets, 0, nullptr, nullptr, nullptr, nullptr,
-                      nullptr, nullptr, nullptr, nullptr, stream);
+                      nullptr, nullptr, nullptr, nullptr, nullptr, stream);
 }
 
 tdp_status tdp_cond_select(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos, int32_t M,
@@ -2161,7 +2229,35 @@ tdp_status tdp_cond_select(const tdp_plan_t* plan, int32_t B, const int32_t* gen
                            int32_t* tile_cond_pos, cudaStream_t stream) {
     if (!tile_extent) return TDP_ERR_INVALID_ARG;
     return tdp_tokens(plan, B, gen_pos, normalize, nullptr, nullptr, M, cond_pos, tile_extent, keep, count, weight,
-                      kept_idx, num_kept, tile_cond_pos, stream);
+                      kept_idx, num_kept, tile_cond_pos, nullptr, stream);
+}
+
+tdp_status tdp_cond_combine(const tdp_plan_t* plan, int32_t B, int32_t M, int32_t D, tdp_dtype in_dtype,
+                            const void* tile_cond_out, const int32_t* slot_of, const float* weight,
+                            tdp_dtype out_dtype, void* out, cudaStream_t stream) {
+    if (!tdp::plan_is_valid(plan) || B < 0 || M < 0 || D < 0) return TDP_ERR_INVALID_ARG;
+    if (!dtype_size(in_dtype) || !dtype_size(out_dtype)) return TDP_ERR_INVALID_ARG;
+    if (B == 0 || M == 0 || D == 0) return TDP_OK;
+    if (!tile_cond_out || !slot_of || !weight || !out) return TDP_ERR_INVALID_ARG;
+    const void* ptrs[] = {tile_cond_out, slot_of, weight, out};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return TDP_ERR_ALIGNMENT;
+    const long long BM = (long long)B * M;
+    if (BM > INT_MAX || (long long)plan->total_tiles * BM * D > (1LL << 62)) return TDP_ERR_INVALID_ARG;
+    const int warps = kThreads / 32;
+    const long long blocks = (BM + warps - 1) / warps;
+    const int T = plan->total_tiles;
+    auto go = [&](auto kernel, const auto* in, auto* o) {
+        return launch(kernel, blocks, kThreads, 0, stream, 1, T, static_cast<int>(BM), M, D, in, slot_of, weight, o);
+    };
+    const bool ib = in_dtype == TDP_BF16, ob = out_dtype == TDP_BF16;
+    if (ib && ob) return go(cond_combine_kernel<__nv_bfloat16, __nv_bfloat16>,
+                            static_cast<const __nv_bfloat16*>(tile_cond_out), static_cast<__nv_bfloat16*>(out));
+    if (ib) return go(cond_combine_kernel<__nv_bfloat16, float>, static_cast<const __nv_bfloat16*>(tile_cond_out),
+                      static_cast<float*>(out));
+    if (ob) return go(cond_combine_kernel<float, __nv_bfloat16>, static_cast<const float*>(tile_cond_out),
+                      static_cast<__nv_bfloat16*>(out));
+    return go(cond_combine_kernel<float, float>, static_cast<const float*>(tile_cond_out), static_cast<float*>(out));
 }
 
 tdp_status tdp_device_error(uint32_t* code, int32_t clear) {

@@ -110,8 +110,11 @@ _lib.tdp_cond_select.argtypes = [_P(Plan), C.c_int32, C.c_void_p, C.c_int32, C.c
 _lib.tdp_cond_select.restype = C.c_int
 _lib.tdp_tokens.argtypes = [_P(Plan), C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32,
                             C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
-                            C.c_void_p, C.c_void_p]
+                            C.c_void_p, C.c_void_p, C.c_void_p]
 _lib.tdp_tokens.restype = C.c_int
+_lib.tdp_cond_combine.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_void_p,
+                                  C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]
+_lib.tdp_cond_combine.restype = C.c_int
 _lib.tdp_device_error.argtypes = [_P(C.c_uint32), C.c_int32]
 _lib.tdp_device_error.restype = C.c_int
 _lib.tdp_status_str.argtypes = [C.c_int]
@@ -125,7 +128,8 @@ if _lib.tdp_plan_struct_size() != C.sizeof(Plan):
     raise ImportError("tdp_plan_t layout mismatch between libtdp.so and the binding")
 
 EXPORTS = ("tdp_plan", "tdp_tile_offset", "tdp_tiles_numel", "tdp_tile_box", "tdp_plan_stats",
-           "tdp_extract", "tdp_positions", "tdp_cond_select", "tdp_tokens", "tdp_blend", "tdp_window_sum",
+           "tdp_extract", "tdp_positions", "tdp_cond_select", "tdp_tokens", "tdp_cond_combine", "tdp_blend",
+           "tdp_window_sum",
            "tdp_device_error", "tdp_status_str", "tdp_last_cuda_error", "tdp_plan_struct_size")
 
 
@@ -316,6 +320,7 @@ def tokens(p: Plan, gen_pos: torch.Tensor, cond_pos: torch.Tensor, normalize: bo
             o["kept_idx"] = torch.empty((T, B, M), dtype=torch.int32, device=dev)
             o["num_kept"] = torch.empty((T, B), dtype=torch.int32, device=dev)
             o["tile_cond_pos"] = torch.empty((T, B, 3, M, 2), dtype=torch.int32, device=dev)
+            o["slot_of"] = torch.empty((T, B, M), dtype=torch.int32, device=dev)
 
     def opt(name, dtype):
         return _dev(o[name], name, dtype) if name in o else None
@@ -325,8 +330,27 @@ def tokens(p: Plan, gen_pos: torch.Tensor, cond_pos: torch.Tensor, normalize: bo
                            _dev(cond_pos, "cond_pos", torch.int32) if M > 0 else None,
                            opt("extent", torch.int32), opt("keep", torch.uint8), opt("count", torch.int32),
                            opt("weight", torch.float32), opt("kept_idx", torch.int32), opt("num_kept", torch.int32),
-                           opt("tile_cond_pos", torch.int32), _stream(stream)), "tdp_tokens")
+                           opt("tile_cond_pos", torch.int32), opt("slot_of", torch.int32), _stream(stream)),
+           "tdp_tokens")
     return o
+
+
+def cond_combine(p: Plan, tile_cond_out: torch.Tensor, slot_of: torch.Tensor, weight: torch.Tensor,
+                 out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """tdp_cond_combine: tile_cond_out [T, B, M, D] (bf16/fp32, kept order),
+    slot_of int32 [T, B, M], weight float [B, M] -> out [B, M, D]."""
+    T, B, M, D = (int(v) for v in tile_cond_out.shape)
+    if T != p.T or tuple(slot_of.shape) != (T, B, M) or tuple(weight.shape) != (B, M):
+        raise ValueError("tile_cond_out [T,B,M,D], slot_of [T,B,M] and weight [B,M] must agree with the plan")
+    odt = out_dtype or tile_cond_out.dtype
+    if out is None:
+        out = torch.empty((B, M, D), dtype=odt, device=tile_cond_out.device)
+    _check(_lib.tdp_cond_combine(C.byref(p), B, M, D, _DT[tile_cond_out.dtype],
+                                 _dev(tile_cond_out, "tile_cond_out", tile_cond_out.dtype),
+                                 _dev(slot_of, "slot_of", torch.int32), _dev(weight, "weight", torch.float32),
+                                 _DT[out.dtype], _dev(out, "out", out.dtype), _stream(stream)), "tdp_cond_combine")
+    return out
 
 
 def device_error(clear: bool = True) -> int:

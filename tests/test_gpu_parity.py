@@ -315,3 +315,44 @@ def test_window_max_alone_equals_full_sum(T, case):
     assert none is None
     assert dev_alone.item() == full               # bit-identical maximum
     assert abs(full - float(np.max(np.abs(_np64(S) - 1.0)))) == 0.0
+
+
+# ----------------------------------------------------------------- conditioning combine
+@pytest.mark.parametrize("case", ["4k", "ragged_f32", "ragged_bf16_to_f32", "many_tiles", "d_odd", "no_cond"])
+def test_cond_combine(T, case):
+    if case == "4k":
+        wl = WORKLOADS["4k"]
+        dims, tiling, B, M, D, dt, odt = wl.dims, wl.tiling, 1, wl.num_cond, 128, torch.bfloat16, torch.bfloat16
+    elif case.startswith("ragged"):
+        dims, tiling, B, M, D = (5, 37, 53), ((2, 1), (3, 5), (4, 6)), 2, 60, 33
+        dt = torch.float32 if case == "ragged_f32" else torch.bfloat16
+        odt = torch.float32
+    elif case == "many_tiles":     # 64 tiles: two 32-lane slot passes per token
+        dims, tiling, B, M, D, dt, odt = (12, 40, 40), ((4, 1), (4, 2), (4, 2)), 1, 90, 64, torch.float32, torch.bfloat16
+    elif case == "d_odd":
+        dims, tiling, B, M, D, dt, odt = (3, 10, 12), ((1, 0), (2, 3), (3, 3)), 2, 300, 7, torch.bfloat16, torch.bfloat16
+    else:
+        dims, tiling, B, M, D, dt, odt = (5, 37, 53), ((2, 1), (3, 5), (4, 6)), 1, 0, 16, torch.float32, torch.float32
+    p = T.plan(dims, tiling)
+    rp = O.make_plan(dims, tiling)
+    gen = inputs.grid_positions(B, *dims)
+    cond = inputs.cond_positions(B, M, *dims, n_negative=M // 5, seed=11)
+    o = T.tokens(p, _dev(gen, torch.int32), _dev(cond, torch.int32))
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((p.T, B, M, D)).astype(np.float32)
+    xd = _dev(x, dt)
+    Y = T.cond_combine(p, xd, o["slot_of"], o["weight"], out_dtype=odt)
+    torch.cuda.synchronize()
+    assert Y.shape == (B, M, D) and Y.dtype == odt
+    if M == 0:
+        return
+    sel = O.cond_select(rp, gen, cond)
+    assert np.array_equal(o["slot_of"].cpu().numpy(), O.cond_slots(sel))
+    ref = O.cond_combine(sel, _np64(xd))          # the same (rounded) inputs, float64 sums, weight 1/k
+    Yn = _np64(Y)
+    if odt == torch.float32:
+        assert np.max(np.abs(Yn - ref)) <= 1e-5
+    else:
+        assert np.all(np.abs(Yn - ref) <= 8e-3 * np.abs(ref) + 1e-5)
+    assert np.all(Yn[sel.count == 0] == 0.0)
+    assert T.device_error() == 0
