@@ -87,15 +87,16 @@ def read_peak() -> tuple:
     return FALLBACK_HBM_GBS, "fallback"
 
 
+# The sources the profiled kernels (extract, blend, tokens) are built from.
+PROFILED_SOURCES = ("tdp_kernels.cu", "tdp_geometry.h")
+
+
 def source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "overlap_add_blending_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cpp", ".h")):
-            with open(os.path.join(csrc, name), "rb") as fh:
-                h.update(name.encode() + b"\0" + fh.read())
-    with open(os.path.join(ROOT, "include", "tdp.h"), "rb") as fh:
-        h.update(fh.read())
+    for name in PROFILED_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
