@@ -186,6 +186,52 @@ def unpack(plan: Plan, B: int, C: int, flat: np.ndarray) -> List[np.ndarray]:
 
 
 # ---------------------------------------------------------------------------
+# Token-major tiles (TDP docs §What it is and §When to use it: every tile is
+# run through the transformer on its own, as a sequence of its N_t tokens;
+# §Position normalization: a tile's generated tokens are its sub-grid of the
+# latent's token grid, in the same row-major order).  Reading: token n of a
+# tile with shape (f_t, h_t, w_t) is local (k, y, x) with
+# n = (k*h_t + y)*w_t + x, and each token carries all C channels.
+# ---------------------------------------------------------------------------
+def extract_tokens(plan: Plan, latent: np.ndarray) -> List[np.ndarray]:
+    """tokens[t][b, n, c] = X[b, c, f0+k, h0+y, w0+x], n = (k*h_t + y)*w_t + x."""
+    assert latent.ndim == 5 and tuple(latent.shape[2:]) == plan.dims
+    B, C = latent.shape[:2]
+    out = []
+    for t in range(plan.num_tiles):
+        (f0, f1), (h0, h1), (w0, w1) = plan.box(t)
+        sub = latent[:, :, f0:f1, h0:h1, w0:w1]            # [B, C, f_t, h_t, w_t]
+        out.append(np.ascontiguousarray(sub.reshape(B, C, -1).transpose(0, 2, 1)))
+    return out
+
+
+def unpack_tokens(plan: Plan, B: int, C: int, flat: np.ndarray) -> List[np.ndarray]:
+    """Packed token-major buffer -> per-tile [B, N_t, C] views (tile after
+    tile, the same tile offsets as the channel-first packing)."""
+    out, pos = [], 0
+    for t in range(plan.num_tiles):
+        n_t = int(np.prod(plan.shape(t)))
+        out.append(flat[pos:pos + B * n_t * C].reshape(B, n_t, C))
+        pos += B * n_t * C
+    assert pos == flat.size
+    return out
+
+
+def blend_tokens(plan: Plan, tiles_tok: Sequence[np.ndarray]) -> np.ndarray:
+    """Overlap-add of token-major tile outputs: the token (k, y, x) of tile t
+    lands on latent point (f0+k, h0+y, w0+x) of every channel, weighted by
+    the tile's separable trapezoid there.  float64 accumulation."""
+    B, _, C = tiles_tok[0].shape
+    acc = np.zeros((B, C) + plan.dims, dtype=np.float64)
+    for t in range(plan.num_tiles):
+        (f0, f1), (h0, h1), (w0, w1) = plan.box(t)
+        ft, ht, wt = plan.shape(t)
+        grid = tiles_tok[t].astype(np.float64).transpose(0, 2, 1).reshape(B, C, ft, ht, wt)
+        acc[:, :, f0:f1, h0:h1, w0:w1] += tile_window(plan, t)[None, None] * grid
+    return acc
+
+
+# ---------------------------------------------------------------------------
 # Step 5: window and overlap-add (TDP docs §What it is; mold §A bug found
 # while porting: blend has no normalisation pass).
 # ---------------------------------------------------------------------------

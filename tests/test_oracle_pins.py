@@ -425,3 +425,103 @@ def test_cond_combine_partition_of_unity_and_reference_tokens():
     # reference (negative time) tokens are kept by every tile, weight 1/T each
     cond_neg = sel.keep.all(axis=0)
     assert cond_neg.any() and np.all(sel.count[cond_neg] == T)
+
+
+# ---------------------------------------------------------------- token-major tiles
+def test_extract_tokens_bruteforce_order():
+    """Each token of each tile, found by walking the tile's box in (f, h, w)
+    order with a running counter, holds that point's C channels."""
+    rng = np.random.default_rng(7)
+    X = rng.standard_normal((2, 5, 5, 9, 11))
+    plan = O.make_plan((5, 9, 11), ((2, 1), (3, 2), (2, 3)))
+    tok = O.extract_tokens(plan, X)
+    for t in range(plan.num_tiles):
+        (f0, f1), (h0, h1), (w0, w1) = plan.box(t)
+        assert tok[t].shape == (2, (f1 - f0) * (h1 - h0) * (w1 - w0), 5)
+        n = 0
+        for f in range(f0, f1):
+            for h in range(h0, h1):
+                for w in range(w0, w1):
+                    for b in range(2):
+                        for c in range(5):
+                            assert tok[t][b, n, c] == X[b, c, f, h, w]
+                    n += 1
+        assert n == tok[t].shape[1]
+
+
+def test_extract_tokens_carry_their_positions():
+    """Token n of tile t sits at the point whose generated-token position is
+    the n-th entry of the tile's (unnormalised) position list: the value
+    latent encodes each point's grid position, so the two layouts agree."""
+    F, H, W = 4, 16, 16
+    plan = O.make_plan((F, H, W), ((2, 1), (2, 4), (2, 4)))
+    gen = inputs.grid_positions(1, F, H, W)
+    f, h, w = np.meshgrid(np.arange(F), np.arange(H), np.arange(W), indexing="ij")
+    X = np.stack([f * 8, h * 32, w * 32]).astype(np.float64)[None]      # [1, 3, F, H, W]
+    tok = O.extract_tokens(plan, X)
+    raw, _ = O.positions(plan, gen, normalize=False)
+    for t in range(plan.num_tiles):
+        assert np.array_equal(tok[t][0].T, raw[t][0, :, :, 0])           # [3, N_t] starts
+
+
+def test_extract_tokens_single_tile_is_patchify():
+    """One tile: the token sequence is the latent flattened over (F, H, W)
+    and transposed to channel-last."""
+    X = inputs.latent((2, 3, 4, 5, 6), seed=4).astype(np.float64)
+    plan = O.make_plan((4, 5, 6), ((1, 0), (1, 0), (1, 0)))
+    tok = O.extract_tokens(plan, X)
+    assert len(tok) == 1
+    assert np.array_equal(tok[0], np.moveaxis(X.reshape(2, 3, 120), 1, 2))
+    assert np.array_equal(O.blend_tokens(plan, tok), X)
+
+
+@pytest.mark.parametrize("name", ["tiny", "stage1", "strips", "grid"])
+def test_blend_tokens_identity_reproduces_input(name):
+    wl = WORKLOADS[name]
+    X = inputs.latent((wl.B, min(wl.C, 4)) + wl.dims, seed=0).astype(np.float64)
+    plan = O.make_plan(wl.dims, wl.tiling)
+    assert np.max(np.abs(O.blend_tokens(plan, O.extract_tokens(plan, X)) - X)) < 1e-12
+
+
+def test_blend_tokens_bruteforce_exact_weights():
+    """Per-tile, per-channel random token outputs, summed point by point with
+    the exact rational window of each tile (no reshape, no window array)."""
+    rng = np.random.default_rng(9)
+    dims = (3, 7, 9)
+    plan = O.make_plan(dims, ((2, 1), (2, 2), (3, 2)), compat=True)
+    C = 3
+    tok = [rng.standard_normal((1, int(np.prod(plan.shape(t))), C)) for t in range(plan.num_tiles)]
+    Y = O.blend_tokens(plan, tok)
+    for f, h, w in itertools.product(*(range(d) for d in dims)):
+        want = np.zeros(C)
+        for t in range(plan.num_tiles):
+            (f0, f1), (h0, h1), (w0, w1) = plan.box(t)
+            if not (f0 <= f < f1 and h0 <= h < h1 and w0 <= w < w1):
+                continue
+            i = plan.tile_index(t)
+            wt = Fraction(1)
+            for d, x in enumerate((f, h, w)):
+                wt *= O.ramp_exact(plan.intervals[d], plan.overlaps[d], i[d], x)
+            n = ((f - f0) * (h1 - h0) + (h - h0)) * (w1 - w0) + (w - w0)
+            want += float(wt) * tok[t][0, n]
+        assert np.max(np.abs(Y[0, :, f, h, w] - want)) < 1e-12
+
+
+def test_blend_tokens_agrees_with_channel_first_blend():
+    """The same per-tile outputs in either layout blend to the same latent."""
+    rng = np.random.default_rng(12)
+    plan = O.make_plan((16, 68, 120), ((2, 2), (4, 8), (4, 12)))
+    B, C = 1, 2
+    tiles = [rng.standard_normal((B, C) + plan.shape(t)) for t in range(plan.num_tiles)]
+    tok = [np.moveaxis(x.reshape(B, C, -1), 1, 2) for x in tiles]
+    assert np.max(np.abs(O.blend_tokens(plan, tok) - O.blend(plan, tiles))) < 1e-12
+
+
+def test_tokens_packing_uses_channel_first_offsets():
+    plan = O.make_plan((5, 9, 11), ((2, 1), (3, 2), (2, 3)))
+    X = np.random.default_rng(2).standard_normal((2, 4, 5, 9, 11))
+    tok = O.extract_tokens(plan, X)
+    flat = O.pack(tok)
+    assert flat.size == O.pack(O.extract(plan, X)).size
+    back = O.unpack_tokens(plan, 2, 4, flat)
+    assert all(np.array_equal(a, b) for a, b in zip(back, tok))
