@@ -349,6 +349,27 @@ def run_tdp(args, rank: int, world: int):
     torch.cuda.synchronize()
     comb_ms = float(np.median([e[0].elapsed_time(e[1]) for e in cev]))
 
+    # The next row after that: the token-major pair (tiles as [B, N_t, C] token
+    # sequences), each launch timed alone after an L2 flush outside its events.
+    tm_tiles = torch.empty_like(tiles)
+    tm_out = torch.empty_like(X)
+
+    def time_alone(fn, reps: int = 20) -> float:
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+        for e in ev2:
+            flush.zero_()
+            e[0].record(stream)
+            fn()
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        return float(np.median([e[0].elapsed_time(e[1]) for e in ev2]))
+
+    tmx_ms = time_alone(lambda: tdp.extract_tokens(p, X, tm_tiles))
+    tmb_ms = time_alone(lambda: tdp.blend_tokens(p, tm_tiles, wl.B, wl.C, tm_out))
+
     # e2e: host buffers in, blended latent out, through the same C-ABI calls
     X_h = X.cpu().pin_memory()
     gen_h = gen.cpu().pin_memory()
@@ -405,7 +426,12 @@ def run_tdp(args, rank: int, world: int):
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
         "gpu_launches": KERNELS_PER_STEP * K,
         "next_rows": {"cond_combine": {"ms": comb_ms, "workload": f"T={p.T} tiles, B={wl.B}, M={wl.num_cond} "
-                                       f"conditioning tokens, D={wl.C} bf16 features; median of 20, not in the step"}},
+                                       f"conditioning tokens, D={wl.C} bf16 features; median of 20, not in the step"},
+                      "token_major": {
+                          "extract_tokens": {"ms": tmx_ms, "gbs": ab["extract"] / (tmx_ms * 1e-3) / 1e9},
+                          "blend_tokens": {"ms": tmb_ms, "gbs": ab["blend"] / (tmb_ms * 1e-3) / 1e9},
+                          "workload": "the step's latent and tiles with each tile as [B, N_t, C] tokens; "
+                                      "median of 20 launches, each after an L2 flush; not in the step"}},
         "clocks": clocks,
         "timed_wall_s": wall,
     }

@@ -68,7 +68,7 @@ typedef enum {
     TDP_ERR_TOO_MANY_TILES = 3,  /* num_tiles > TDP_MAX_PER_AXIS */
     TDP_ERR_ALIGNMENT = 4,       /* a device pointer is not 16-byte aligned */
     TDP_ERR_CUDA = 5,            /* a CUDA launch or runtime call failed */
-    TDP_ERR_UNSUPPORTED = 6      /* a tile row is too long for shared-memory staging */
+    TDP_ERR_UNSUPPORTED = 6      /* a shape the kernels cannot stage (see each call) */
 } tdp_status;
 
 typedef enum { TDP_F32 = 0, TDP_BF16 = 1 } tdp_dtype;
@@ -270,6 +270,43 @@ tdp_status tdp_cond_combine(const tdp_plan_t* plan, int32_t B, int32_t M, int32_
  */
 tdp_status tdp_blend(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_dtype,
                      const void* tiles, tdp_dtype out_dtype, void* out, cudaStream_t stream);
+
+/*
+ * tdp_extract_tokens -- step 2 into token-major tiles.
+ *
+ * Source: "Tiled Data Parallelism (TDP)", What it is and When to use it
+ * (every tile goes through the transformer on its own, as the sequence of
+ * its N_t = f_t*h_t*w_t tokens) and Position normalization (a tile's
+ * generated tokens are its sub-grid of the latent's token grid, in the
+ * grid's row-major order).
+ *   tokens[t][b, n, c] = latent[b, c, f0_t + k, h0_t + y, w0_t + x],
+ *   n = (k * h_t + y) * w_t + x
+ * latent: device, [B, C, F, H, W] of `dtype`.
+ * tokens: device, packed tile after tile like tdp_extract (tile t starts at
+ *         element tdp_tile_offset(plan, t, B, C)), each tile [B, N_t, C]
+ *         with C fastest; tdp_tiles_numel elements of `dtype`.
+ * C * sizeof(dtype) must be a multiple of 16 bytes and at most 16 KiB
+ * (else TDP_ERR_UNSUPPORTED).  Bit-exact copy.  Asynchronous on `stream`.
+ */
+tdp_status tdp_extract_tokens(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype dtype,
+                              const void* latent, void* tokens, cudaStream_t stream);
+
+/*
+ * tdp_blend_tokens -- step 5 from token-major tiles.
+ *
+ * Source: as tdp_blend, with the tiles in the layout of tdp_extract_tokens.
+ *   out[b,c,f,h,w] = sum over tiles t covering (f,h,w) of
+ *                    r_f(f) * r_h(h) * r_w(w) * tokens[t][b, n_t(f,h,w), c]
+ * with n_t(f,h,w) = ((f-f0)*h_t + (h-h0))*w_t + (w-w0) and the same fp32
+ * windows as tdp_blend.  fp32 accumulation, one store per element in
+ * `out_dtype` (round to nearest even for bf16); every element of `out` is
+ * written.  tokens: device, packed token-major, `in_dtype`.
+ * out: device [B, C, F, H, W].  C * sizeof(in_dtype) must be a multiple of
+ * 16 bytes and at most 16 KiB (else TDP_ERR_UNSUPPORTED).
+ * Asynchronous on `stream`.
+ */
+tdp_status tdp_blend_tokens(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_dtype,
+                            const void* tokens, tdp_dtype out_dtype, void* out, cudaStream_t stream);
 
 /*
  * tdp_window_sum -- window-sum check (K3).

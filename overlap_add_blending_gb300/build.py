@@ -2,7 +2,8 @@
 
     python -m overlap_add_blending_gb300.build
 
-Two translation units (host planner, kernels) compiled in parallel and
+Three translation units (host planner, channel-first kernels, token-major
+kernels) compiled in parallel and
 linked into overlap_add_blending_gb300/libtdp.so.  The CUDA runtime is
 linked statically, so the library needs only the driver at run time.
 """
@@ -22,7 +23,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtdp.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["tdp_plan.cpp", "tdp_kernels.cu"]
+SOURCES = ["tdp_plan.cpp", "tdp_kernels.cu", "tdp_token_major.cu"]
 
 
 def _nvcc() -> str:

@@ -61,6 +61,19 @@ TDP_HD void axis_range_cover(const tdp_plan_t& p, int d, int x0, int x1, int& lo
     (void)b;
 }
 
+#if defined(__CUDACC__)
+// 1-D trapezoid of tile i on axis d at coordinate x (x inside the tile):
+// rising ramp min(1, (x-a+1)/(o+1)) except on the first tile, falling ramp
+// min(1, (e-x)/(o+1)) except on the last, multiplied.  IEEE fp32 division.
+__device__ __forceinline__ float axis_weight(const tdp_plan_t& p, int d, int i, int x) {
+    const float o1 = static_cast<float>(p.overlap[d] + 1);
+    float up = 1.0f, dn = 1.0f;
+    if (i > 0) up = fminf(1.0f, static_cast<float>(x - p.start[d][i] + 1) / o1);
+    if (i < p.num_tiles[d] - 1) dn = fminf(1.0f, static_cast<float>(p.end[d][i] - x) / o1);
+    return __fmul_rn(up, dn);
+}
+#endif
+
 }  // namespace tdp
 
 #endif  // TDP_GEOMETRY_H_

@@ -157,16 +157,7 @@ __device__ __forceinline__ void load_plan(tdp_plan_t* dst, const tdp_plan_t& src
 
 // ------------------------------------------------------------------ element helpers
 
-// 1-D trapezoid of tile i on axis d at coordinate x (x inside the tile):
-// rising ramp min(1, (x-a+1)/(o+1)) except on the first tile, falling ramp
-// min(1, (e-x)/(o+1)) except on the last, multiplied.  IEEE fp32 division.
-__device__ __forceinline__ float axis_weight(const tdp_plan_t& p, int d, int i, int x) {
-    const float o1 = static_cast<float>(p.overlap[d] + 1);
-    float up = 1.0f, dn = 1.0f;
-    if (i > 0) up = fminf(1.0f, static_cast<float>(x - p.start[d][i] + 1) / o1);
-    if (i < p.num_tiles[d] - 1) dn = fminf(1.0f, static_cast<float>(p.end[d][i] - x) / o1);
-    return __fmul_rn(up, dn);
-}
+using tdp::axis_weight;
 
 // ------------------------------------------------------------------ block / warp scans
 __device__ __forceinline__ int warp_incl_scan(int v) {
@@ -2115,6 +2106,12 @@ tdp_status launch_blend(const tdp_plan_t& p, int BC, const void* tiles, long lon
 }
 
 }  // namespace
+
+namespace tdp {
+// Shared with the token-major translation unit.
+tdp_status record_cuda(cudaError_t e) { return cuda_status(e); }
+int device_sm_count() { return sm_count(); }
+}  // namespace tdp
 
 extern "C" {
 

@@ -100,6 +100,11 @@ _lib.tdp_extract.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int, C.c_void_p
 _lib.tdp_extract.restype = C.c_int
 _lib.tdp_blend.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]
 _lib.tdp_blend.restype = C.c_int
+_lib.tdp_extract_tokens.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p]
+_lib.tdp_extract_tokens.restype = C.c_int
+_lib.tdp_blend_tokens.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_int, C.c_void_p,
+                                  C.c_void_p]
+_lib.tdp_blend_tokens.restype = C.c_int
 _lib.tdp_window_sum.argtypes = [_P(Plan), C.c_void_p, C.c_void_p, C.c_void_p]
 _lib.tdp_window_sum.restype = C.c_int
 _lib.tdp_positions.argtypes = [_P(Plan), C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]
@@ -129,7 +134,7 @@ if _lib.tdp_plan_struct_size() != C.sizeof(Plan):
 
 EXPORTS = ("tdp_plan", "tdp_tile_offset", "tdp_tiles_numel", "tdp_tile_box", "tdp_plan_stats",
            "tdp_extract", "tdp_positions", "tdp_cond_select", "tdp_tokens", "tdp_cond_combine", "tdp_blend",
-           "tdp_window_sum",
+           "tdp_extract_tokens", "tdp_blend_tokens", "tdp_window_sum",
            "tdp_device_error", "tdp_status_str", "tdp_last_cuda_error", "tdp_plan_struct_size")
 
 
@@ -222,6 +227,37 @@ def blend(p: Plan, tiles: torch.Tensor, B: int, C_: int, out: Optional[torch.Ten
         raise ValueError("out has the wrong shape")
     _check(_lib.tdp_blend(C.byref(p), B, C_, _dtype_code(tiles.dtype), _dev(tiles, "tiles"),
                           _dtype_code(out.dtype), _dev(out, "out"), _stream(stream)), "tdp_blend")
+    return out
+
+
+def extract_tokens(p: Plan, latent: torch.Tensor, tokens: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """tdp_extract_tokens: latent [B, C, F, H, W] -> packed token-major tiles
+    (1-D, same dtype; tile t is [B, N_t, C] at tile_offset(t, B, C))."""
+    if latent.dim() != 5 or tuple(latent.shape[2:]) != tuple(p.dims):
+        raise ValueError(f"latent must be [B, C, {tuple(p.dims)}], got {tuple(latent.shape)}")
+    B, Cc = int(latent.shape[0]), int(latent.shape[1])
+    n = p.tiles_numel(B, Cc)
+    if tokens is None:
+        tokens = torch.empty(n, dtype=latent.dtype, device=latent.device)
+    if tokens.numel() != n or tokens.dtype != latent.dtype:
+        raise ValueError("tokens buffer has the wrong size or dtype")
+    _check(_lib.tdp_extract_tokens(C.byref(p), B, Cc, _dtype_code(latent.dtype), _dev(latent, "latent"),
+                                   _dev(tokens, "tokens"), _stream(stream)), "tdp_extract_tokens")
+    return tokens
+
+
+def blend_tokens(p: Plan, tokens: torch.Tensor, B: int, C_: int, out: Optional[torch.Tensor] = None,
+                 out_dtype: Optional[torch.dtype] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """tdp_blend_tokens: packed token-major tiles -> latent [B, C, F, H, W]."""
+    if tokens.numel() != p.tiles_numel(B, C_):
+        raise ValueError("tokens has the wrong number of elements for this plan and batch")
+    if out is None:
+        out = torch.empty((B, C_) + tuple(p.dims), dtype=out_dtype or tokens.dtype, device=tokens.device)
+    if tuple(out.shape) != (B, C_) + tuple(p.dims):
+        raise ValueError("out has the wrong shape")
+    _check(_lib.tdp_blend_tokens(C.byref(p), B, C_, _dtype_code(tokens.dtype), _dev(tokens, "tokens"),
+                                 _dtype_code(out.dtype), _dev(out, "out"), _stream(stream)), "tdp_blend_tokens")
     return out
 
 
