@@ -417,3 +417,118 @@ def layout_stats(axis_intervals: Sequence[Sequence[Tuple[int, int]]], dims: Sequ
         per_rank[t % ranks] += v
     even = sum(vols) / ranks
     return LayoutStats(area, seams, max(vols) / latent, max(per_rank) / even - 1.0)
+
+
+# ---------------------------------------------------------------------------
+# Layout planning (TDP docs §Usage: a balanced height x width tile grid from
+# the rank count; DistVAE "Choosing a tile window" §Benchmark plan selection:
+# search grids of max(2, ranks)..4*ranks tiles, drop unsupported windows,
+# keep the candidates no other one beats on window area, decoded area, rank
+# imbalance and tile columns, and name coarse / fine / balanced among them).
+# ---------------------------------------------------------------------------
+def balanced_tile_split(ranks: int) -> Tuple[int, int]:
+    """(height tiles, width tiles): the factor pair of `ranks` closest to a
+    square, the smaller count on height (the latents here are wider than
+    tall).  Reading: the pages print only the call, not the rule."""
+    if ranks < 1:
+        raise ValueError("ranks must be >= 1")
+    h = max(d for d in range(1, int(np.sqrt(ranks)) + 2) if d * d <= ranks and ranks % d == 0)
+    return h, ranks // h
+
+
+@dataclass
+class LayoutCandidate:
+    counts: Tuple[int, int, int]       # (n_f, n_h, n_w)
+    overlaps: Tuple[int, int, int]
+    window_volume: int                 # largest tile's f*h*w (window area, frames fixed)
+    decoded_volume: int                # sum of tile volumes (decoded area)
+    heaviest_rank_volume: int          # round-robin assignment, tile t -> rank t mod ranks
+    seams: int
+    role: str = ""                     # "coarse", "fine", "balanced", "frontier" or "dominated"
+
+    @property
+    def columns(self) -> int:
+        return self.counts[2]
+
+    def imbalance(self, ranks: int) -> float:
+        return self.heaviest_rank_volume * ranks / self.decoded_volume - 1.0
+
+
+def _beats(a: LayoutCandidate, b: LayoutCandidate) -> bool:
+    """a is no worse than b on every criterion and better on one (imbalance
+    compared as heaviest/total, cross-multiplied to stay exact)."""
+    ia = a.heaviest_rank_volume * b.decoded_volume
+    ib = b.heaviest_rank_volume * a.decoded_volume
+    le = (a.window_volume <= b.window_volume and a.decoded_volume <= b.decoded_volume
+          and ia <= ib and a.columns <= b.columns)
+    lt = (a.window_volume < b.window_volume or a.decoded_volume < b.decoded_volume
+          or ia < ib or a.columns < b.columns)
+    return le and lt
+
+
+def search_layouts(dims: Sequence[int], ranks: int, frames: Tuple[int, int], overlap_h: int, overlap_w: int,
+                   compat: bool = False, limits: bool = True) -> List[LayoutCandidate]:
+    """Every supported (n_h, n_w) grid with max(2, ranks) <= n_f*n_h*n_w <=
+    4*ranks, each marked with its role.  With `limits`, the DistVAE limits
+    apply: the latent's narrow spatial axis holds >= 16 units and >= one
+    unit per rank (else no candidate), and every tiled spatial axis has
+    overlap >= a quarter of its window (stride + overlap).  An untiled axis
+    takes overlap 0."""
+    F, H, W = (int(v) for v in dims)
+    if ranks < 1:
+        raise ValueError("ranks must be >= 1")
+    if limits and min(H, W) < max(16, ranks):
+        return []
+    lo, hi = max(2, ranks), 4 * ranks
+    out = []
+    for n_h in range(1, H + 1):
+        for n_w in range(1, W + 1):
+            if not lo <= frames[0] * n_h * n_w <= hi:
+                continue
+            oh = overlap_h if n_h > 1 else 0
+            ow = overlap_w if n_w > 1 else 0
+            try:
+                plan = make_plan((F, H, W), (frames, (n_h, oh), (n_w, ow)), compat=compat)
+            except ValueError:
+                continue                                   # unsupported window (incl. the guard)
+            if limits:
+                windows = [(plan.intervals[d][0][1] - plan.intervals[d][0][0], plan.overlaps[d])
+                           for d in (1, 2) if plan.counts[d] > 1]
+                if any(4 * o < win for win, o in windows):
+                    continue
+            vols = [int(np.prod(plan.shape(t))) for t in range(plan.num_tiles)]
+            per_rank = [0] * ranks
+            for t, v in enumerate(vols):
+                per_rank[t % ranks] += v
+            stats = layout_stats(plan.intervals, plan.dims, ranks)
+            out.append(LayoutCandidate(plan.counts, plan.overlaps, max(vols), sum(vols), max(per_rank),
+                                       stats.seams))
+    frontier = [c for c in out if not any(_beats(d, c) for d in out)]
+    for c in out:
+        c.role = "frontier" if c in frontier else "dominated"
+    if not frontier:
+        return out
+
+    def ties(c):   # fixed order among equals: less decoded, less imbalance, fewer columns, fewer rows
+        return (c.decoded_volume, Fraction(c.heaviest_rank_volume, c.decoded_volume), c.columns, c.counts[1])
+
+    coarse = min(frontier, key=lambda c: (-c.window_volume,) + ties(c))
+    coarse.role = "coarse"
+    rest = [c for c in frontier if c is not coarse]
+    if rest:
+        fine = min(rest, key=lambda c: (c.window_volume,) + ties(c))
+        fine.role = "fine"
+        rest = [c for c in rest if c is not fine]
+    if rest:
+        # worst of the three scores, each divided by its largest value on the frontier
+        top_w = max(c.window_volume for c in frontier)
+        top_d = max(c.decoded_volume for c in frontier)
+        top_i = max(c.imbalance(ranks) for c in frontier)
+
+        def score(c):
+            s_i = c.imbalance(ranks) / top_i if top_i > 0 else 0.0
+            return max(c.window_volume / top_w, c.decoded_volume / top_d, s_i)
+
+        balanced = min(rest, key=lambda c: (score(c),) + ties(c))
+        balanced.role = "balanced"
+    return out

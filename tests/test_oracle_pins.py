@@ -525,3 +525,83 @@ def test_tokens_packing_uses_channel_first_offsets():
     assert flat.size == O.pack(O.extract(plan, X)).size
     back = O.unpack_tokens(plan, 2, 4, flat)
     assert all(np.array_equal(a, b) for a, b in zip(back, tok))
+
+
+# ---------------------------------------------------------------- layout planning
+def test_balanced_tile_split_is_the_squarest_factor_pair():
+    assert [O.balanced_tile_split(r) for r in (1, 2, 4, 6, 8, 12, 16, 7)] == \
+        [(1, 1), (1, 2), (2, 2), (2, 3), (2, 4), (3, 4), (4, 4), (1, 7)]
+    for r in range(1, 300):
+        h, w = O.balanced_tile_split(r)
+        pairs = [(a, r // a) for a in range(1, r + 1) if r % a == 0]
+        assert h * w == r and h <= w
+        assert w - h == min(abs(b - a) for a, b in pairs)
+
+
+@pytest.mark.parametrize("ranks", [2, 3])
+def test_search_layouts_hand_worked_cases(golden_rows, ranks):
+    got = {(c.counts, c.window_volume, c.decoded_volume, c.heaviest_rank_volume, c.seams, c.role)
+           for c in O.search_layouts((1, 32, 32), ranks, (1, 0), 4, 4)}
+    want = {((int(r[0]), int(r[1]), int(r[2])), int(r[3]), int(r[4]), int(r[5]), int(r[6]), r[7])
+            for r in golden_rows(f"plan_search_32x32_r{ranks}.txt")}
+    assert got == want
+
+
+def test_dominance_compares_imbalance_as_a_share():
+    """Less decoded work does not beat a layout whose heaviest rank carries a
+    smaller share of its (larger) total: 60/100 of the work against 100/200."""
+    a = O.LayoutCandidate((1, 2, 1), (0, 4, 0), 10, 100, 60, 1)
+    b = O.LayoutCandidate((1, 2, 1), (0, 4, 0), 10, 200, 100, 1)
+    assert not O._beats(a, b) and not O._beats(b, a)
+    c = O.LayoutCandidate((1, 2, 1), (0, 4, 0), 10, 100, 50, 1)
+    assert O._beats(c, b) and not O._beats(b, c)
+    d = O.LayoutCandidate((1, 1, 2), (0, 0, 4), 10, 100, 50, 2)    # same, one more tile column
+    assert O._beats(c, d) and not O._beats(d, c)
+
+
+@pytest.mark.parametrize("dims,ranks,frames,oh,ow,limits", [
+    ((16, 68, 120), 8, (2, 2), 8, 12, True),
+    ((16, 68, 120), 4, (1, 0), 8, 12, True),
+    ((1, 128, 128), 4, (1, 0), 8, 8, True),
+    ((16, 32, 48), 2, (1, 0), 8, 12, False),
+    ((16, 16, 24), 4, (1, 0), 4, 6, False),
+])
+def test_search_layouts_frontier_properties(dims, ranks, frames, oh, ow, limits):
+    cands = O.search_layouts(dims, ranks, frames, oh, ow, limits=limits)
+    assert cands
+    front = [c for c in cands if c.role != "dominated"]
+    for c in cands:
+        T = c.counts[0] * c.counts[1] * c.counts[2]
+        assert max(2, ranks) <= T <= 4 * ranks
+        beaten = any(O._beats(d, c) for d in cands)
+        assert beaten == (c.role == "dominated")
+        if beaten:     # beaten by the frontier itself (the relation is transitive)
+            assert any(O._beats(d, c) for d in front)
+    roles = [c.role for c in front]
+    assert roles.count("coarse") == 1 and roles.count("fine") == (len(front) > 1)
+    assert roles.count("balanced") == (len(front) > 2)
+    coarse = next(c for c in front if c.role == "coarse")
+    assert coarse.window_volume == max(c.window_volume for c in front)
+    if len(front) > 1:
+        fine = next(c for c in front if c.role == "fine")
+        assert fine.window_volume == min(c.window_volume for c in front if c is not coarse)
+
+
+def test_search_layouts_contains_the_4k_workload_tiling():
+    """The bench's 4k tiling (2x4x4, overlaps 2/8/12) is a supported grid
+    for 8 ranks; its window is one tile of 9x23x39 tokens."""
+    cands = O.search_layouts((16, 68, 120), 8, (2, 2), 8, 12)
+    c = next(c for c in cands if c.counts == (2, 4, 4))
+    assert c.window_volume == 9 * 23 * 39
+    assert c.decoded_volume == 32 * 9 * 23 * 39
+    assert c.heaviest_rank_volume * 8 == c.decoded_volume   # 32 equal tiles over 8 ranks
+
+
+def test_search_layouts_limits():
+    # a latent narrower than 16 units, or than one unit per rank, has no candidate
+    assert O.search_layouts((1, 15, 64), 2, (1, 0), 4, 4) == []
+    assert O.search_layouts((1, 20, 64), 24, (1, 0), 4, 4) == []
+    # without the limits the quarter-window rule no longer drops wide windows
+    with_l = {c.counts for c in O.search_layouts((1, 32, 32), 2, (1, 0), 4, 4)}
+    without = {c.counts for c in O.search_layouts((1, 32, 32), 2, (1, 0), 4, 4, limits=False)}
+    assert (1, 2, 1) in without - with_l
