@@ -370,6 +370,14 @@ def run_tdp(args, rank: int, world: int):
     tmx_ms = time_alone(lambda: tdp.extract_tokens(p, X, tm_tiles))
     tmb_ms = time_alone(lambda: tdp.blend_tokens(p, tm_tiles, wl.B, wl.C, tm_out))
 
+    # The host planner (the last next row): the layout search for this
+    # latent at 8 ranks, frame tiling and overlaps as in the workload.
+    t0 = time.perf_counter()
+    for _ in range(20):
+        cands = tdp.search_layouts(wl.dims, 8, wl.tiling[0], wl.tiling[1][1], wl.tiling[2][1])
+    search_us = (time.perf_counter() - t0) / 20 * 1e6
+    picks = {c["role"]: list(c["counts"]) for c in cands if c["role"] in ("coarse", "fine", "balanced")}
+
     # e2e: host buffers in, blended latent out, through the same C-ABI calls
     X_h = X.cpu().pin_memory()
     gen_h = gen.cpu().pin_memory()
@@ -431,7 +439,10 @@ def run_tdp(args, rank: int, world: int):
                           "extract_tokens": {"ms": tmx_ms, "gbs": ab["extract"] / (tmx_ms * 1e-3) / 1e9},
                           "blend_tokens": {"ms": tmb_ms, "gbs": ab["blend"] / (tmb_ms * 1e-3) / 1e9},
                           "workload": "the step's latent and tiles with each tile as [B, N_t, C] tokens; "
-                                      "median of 20 launches, each after an L2 flush; not in the step"}},
+                                      "median of 20 launches, each after an L2 flush; not in the step"},
+                      "layout_search": {"us": search_us, "ranks": 8, "candidates": len(cands), "picks": picks,
+                                        "workload": "host layout search for this latent, frame tiling and "
+                                                    "overlaps; mean of 20 calls"}},
         "clocks": clocks,
         "timed_wall_s": wall,
     }

@@ -139,6 +139,65 @@ tdp_status tdp_plan_stats(const tdp_plan_t* plan, int32_t ranks, double* decoded
                           double* max_window_sum);
 
 /*
+ * tdp_balanced_tile_split -- height x width tile counts for a rank count.
+ *
+ * Source: "Tiled Data Parallelism (TDP)", Usage: balanced_tile_split(world
+ * size) gives the balanced 2-D spatial grid of the upscale stage.  The rule
+ * is not printed; the one used here is the factor pair of `ranks` closest to
+ * a square, with the smaller count on height (the latents are wider than
+ * tall).  ranks >= 1; h_tiles, w_tiles: host pointers.  Host only.
+ */
+tdp_status tdp_balanced_tile_split(int32_t ranks, int32_t* h_tiles, int32_t* w_tiles);
+
+#define TDP_SEARCH_NO_LIMITS 2u   /* tdp_search_layouts: skip the DistVAE window limits */
+
+typedef enum {
+    TDP_ROLE_DOMINATED = 0,   /* another candidate is no worse on every criterion and better on one */
+    TDP_ROLE_FRONTIER = 1,    /* on the frontier, not selected */
+    TDP_ROLE_COARSE = 2,      /* the frontier's largest window */
+    TDP_ROLE_FINE = 3,        /* the smallest window among the rest */
+    TDP_ROLE_BALANCED = 4     /* the least worst normalised score among the rest */
+} tdp_layout_role;
+
+typedef struct {
+    int32_t num_tiles[3];           /* n_f, n_h, n_w */
+    int32_t overlap[3];
+    int64_t window_volume;          /* largest tile, f*h*w latent units (window area) */
+    int64_t decoded_volume;         /* sum of tile volumes (decoded area) */
+    int64_t heaviest_rank_volume;   /* round-robin, tile t on rank t mod ranks */
+    int32_t seams;                  /* sum_a (n_a - 1) * prod_{b != a} n_b */
+    int32_t role;                   /* tdp_layout_role */
+} tdp_layout_candidate;
+
+/*
+ * tdp_search_layouts -- layout search over tile counts (host only).
+ *
+ * Source: DistVAE docs "Choosing a tile window", Benchmark plan selection,
+ * applied to TDP tile counts:
+ *   - candidates: every (n_h, n_w) with max(2, ranks) <= n_f*n_h*n_w <=
+ *     4*ranks whose plan tdp_plan accepts (the frame axis keeps `frames`;
+ *     a tiled spatial axis takes overlap_h / overlap_w, an untiled one 0);
+ *   - unless TDP_SEARCH_NO_LIMITS: no candidate at all when the latent's
+ *     narrow spatial axis has fewer than max(16, ranks) units, and none
+ *     whose overlap on a tiled spatial axis is below a quarter of the
+ *     window (stride + overlap) -- the page's conservative limits;
+ *   - roles: dominated / frontier on window area, decoded area, rank
+ *     imbalance (heaviest / total) and tile columns; among the frontier,
+ *     coarse = largest window, fine = smallest window among the rest,
+ *     balanced = least max(window / top window, decoded / top decoded,
+ *     imbalance / top imbalance) among the rest (tops over the frontier);
+ *     ties go to less decoded area, less imbalance, fewer columns, fewer rows.
+ * flags: TDP_PLAN_UPSTREAM_COMPAT (plans without the guard) and/or
+ *        TDP_SEARCH_NO_LIMITS.
+ * out:   host array of `capacity` entries (NULL allowed when capacity is 0).
+ * count: receives the number of candidates; when it exceeds `capacity`
+ *        only the first `capacity` are written.  Order: n_h, then n_w.
+ */
+tdp_status tdp_search_layouts(const int32_t dims_fhw[3], int32_t ranks, const tdp_dim_cfg* frames,
+                              int32_t overlap_h, int32_t overlap_w, uint32_t flags,
+                              tdp_layout_candidate* out, int32_t capacity, int32_t* count);
+
+/*
  * tdp_extract -- step 2, tile extract (K1).
  *
  * Source: "Tiled Data Parallelism (TDP)", What it is (each tile is the

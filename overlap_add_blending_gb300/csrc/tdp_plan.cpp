@@ -61,6 +61,35 @@ std::vector<int64_t> axis_sum_numerators(const tdp_plan_t& p, int d) {
     return s;
 }
 
+// ---------------------------------------------------------------- layout search
+// The criteria of DistVAE "Choosing a tile window" (Benchmark plan
+// selection): window area, decoded area, rank imbalance, tile columns.
+// Imbalance is heaviest rank / total, compared by cross-multiplying.
+bool beats(const tdp_layout_candidate& a, const tdp_layout_candidate& b) {
+    const __int128 ia = (__int128)a.heaviest_rank_volume * b.decoded_volume;
+    const __int128 ib = (__int128)b.heaviest_rank_volume * a.decoded_volume;
+    const bool le = a.window_volume <= b.window_volume && a.decoded_volume <= b.decoded_volume && ia <= ib &&
+                    a.num_tiles[2] <= b.num_tiles[2];
+    const bool lt = a.window_volume < b.window_volume || a.decoded_volume < b.decoded_volume || ia < ib ||
+                    a.num_tiles[2] < b.num_tiles[2];
+    return le && lt;
+}
+
+// Fixed order among candidates equal on the selection key: less decoded
+// area, less imbalance, fewer tile columns, fewer tile rows.
+bool before_on_ties(const tdp_layout_candidate& a, const tdp_layout_candidate& b) {
+    if (a.decoded_volume != b.decoded_volume) return a.decoded_volume < b.decoded_volume;
+    const __int128 ia = (__int128)a.heaviest_rank_volume * b.decoded_volume;
+    const __int128 ib = (__int128)b.heaviest_rank_volume * a.decoded_volume;
+    if (ia != ib) return ia < ib;
+    if (a.num_tiles[2] != b.num_tiles[2]) return a.num_tiles[2] < b.num_tiles[2];
+    return a.num_tiles[1] < b.num_tiles[1];
+}
+
+double imbalance_of(const tdp_layout_candidate& c, int ranks) {
+    return (double)(c.heaviest_rank_volume * ranks) / (double)c.decoded_volume - 1.0;
+}
+
 }  // namespace
 
 namespace tdp {
@@ -170,6 +199,114 @@ tdp_status tdp_plan_stats(const tdp_plan_t* plan, int32_t ranks, double* decoded
     return TDP_OK;
 }
 
+tdp_status tdp_balanced_tile_split(int32_t ranks, int32_t* h_tiles, int32_t* w_tiles) {
+    if (ranks < 1 || !h_tiles || !w_tiles) return TDP_ERR_INVALID_ARG;
+    int32_t h = 1;
+    for (int64_t d = 1; d * d <= ranks; ++d)
+        if (ranks % d == 0) h = (int32_t)d;
+    *h_tiles = h;
+    *w_tiles = ranks / h;
+    return TDP_OK;
+}
+
+tdp_status tdp_search_layouts(const int32_t dims_fhw[3], int32_t ranks, const tdp_dim_cfg* frames,
+                              int32_t overlap_h, int32_t overlap_w, uint32_t flags, tdp_layout_candidate* out,
+                              int32_t capacity, int32_t* count) {
+    if (!dims_fhw || !frames || !count || ranks < 1 || capacity < 0 || (capacity > 0 && !out)) return TDP_ERR_INVALID_ARG;
+    if (flags & ~(TDP_PLAN_UPSTREAM_COMPAT | TDP_SEARCH_NO_LIMITS)) return TDP_ERR_INVALID_ARG;
+    const bool limits = !(flags & TDP_SEARCH_NO_LIMITS);
+    const uint32_t plan_flags = flags & TDP_PLAN_UPSTREAM_COMPAT;
+    const int32_t H = dims_fhw[1], W = dims_fhw[2];
+    *count = 0;
+    std::vector<tdp_layout_candidate> cands;
+    if (!(limits && std::min(H, W) < std::max(16, ranks))) {
+        const int64_t lo = std::max(2, ranks), hi = 4LL * ranks;
+        const int64_t nf = std::max(1, frames->num_tiles);
+        for (int32_t n_h = 1; n_h <= std::min(H, TDP_MAX_PER_AXIS) && nf * n_h <= hi; ++n_h) {
+            for (int32_t n_w = 1; n_w <= std::min(W, TDP_MAX_PER_AXIS) && nf * n_h * n_w <= hi; ++n_w) {
+                if (nf * n_h * n_w < lo) continue;
+                const tdp_tile_count_cfg cfg = {*frames, {n_h, n_h > 1 ? overlap_h : 0}, {n_w, n_w > 1 ? overlap_w : 0}};
+                tdp_plan_t p;
+                if (tdp_plan(dims_fhw, &cfg, plan_flags, &p) != TDP_OK) continue;   // unsupported window
+                if (limits) {
+                    // overlap >= a quarter of the window (stride + overlap) on every tiled spatial axis
+                    bool ok = true;
+                    for (int d = 1; d < 3; ++d)
+                        if (p.num_tiles[d] > 1 && 4LL * p.overlap[d] < (int64_t)p.end[d][0] - p.start[d][0]) ok = false;
+                    if (!ok) continue;
+                }
+                tdp_layout_candidate c;
+                std::memset(&c, 0, sizeof(c));
+                std::vector<int64_t> per_rank(ranks, 0);
+                for (int t = 0; t < p.total_tiles; ++t) {
+                    int i_f, i_h, i_w;
+                    tdp::tile_coords(p, t, i_f, i_h, i_w);
+                    const int64_t v =
+                        (int64_t)tdp::tile_size(p, 0, i_f) * tdp::tile_size(p, 1, i_h) * tdp::tile_size(p, 2, i_w);
+                    c.window_volume = std::max(c.window_volume, v);
+                    c.decoded_volume += v;
+                    per_rank[t % ranks] += v;
+                }
+                c.heaviest_rank_volume = *std::max_element(per_rank.begin(), per_rank.end());
+                for (int d = 0; d < 3; ++d) {
+                    c.num_tiles[d] = p.num_tiles[d];
+                    c.overlap[d] = p.overlap[d];
+                }
+                c.seams = (p.num_tiles[0] - 1) * p.num_tiles[1] * p.num_tiles[2] +
+                          (p.num_tiles[1] - 1) * p.num_tiles[0] * p.num_tiles[2] +
+                          (p.num_tiles[2] - 1) * p.num_tiles[0] * p.num_tiles[1];
+                cands.push_back(c);
+            }
+        }
+    }
+    std::vector<int> front;
+    for (size_t i = 0; i < cands.size(); ++i) {
+        bool beaten = false;
+        for (size_t j = 0; j < cands.size() && !beaten; ++j) beaten = beats(cands[j], cands[i]);
+        cands[i].role = beaten ? TDP_ROLE_DOMINATED : TDP_ROLE_FRONTIER;
+        if (!beaten) front.push_back((int)i);
+    }
+    if (!front.empty()) {
+        auto pick = [&](auto better) {   // first frontier member still marked FRONTIER under `better`
+            int best = -1;
+            for (int i : front)
+                if (cands[i].role == TDP_ROLE_FRONTIER && (best < 0 || better(cands[i], cands[best]))) best = i;
+            return best;
+        };
+        const int coarse = pick([](const tdp_layout_candidate& a, const tdp_layout_candidate& b) {
+            return a.window_volume != b.window_volume ? a.window_volume > b.window_volume : before_on_ties(a, b);
+        });
+        cands[coarse].role = TDP_ROLE_COARSE;
+        const int fine = pick([](const tdp_layout_candidate& a, const tdp_layout_candidate& b) {
+            return a.window_volume != b.window_volume ? a.window_volume < b.window_volume : before_on_ties(a, b);
+        });
+        if (fine >= 0) {
+            cands[fine].role = TDP_ROLE_FINE;
+            // worst of the three scores, each divided by its largest value on the frontier
+            int64_t top_w = 0, top_d = 0;
+            double top_i = 0.0;
+            for (int i : front) {
+                top_w = std::max(top_w, cands[i].window_volume);
+                top_d = std::max(top_d, cands[i].decoded_volume);
+                top_i = std::max(top_i, imbalance_of(cands[i], ranks));
+            }
+            auto score = [&](const tdp_layout_candidate& c) {
+                const double s_i = top_i > 0.0 ? imbalance_of(c, ranks) / top_i : 0.0;
+                return std::max(std::max((double)c.window_volume / (double)top_w,
+                                         (double)c.decoded_volume / (double)top_d), s_i);
+            };
+            const int balanced = pick([&](const tdp_layout_candidate& a, const tdp_layout_candidate& b) {
+                const double sa = score(a), sb = score(b);
+                return sa != sb ? sa < sb : before_on_ties(a, b);
+            });
+            if (balanced >= 0) cands[balanced].role = TDP_ROLE_BALANCED;
+        }
+    }
+    *count = (int32_t)cands.size();
+    for (int32_t i = 0; i < std::min<int32_t>(capacity, *count); ++i) out[i] = cands[i];
+    return TDP_OK;
+}
+
 size_t tdp_plan_struct_size(void) { return sizeof(tdp_plan_t); }
 
 const char* tdp_status_str(tdp_status status) {
@@ -180,7 +317,7 @@ const char* tdp_status_str(tdp_status status) {
         case TDP_ERR_TOO_MANY_TILES: return "more than TDP_MAX_PER_AXIS tiles on an axis";
         case TDP_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
         case TDP_ERR_CUDA: return "CUDA error";
-        case TDP_ERR_UNSUPPORTED: return "tile rows too long for shared-memory staging";
+        case TDP_ERR_UNSUPPORTED: return "shape not supported by the kernels (see the call)";
     }
     return "unknown status";
 }

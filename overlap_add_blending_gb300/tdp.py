@@ -84,6 +84,21 @@ class Plan(C.Structure):
         return int(_lib.tdp_tiles_numel(C.byref(self), 1, 1))
 
 
+class LayoutCandidate(C.Structure):
+    _fields_ = [
+        ("num_tiles", C.c_int32 * 3),
+        ("overlap", C.c_int32 * 3),
+        ("window_volume", C.c_int64),
+        ("decoded_volume", C.c_int64),
+        ("heaviest_rank_volume", C.c_int64),
+        ("seams", C.c_int32),
+        ("role", C.c_int32),
+    ]
+
+
+ROLES = {0: "dominated", 1: "frontier", 2: "coarse", 3: "fine", 4: "balanced"}
+SEARCH_NO_LIMITS = 2
+
 _P = C.POINTER
 _lib.tdp_plan.argtypes = [_P(C.c_int32 * 3), _P(TileCountCfg), C.c_uint32, _P(Plan)]
 _lib.tdp_plan.restype = C.c_int
@@ -120,6 +135,11 @@ _lib.tdp_tokens.restype = C.c_int
 _lib.tdp_cond_combine.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_void_p,
                                   C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]
 _lib.tdp_cond_combine.restype = C.c_int
+_lib.tdp_balanced_tile_split.argtypes = [C.c_int32, _P(C.c_int32), _P(C.c_int32)]
+_lib.tdp_balanced_tile_split.restype = C.c_int
+_lib.tdp_search_layouts.argtypes = [_P(C.c_int32 * 3), C.c_int32, _P(DimCfg), C.c_int32, C.c_int32, C.c_uint32,
+                                    _P(LayoutCandidate), C.c_int32, _P(C.c_int32)]
+_lib.tdp_search_layouts.restype = C.c_int
 _lib.tdp_device_error.argtypes = [_P(C.c_uint32), C.c_int32]
 _lib.tdp_device_error.restype = C.c_int
 _lib.tdp_status_str.argtypes = [C.c_int]
@@ -133,6 +153,7 @@ if _lib.tdp_plan_struct_size() != C.sizeof(Plan):
     raise ImportError("tdp_plan_t layout mismatch between libtdp.so and the binding")
 
 EXPORTS = ("tdp_plan", "tdp_tile_offset", "tdp_tiles_numel", "tdp_tile_box", "tdp_plan_stats",
+           "tdp_balanced_tile_split", "tdp_search_layouts",
            "tdp_extract", "tdp_positions", "tdp_cond_select", "tdp_tokens", "tdp_cond_combine", "tdp_blend",
            "tdp_extract_tokens", "tdp_blend_tokens", "tdp_window_sum",
            "tdp_device_error", "tdp_status_str", "tdp_last_cuda_error", "tdp_plan_struct_size")
@@ -173,6 +194,31 @@ def plan_stats(p: Plan, ranks: int = 1) -> PlanStats:
     _check(_lib.tdp_plan_stats(C.byref(p), ranks, C.byref(a), C.byref(s), C.byref(tf), C.byref(im), C.byref(mw)),
            "tdp_plan_stats")
     return PlanStats(a.value, s.value, tf.value, im.value, mw.value)
+
+
+def balanced_tile_split(ranks: int) -> Tuple[int, int]:
+    """tdp_balanced_tile_split: (height tiles, width tiles) for `ranks` ranks."""
+    h, w = C.c_int32(), C.c_int32()
+    _check(_lib.tdp_balanced_tile_split(int(ranks), C.byref(h), C.byref(w)), "tdp_balanced_tile_split")
+    return h.value, w.value
+
+
+def search_layouts(dims: Sequence[int], ranks: int, frames: Tuple[int, int] = (1, 0), overlap_h: int = 0,
+                   overlap_w: int = 0, compat: bool = False, limits: bool = True) -> list:
+    """tdp_search_layouts: every candidate grid as a dict (counts, overlaps,
+    volumes, seams, role), ordered by (n_h, n_w)."""
+    d = (C.c_int32 * 3)(*[int(v) for v in dims])
+    fr = DimCfg(*frames)
+    flags = (PLAN_UPSTREAM_COMPAT if compat else 0) | (0 if limits else SEARCH_NO_LIMITS)
+    n = C.c_int32()
+    _check(_lib.tdp_search_layouts(C.byref(d), int(ranks), C.byref(fr), int(overlap_h), int(overlap_w), flags,
+                                   None, 0, C.byref(n)), "tdp_search_layouts")
+    buf = (LayoutCandidate * max(1, n.value))()
+    _check(_lib.tdp_search_layouts(C.byref(d), int(ranks), C.byref(fr), int(overlap_h), int(overlap_w), flags,
+                                   buf, n.value, C.byref(n)), "tdp_search_layouts")
+    return [{"counts": tuple(c.num_tiles), "overlaps": tuple(c.overlap), "window_volume": c.window_volume,
+             "decoded_volume": c.decoded_volume, "heaviest_rank_volume": c.heaviest_rank_volume,
+             "seams": c.seams, "role": ROLES[c.role]} for c in buf[:n.value]]
 
 
 # ----------------------------------------------------------------- device calls

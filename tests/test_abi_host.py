@@ -143,3 +143,66 @@ def test_device_calls_reject_bad_arguments_before_launch(T):
     q.end[1][0] += 1
     assert lib.tdp_extract(C.byref(q), 1, 8, 0, C.c_void_p(good), C.c_void_p(good), None) == 1
     assert lib.tdp_plan_stats(C.byref(q), 1, None, None, None, None, None) == 1
+
+
+# ----------------------------------------------------------------- layout planner (host)
+def test_balanced_tile_split_matches_oracle(T):
+    for r in range(1, 300):
+        assert T.balanced_tile_split(r) == O.balanced_tile_split(r)
+    with pytest.raises(T.TdpError):
+        T.balanced_tile_split(0)
+
+
+@pytest.mark.parametrize("dims,ranks,frames,oh,ow,compat,limits", [
+    ((1, 32, 32), 2, (1, 0), 4, 4, False, True),
+    ((1, 32, 32), 3, (1, 0), 4, 4, False, True),
+    ((16, 68, 120), 1, (2, 2), 8, 12, False, True),
+    ((16, 68, 120), 2, (2, 2), 8, 12, False, True),
+    ((16, 68, 120), 4, (2, 2), 8, 12, False, True),
+    ((16, 68, 120), 8, (2, 2), 8, 12, False, True),
+    ((16, 68, 120), 16, (2, 2), 8, 12, False, True),
+    ((16, 68, 120), 8, (1, 0), 5, 5, False, False),
+    ((1, 128, 128), 4, (1, 0), 8, 8, False, True),
+    ((1, 128, 128), 8, (1, 0), 8, 8, False, False),
+    ((16, 16, 24), 4, (1, 0), 4, 6, False, False),
+    ((16, 32, 48), 2, (1, 0), 8, 12, False, False),
+    ((1, 21, 21), 4, (1, 0), 8, 8, True, False),
+    ((1, 15, 64), 2, (1, 0), 4, 4, False, True),      # narrow axis below 16: no candidate
+])
+def test_search_layouts_matches_oracle(T, dims, ranks, frames, oh, ow, compat, limits):
+    got = T.search_layouts(dims, ranks, frames, oh, ow, compat=compat, limits=limits)
+    want = O.search_layouts(dims, ranks, frames, oh, ow, compat=compat, limits=limits)
+    assert [(c["counts"], c["overlaps"], c["window_volume"], c["decoded_volume"], c["heaviest_rank_volume"],
+             c["seams"], c["role"]) for c in got] == \
+        [(c.counts, c.overlaps, c.window_volume, c.decoded_volume, c.heaviest_rank_volume, c.seams, c.role)
+         for c in want]
+
+
+def test_search_layouts_random_shapes_match_oracle(T):
+    rng = np.random.default_rng(21)
+    for _ in range(60):
+        dims = (int(rng.integers(1, 5)), int(rng.integers(8, 90)), int(rng.integers(8, 130)))
+        ranks = int(rng.integers(1, 13))
+        frames = (1, 0) if dims[0] < 4 or rng.random() < 0.5 else (2, 1)
+        oh, ow = int(rng.integers(0, 12)), int(rng.integers(0, 12))
+        limits = bool(rng.random() < 0.5)
+        got = T.search_layouts(dims, ranks, frames, oh, ow, limits=limits)
+        want = O.search_layouts(dims, ranks, frames, oh, ow, limits=limits)
+        assert [(c["counts"], c["heaviest_rank_volume"], c["role"]) for c in got] == \
+            [(c.counts, c.heaviest_rank_volume, c.role) for c in want], (dims, ranks, frames, oh, ow, limits)
+
+
+def test_search_layouts_capacity_and_errors(T):
+    import ctypes as C_
+    d = (C_.c_int32 * 3)(1, 32, 32)
+    fr = T.DimCfg(1, 0)
+    n = C_.c_int32()
+    lib = T._lib
+    assert lib.tdp_search_layouts(C_.byref(d), 3, C_.byref(fr), 4, 4, 0, None, 0, C_.byref(n)) == 0
+    assert n.value == 13
+    buf = (T.LayoutCandidate * 4)()
+    assert lib.tdp_search_layouts(C_.byref(d), 3, C_.byref(fr), 4, 4, 0, buf, 4, C_.byref(n)) == 0
+    assert n.value == 13 and tuple(buf[3].num_tiles) == (1, 1, 6)
+    assert lib.tdp_search_layouts(C_.byref(d), 0, C_.byref(fr), 4, 4, 0, None, 0, C_.byref(n)) == 1
+    assert lib.tdp_search_layouts(C_.byref(d), 3, C_.byref(fr), 4, 4, 8, None, 0, C_.byref(n)) == 1
+    assert lib.tdp_search_layouts(C_.byref(d), 3, C_.byref(fr), 4, 4, 0, None, 2, C_.byref(n)) == 1
