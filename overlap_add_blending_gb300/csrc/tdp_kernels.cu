@@ -270,6 +270,38 @@ __device__ __forceinline__ void cta_item_range(int n_items, int& first, int& las
     last = first + q + (b < r ? 1 : 0);
 }
 
+// Items of one (frame, band) group cost alike, but groups do not: a frame
+// covered by two frame tiles stages and blends twice the tile rows.  The
+// host tabulates, per group, the elements one item moves (the band's latent
+// rows, plus the tile rows of every covering (frame tile, row tile, column
+// tile)), and a CTA then takes the contiguous item range holding its equal
+// share of the total.  groups == 0: equal item counts (cta_item_range).
+constexpr int kCostGroups = 64;
+
+struct ItemCosts {
+    int groups;
+    long long cum[kCostGroups + 1];   // B*C times the cost of one item of every group before g
+};
+
+// First item of CTA b's share: the first item whose cost-so-far reaches
+// b / G of the total.
+__device__ __forceinline__ int cost_share_start(const ItemCosts& ic, int BC, int n_items, int G, int b) {
+    if (b >= G) return n_items;
+    const long long target = (long long)b * ic.cum[ic.groups] / G;
+    int g = 0;
+    while (g + 1 < ic.groups && ic.cum[g + 1] <= target) ++g;
+    const long long per = (ic.cum[g + 1] - ic.cum[g]) / BC;
+    const long long j = (target - ic.cum[g] + per - 1) / per;
+    return g * BC + static_cast<int>(j < BC ? j : BC);
+}
+
+__device__ __forceinline__ void cta_cost_range(const ItemCosts& ic, int BC, int n_items, int& first, int& last) {
+    if (ic.groups == 0) return cta_item_range(n_items, first, last);
+    const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    first = cost_share_start(ic, BC, n_items, G, b);
+    last = cost_share_start(ic, BC, n_items, G, b + 1);
+}
+
 struct FrameBand {
     int f, hb0, hb1;
 };
@@ -542,6 +574,7 @@ struct BlendArgs {
     // are at most kMaxOrdered units; otherwise the identity order
     int ordered;
     uint16_t order[kMaxOrdered];
+    ItemCosts costs;   // fast kernel: the item split
 };
 
 __host__ __device__ inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
@@ -916,7 +949,7 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
     static_assert(kBlendQueue <= 4 && kConsumerWarps <= 8, "shared header: 12 ints of run count and row-group bounds, 4 ring offsets");
 
     int first, last;
-    cta_item_range(a.n_items, first, last);
+    cta_cost_range(a.costs, a.BC, a.n_items, first, last);
     if (first >= last) return;
     const int n = last - first;
     if (threadIdx.x == 0) {
@@ -2024,6 +2057,30 @@ int max_terms(const tdp_plan_t& p, int U) {
     return best;
 }
 
+// The per-group item costs of the fast blend's split (see ItemCosts); an
+// equal split when there are more groups than the table holds.
+ItemCosts item_costs(const tdp_plan_t& p, int band_rows, int nbands, int BC) {
+    ItemCosts ic;
+    std::memset(&ic, 0, sizeof(ic));
+    const int ng = p.dims[0] * nbands;
+    if (ng > kCostGroups) return ic;
+    const long long SW = p.prefix[2][p.num_tiles[2]], W = p.dims[2];
+    for (int g = 0; g < ng; ++g) {
+        const int f = g / nbands, hb0 = (g % nbands) * band_rows, hb1 = std::min(p.dims[1], hb0 + band_rows);
+        int lo, hi;
+        tdp::axis_cover(p, 0, f, lo, hi);
+        long long rows = 0;   // band rows times the row tiles covering each
+        for (int i = 0; i < p.num_tiles[1]; ++i)
+            rows += std::max(0, std::min(hb1, p.end[1][i]) - std::max(hb0, p.start[1][i]));
+        ic.cum[g + 1] = ic.cum[g] + ((long long)(hb1 - hb0) * W + (long long)(hi - lo + 1) * rows * SW) * BC;
+    }
+    if (ic.cum[ng] >= (1LL << 46)) return ItemCosts{};   // keeps (CTA index) * total inside 64 bits
+    ic.groups = ng;
+    return ic;
+}
+
+static_assert(sizeof(tdp_plan_t) + sizeof(BlendArgs) <= 4096, "blend kernel parameters stay within 4 KB");
+
 template <typename Tin, typename Tout>
 tdp_status launch_blend(const tdp_plan_t& p, int BC, const void* tiles, long long tiles_numel, void* out,
                         cudaStream_t stream) {
@@ -2060,6 +2117,7 @@ tdp_status launch_blend(const tdp_plan_t& p, int BC, const void* tiles, long lon
     a.kf = p.max_cover[0];
     a.kh = p.max_cover[1];
     a.kw = p.max_cover[2];
+    a.costs = item_costs(p, band_rows, nbands, BC);
     const bool pairs = p.dims[2] % 2 == 0;
     {
         // column units ordered by the number of column tiles they touch
