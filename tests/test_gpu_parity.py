@@ -139,6 +139,17 @@ def test_guard_violating_splits_brighten(T, n):
     assert abs(Y.max().item() - printed) <= 6e-4
 
 
+def test_blend_cost_split_leaves_a_cta_without_items(T):
+    # 3 items (B*C = 1, 3 frames, the middle one in both frame tiles) on 3
+    # CTAs: the cost split gives the middle CTA an empty range
+    run_path(T, (3, 16, 16), ((2, 1), (2, 4), (2, 4)), 1, 1, torch.float32)
+
+
+def test_blend_many_frame_groups_use_the_count_split(T):
+    # 70 frames: more (frame, band) groups than the blend's cost table holds
+    run_path(T, (70, 12, 16), ((4, 3), (2, 2), (2, 4)), 1, 2, torch.bfloat16)
+
+
 def test_compat_3d_triple_cover(T):
     run_path(T, (6, 21, 21), ((3, 2), (4, 8), (3, 8)), 1, 3, torch.float32, compat=True)
 
