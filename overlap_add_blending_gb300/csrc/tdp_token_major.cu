@@ -52,6 +52,7 @@ struct TmArgs {
     int J;                // 16-byte chunks per token in the token-major buffer
     int jf;               // blend: fp32 chunks (4 channels) per column in shared memory
     int pmask, pfmask;    // swizzle masks: min(largest power of two <= chunks, 8) - 1
+    int ipt, lpt;         // blend: chunks of one token per thread (4, 2 or 1) and threads per token
     int xb, nxb;          // columns per unit, column blocks per latent row
     int units;            // B * F * H * nxb
 };
@@ -64,6 +65,14 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // the low bits are XOR-ed with the column's, so that 8 neighbouring columns
 // hit 8 different bank groups; a trailing partial group keeps its order.
 __device__ __forceinline__ int swz(int j, int x, int mask, int n) { return (j | mask) < n ? (j ^ (x & mask)) : j; }
+
+// The blend's fp32 rows: the same, with the column's low three bits
+// permuted (bit 0 to the top) when 8 chunks are swizzled, so that two
+// neighbouring columns also fall in opposite halves of the 8 groups.
+__device__ __forceinline__ int swzf(int j, int x, int mask, int n) {
+    const int f = mask == 7 ? (((x & 1) << 2) | ((x >> 1) & 3)) : (x & mask);
+    return (j | mask) < n ? (j ^ f) : j;
+}
 
 // Units are numbered in mixed radix (batch, frame, row, column block); a CTA
 // walks its units with a constant stride, digit by digit.
@@ -281,35 +290,33 @@ template <> struct Elems<float> {
 __device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
-// Pass 1: every thread owns kTmItems (column, 16-byte chunk) items and
-// accumulates, in fp32 registers, the weighted tokens of every tile covering
-// the column -- all of one (frame tile, row tile) pair's loads are issued
-// before any is used.  The sums go to shared memory as fp32 [column][C];
-// pass 2 writes the C latent row segments, a warp storing 32 neighbouring
-// columns of one channel.  With bf16 tokens an item holds two fp32 chunks;
-// chunk c of item j is kept at c * J + j, so that the 8 items of a column
-// that a quarter-warp stores land in 8 different bank groups.
+// Pass 1: every thread owns ipt 16-byte chunks of one column's token (its
+// chunks lit, lit + lpt, ...; lpt threads share a token, so a warp reads
+// contiguous 16*lpt-byte pieces of 32/lpt tokens per load) and accumulates,
+// in fp32 registers, the weighted tokens of every tile covering the column:
+// one address per covering column tile, and all of one (frame tile, row
+// tile) pair's loads issued before any is used.  The sums go to shared
+// memory as fp32 [column][C]; pass 2 writes the C latent row segments, a
+// warp storing 32 neighbouring columns of one channel.  With bf16 tokens a
+// chunk j holds two fp32 chunks, kept at j and J + j.
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(kTmThreads, 2) blend_tokens_kernel(const __grid_constant__ tdp_plan_t p,
                                                                      const TmArgs a) {
     constexpr int VEC = Elems<Tin>::kVec;
-    constexpr int FCH = VEC / 4;          // fp32 chunks per item
+    constexpr int FCH = VEC / 4;          // fp32 chunks per 16-byte chunk
     __shared__ float4 sacc[2 * kTmChunks];
     const uint4* __restrict__ src = static_cast<const uint4*>(a.src);
     Tout* __restrict__ out = static_cast<Tout*>(a.dst);
     const int tid = threadIdx.x;
-    const int J = a.J;
+    const int J = a.J, lpt = a.lpt, ipt = a.ipt;
+    const int xcol = tid / lpt, lit = tid - xcol * lpt;   // the thread's column in a unit, its first chunk
 
-    // Per item: its column, its chunk, the first column tile covering the
-    // column, how many do, and the first kTmKw of their column weights.
-    int ix[kTmItems], ij[kTmItems], wlo[kTmItems], ncov[kTmItems];
-    float ww[kTmItems][kTmKw];
+    // the column's first covering column tile, how many cover it, and the
+    // first kTmKw of their column weights
+    int wlo = 0, ncov = 0;
+    float ww[kTmKw];
 #pragma unroll
-    for (int r = 0; r < kTmItems; ++r) {
-        const int i = tid + r * kTmThreads;
-        ix[r] = i / J;
-        ij[r] = i % J;
-    }
+    for (int q = 0; q < kTmKw; ++q) ww[q] = 0.0f;
     int cached_x0 = -1;
     // pass 2: columns per pass, the thread's first column and channel group, and the group step
     int c_xbu = -1, xt = 1, x2 = 0, q2 = 0, sq2 = 1;
@@ -319,21 +326,19 @@ __global__ void __launch_bounds__(kTmThreads, 2) blend_tokens_kernel(const __gri
     UnitWalk walk = unit_walk(p, a, min(u, a.units - 1), gridDim.x);
     for (; u < a.units; u += gridDim.x, unit_next(p, a, walk)) {
         const Unit U = unit_of(p, a, walk);
+        const bool mine = xcol < U.xbu;
         if (U.x0 != cached_x0) {
             cached_x0 = U.x0;
+            ncov = 0;
+            wlo = 0;
+            if (mine) {
+                const int w = U.x0 + xcol;
+                int lo, hi;
+                tdp::axis_cover(p, 2, w, lo, hi);
+                wlo = lo;
+                ncov = hi - lo + 1;
 #pragma unroll
-            for (int r = 0; r < kTmItems; ++r) {
-                ncov[r] = 0;
-                wlo[r] = 0;
-                if (ix[r] < U.xbu) {
-                    const int w = U.x0 + ix[r];
-                    int lo, hi;
-                    tdp::axis_cover(p, 2, w, lo, hi);
-                    wlo[r] = lo;
-                    ncov[r] = hi - lo + 1;
-#pragma unroll
-                    for (int q = 0; q < kTmKw; ++q) ww[r][q] = axis_weight(p, 2, min(lo + q, hi), w);
-                }
+                for (int q = 0; q < kTmKw; ++q) ww[q] = axis_weight(p, 2, min(lo + q, hi), w);
             }
         }
 
@@ -346,49 +351,53 @@ __global__ void __launch_bounds__(kTmThreads, 2) blend_tokens_kernel(const __gri
         int flo, fhi, hlo, hhi;
         tdp::axis_cover(p, 0, U.f, flo, fhi);
         tdp::axis_cover(p, 1, U.h, hlo, hhi);
+        const int w = U.x0 + xcol;
         for (int i_f = flo; i_f <= fhi; ++i_f) {
             const float wf = axis_weight(p, 0, i_f, U.f);
             const int k = U.f - p.start[0][i_f];
             for (int i_h = hlo; i_h <= hhi; ++i_h) {
                 const float wfh = __fmul_rn(wf, axis_weight(p, 1, i_h, U.h));
                 const TileRow tr_ = tile_row(p, a.B, U.b, i_f, i_h, k, U.h - p.start[1][i_h]);
-                uint4 v[kTmItems][kTmKw];
+                uint4 v[kTmKw][kTmItems];
 #pragma unroll
-                for (int r = 0; r < kTmItems; ++r)
+                for (int q = 0; q < kTmKw; ++q)
+                    if (q < ncov) {
+                        const int i_w = wlo + q;
+                        const uint4* s = src + (row_token(p, tr_, i_w) + (w - p.start[2][i_w])) * J + lit;
 #pragma unroll
-                    for (int q = 0; q < kTmKw; ++q)
-                        if (q < ncov[r]) {
-                            const int i_w = wlo[r] + q;
-                            const long long tok = row_token(p, tr_, i_w) + (U.x0 + ix[r] - p.start[2][i_w]);
-                            v[r][q] = __ldg(src + tok * J + ij[r]);
-                        }
-#pragma unroll
-                for (int r = 0; r < kTmItems; ++r)
-#pragma unroll
-                    for (int q = 0; q < kTmKw; ++q)
-                        if (q < ncov[r]) Elems<Tin>::fma_into(acc[r], v[r][q], __fmul_rn(wfh, ww[r][q]));
-                // Columns covered by more than kTmKw column tiles (only when
-                // the partition-of-unity guard is off): one term at a time.
-#pragma unroll
-                for (int r = 0; r < kTmItems; ++r) {
-                    if (ncov[r] <= kTmKw) continue;
-                    const int w = U.x0 + ix[r];
-                    for (int i_w = wlo[r] + kTmKw; i_w < wlo[r] + ncov[r]; ++i_w) {
-                        const long long tok = row_token(p, tr_, i_w) + (w - p.start[2][i_w]);
-                        Elems<Tin>::fma_into(acc[r], __ldg(src + tok * J + ij[r]),
-                                             __fmul_rn(wfh, axis_weight(p, 2, i_w, w)));
+                        for (int r = 0; r < kTmItems; ++r)
+                            if (r < ipt) v[q][r] = __ldg(s + r * lpt);
                     }
+#pragma unroll
+                for (int q = 0; q < kTmKw; ++q)
+                    if (q < ncov) {
+                        const float wq = __fmul_rn(wfh, ww[q]);
+#pragma unroll
+                        for (int r = 0; r < kTmItems; ++r)
+                            if (r < ipt) Elems<Tin>::fma_into(acc[r], v[q][r], wq);
+                    }
+                // Columns covered by more than kTmKw column tiles (only when
+                // the partition-of-unity guard is off): one tile at a time.
+                for (int i_w = wlo + kTmKw; i_w < wlo + ncov; ++i_w) {
+                    const uint4* s = src + (row_token(p, tr_, i_w) + (w - p.start[2][i_w])) * J + lit;
+                    const float wq = __fmul_rn(wfh, axis_weight(p, 2, i_w, w));
+#pragma unroll
+                    for (int r = 0; r < kTmItems; ++r)
+                        if (r < ipt) Elems<Tin>::fma_into(acc[r], __ldg(s + r * lpt), wq);
                 }
             }
         }
 
+        if (mine) {
 #pragma unroll
-        for (int r = 0; r < kTmItems; ++r) {
-            if (ix[r] >= U.xbu) continue;
+            for (int r = 0; r < kTmItems; ++r) {
+                if (r >= ipt) break;
+                const int j = lit + r * lpt;
 #pragma unroll
-            for (int c = 0; c < FCH; ++c)
-                sacc[ix[r] * a.jf + swz(c * J + ij[r], ix[r], a.pfmask, a.jf)] =
-                    make_float4(acc[r][4 * c], acc[r][4 * c + 1], acc[r][4 * c + 2], acc[r][4 * c + 3]);
+                for (int c = 0; c < FCH; ++c)
+                    sacc[xcol * a.jf + swzf(c * J + j, xcol, a.pfmask, a.jf)] =
+                        make_float4(acc[r][4 * c], acc[r][4 * c + 1], acc[r][4 * c + 2], acc[r][4 * c + 3]);
+            }
         }
         __syncthreads();
 
@@ -405,9 +414,9 @@ __global__ void __launch_bounds__(kTmThreads, 2) blend_tokens_kernel(const __gri
             for (int x = x2; x < U.xbu; x += xt) {
                 Tout* o = orow + 4LL * q2 * a.fhw + x;
                 for (int qc = q2; qc < a.jf; qc += sq2, o += qstride) {
-                    // channels 4qc..4qc+3: item qc / FCH, its chunk qc % FCH
+                    // channels 4qc..4qc+3: chunk qc / FCH, its fp32 half qc % FCH
                     const int slot = FCH == 2 ? ((qc & 1) * J + (qc >> 1)) : qc;
-                    const float4 s = sacc[x * a.jf + swz(slot, x, a.pfmask, a.jf)];
+                    const float4 s = sacc[x * a.jf + swzf(slot, x, a.pfmask, a.jf)];
                     store_out(o, s.x);
                     store_out(o + a.fhw, s.y);
                     store_out(o + 2 * a.fhw, s.z);
@@ -429,13 +438,17 @@ int swizzle_mask(int chunks) {
     return m - 1;
 }
 
-// Shared unit geometry of both calls; `esz` is the token-major element size.
-tdp_status tm_args(const tdp_plan_t& p, int B, int C, int esz, TmArgs& a) {
+// Unit geometry of both calls; `esz` is the token-major element size.
+// Extract: kTmChunks chunks per unit.  Blend: one column per lpt threads.
+tdp_status tm_args(const tdp_plan_t& p, int B, int C, int esz, bool blend, TmArgs& a) {
     if ((static_cast<long long>(C) * esz) % 16 != 0) return TDP_ERR_UNSUPPORTED;
     const long long J = static_cast<long long>(C) * esz / 16;
     if (J > kTmChunks) return TDP_ERR_UNSUPPORTED;
+    a.ipt = J % 4 == 0 ? 4 : (J % 2 == 0 ? 2 : 1);
+    a.lpt = static_cast<int>(J / a.ipt);
+    if (blend && a.lpt > kTmThreads) return TDP_ERR_UNSUPPORTED;
     const int W = p.dims[2];
-    const int xb_max = static_cast<int>(kTmChunks / J);
+    const int xb_max = blend ? kTmThreads / a.lpt : static_cast<int>(kTmChunks / J);
     const int nxb = (W + xb_max - 1) / xb_max;
     const int xb = (W + nxb - 1) / nxb;   // balanced column blocks
     const long long units = static_cast<long long>(B) * p.dims[0] * p.dims[1] * nxb;
@@ -484,7 +497,7 @@ tdp_status tdp_extract_tokens(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_
     if (!latent || !tokens) return TDP_ERR_INVALID_ARG;
     if (!aligned16(latent) || !aligned16(tokens)) return TDP_ERR_ALIGNMENT;
     TmArgs a{};
-    tdp_status st = tm_args(*plan, B, C, esz, a);
+    tdp_status st = tm_args(*plan, B, C, esz, false, a);
     if (st != TDP_OK) return st;
     a.src = latent;
     a.dst = tokens;
@@ -501,7 +514,7 @@ tdp_status tdp_blend_tokens(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dt
     if (!tokens || !out) return TDP_ERR_INVALID_ARG;
     if (!aligned16(tokens) || !aligned16(out)) return TDP_ERR_ALIGNMENT;
     TmArgs a{};
-    tdp_status st = tm_args(*plan, B, C, esz, a);
+    tdp_status st = tm_args(*plan, B, C, esz, true, a);
     if (st != TDP_OK) return st;
     a.src = tokens;
     a.dst = out;
