@@ -38,7 +38,7 @@ int device_sm_count();
 namespace {
 
 constexpr int kTmThreads = 256;
-constexpr int kTmItems = 4;                            // 16-byte chunks per thread per unit
+constexpr int kTmItems = 4;                            // 16-byte chunks per thread per unit (at most, in the blend)
 constexpr int kTmChunks = kTmThreads * kTmItems;       // chunks of one unit's token side
 constexpr int kTmKw = 2;                               // column tiles per column kept in registers
 
@@ -130,7 +130,7 @@ __device__ __forceinline__ long long latent_row(const tdp_plan_t& p, const TmArg
 // Token index, in the packed buffer, of row (k, y) of the tiles of frame
 // tile i_f and row tile i_h for batch b, as A + Bm * P_w + Cm * w_t with P_w
 // and w_t the column tile's width prefix and width:
-//   B * (volume of the tiles before it) + (b * f_t + k) * h_t + y) * w_t.
+//   B * (volume of the tiles before it) + ((b * f_t + k) * h_t + y) * w_t.
 struct TileRow {
     long long A, Bm, Cm;
 };
