@@ -274,18 +274,18 @@ def run_tdp(args, rank: int, world: int):
     # tiles: they run on a side stream beside extract (they feed the per-tile
     # model, not the blend's inputs), and the main stream waits for them
     # before the blend.
-    def side_work():
+    def side_work(g=gen, c=cond, m=maxdev):
         fork.record(stream)
         side.wait_event(fork)
-        tdp.tokens(p, gen, cond, True, True, tok_out, stream=side)
-        tdp.window_sum(p, maxdev, stream=side)
+        tdp.tokens(p, g, c, True, True, tok_out, stream=side)
+        tdp.window_sum(p, m, stream=side)
         join.record(side)
 
-    def path():
-        side_work()
-        tdp.extract(p, X, tiles)
+    def path(x=X, g=gen, c=cond, o=out, m=maxdev):
+        side_work(g, c, m)
+        tdp.extract(p, x, tiles)
         stream.wait_event(join)
-        tdp.blend(p, tiles, wl.B, wl.C, out)
+        tdp.blend(p, tiles, wl.B, wl.C, o)
 
     # One step: extract with the token and window kernels beside it on the
     # side stream, then the blend.  Events on the main stream: ev0 start,
@@ -393,30 +393,66 @@ def run_tdp(args, rank: int, world: int):
     search_us = (time.perf_counter() - t0) / 20 * 1e6
     picks = {c["role"]: list(c["counts"]) for c in cands if c["role"] in ("coarse", "fine", "balanced")}
 
-    # e2e: host buffers in, blended latent out, through the same C-ABI calls
+    # e2e: host buffers in, blended latent out, through the same C-ABI calls.
+    # Steps are pipelined over two device buffer sets: step k's inputs go up
+    # on one copy stream while step k-1 computes, and step k-1's result comes
+    # down on another while step k computes.  Timed from the first upload to
+    # the last download, over K steps.
     X_h = X.cpu().pin_memory()
     gen_h = gen.cpu().pin_memory()
     cond_h = cond.cpu().pin_memory()
-    out_h = torch.empty(out.shape, dtype=dt, pin_memory=True)
-    dev_h = torch.empty(1, dtype=torch.float32, pin_memory=True)
+    out_h = [torch.empty(out.shape, dtype=dt, pin_memory=True) for _ in range(2)]
+    dev_h = [torch.empty(1, dtype=torch.float32, pin_memory=True) for _ in range(2)]
     h2d = X_h.numel() * X_h.element_size() + gen_h.numel() * 4 + cond_h.numel() * 4
-    d2h = out_h.numel() * out_h.element_size() + 4
-    e2e_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    for k in range(-min(3, args.warmup), K):
-        flush.zero_()
-        torch.cuda._sleep(sleep_cycles)
-        if k >= 0:
-            e2e_evs[k][0].record(stream)
-        X.copy_(X_h, non_blocking=True)
-        gen.copy_(gen_h, non_blocking=True)
-        cond.copy_(cond_h, non_blocking=True)
-        path()
-        out_h.copy_(out, non_blocking=True)
-        dev_h.copy_(maxdev[:1], non_blocking=True)
-        if k >= 0:
-            e2e_evs[k][1].record(stream)
+    d2h = out_h[0].numel() * out_h[0].element_size() + 4
+    ref_out = out.cpu()
+    bufs = [(X, gen, cond, out, maxdev),
+            (torch.empty_like(X), torch.empty_like(gen), torch.empty_like(cond), torch.empty_like(out),
+             torch.empty_like(maxdev))]
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    in_ready, in_free, out_ready, out_free = ([torch.cuda.Event() for _ in range(2)] for _ in range(4))
+    for i in range(2):
+        in_free[i].record(stream)
+        out_free[i].record(stream)
+
+    def e2e_step(k):
+        i = k % 2
+        x, g, c, o, m = bufs[i]
+        up.wait_event(in_free[i])
+        with torch.cuda.stream(up):
+            x.copy_(X_h, non_blocking=True)
+            g.copy_(gen_h, non_blocking=True)
+            c.copy_(cond_h, non_blocking=True)
+        in_ready[i].record(up)
+        stream.wait_event(in_ready[i])
+        stream.wait_event(out_free[i])
+        path(x, g, c, o, m)
+        in_free[i].record(stream)
+        out_ready[i].record(stream)
+        down.wait_event(out_ready[i])
+        with torch.cuda.stream(down):
+            out_h[i].copy_(o, non_blocking=True)
+            dev_h[i].copy_(m[:1], non_blocking=True)
+        out_free[i].record(down)
+
+    for k in range(min(3, args.warmup)):
+        e2e_step(k)
     torch.cuda.synchronize()
-    e2e_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in e2e_evs]))
+    t_first, t_last = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    up.wait_stream(stream)
+    with torch.cuda.stream(up):
+        torch.cuda._sleep(sleep_cycles)   # the host enqueues ahead meanwhile
+    t_first.record(up)
+    for k in range(K):
+        e2e_step(k)
+    down.wait_stream(stream)
+    t_last.record(down)
+    torch.cuda.synchronize()
+    for i in range(2):
+        if not torch.equal(out_h[i], ref_out):
+            raise SystemExit("e2e: a downloaded result differs from the device-resident step's")
+    e2e_ms = t_first.elapsed_time(t_last) / K
+
 
     # replicas: slowest rank's times, every rank's work
     mx, job_bytes = combine([step_ms, e2e_ms] + [float(v) for v in per_kernel_ms], ab["total"], device=dev)
@@ -446,7 +482,9 @@ def run_tdp(args, rank: int, world: int):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src},
         "e2e": {"value": job_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+                "pipelined": "two buffer sets; uploads, steps and downloads on three streams; "
+                             "first upload to last download over K steps"},
         "gpu_launches": KERNELS_PER_STEP * K,
         "next_rows": {"cond_combine": {"ms": comb_ms, "workload": f"T={p.T} tiles, B={wl.B}, M={wl.num_cond} "
                                        f"conditioning tokens, D={wl.C} bf16 features; median of 20, not in the step"},
