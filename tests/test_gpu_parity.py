@@ -98,6 +98,13 @@ def test_4k_identity_roundtrip_is_near_exact(T):
     assert (Y - X.float()).abs().max().item() <= 2e-6 * X.float().abs().max().item() + 1e-7
 
 
+def test_4k_two_batches(T):
+    # the 4k tiling with B = 2, C = 64: batch offsets in every kernel and
+    # 128 items per (frame, band) group split by cost across the blend's CTAs
+    wl = WORKLOADS["4k"]
+    run_path(T, wl.dims, wl.tiling, 2, 64, torch.bfloat16, seed=5)
+
+
 # ----------------------------------------------------------------- edge cases
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_ragged_odd_shapes(T, dtype):

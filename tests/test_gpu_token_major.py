@@ -86,6 +86,11 @@ def test_token_major_4k_fp32_output(T):
     run_tokens(T, wl.dims, wl.tiling, wl.B, wl.C, torch.bfloat16, out_dtype=torch.float32)
 
 
+def test_token_major_4k_two_batches(T):
+    wl = WORKLOADS["4k"]
+    run_tokens(T, wl.dims, wl.tiling, 2, 64, torch.bfloat16, seed=5)
+
+
 def test_tokens_are_channel_first_tiles_transposed(T):
     """The two extract layouts hold the same values, tile by tile."""
     wl = WORKLOADS["fullres"]
