@@ -357,6 +357,7 @@ def run_tdp(args, rank: int, world: int):
     for _ in range(3):
         tdp.cond_combine(p, comb_in, tok_out["slot_of"], tok_out["weight"], out=comb_out)
     cev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(20)]
+    torch.cuda._sleep(20 * sleep_cycles)   # the host enqueues all 20 launches meanwhile
     for e in cev:
         e[0].record(stream)
         tdp.cond_combine(p, comb_in, tok_out["slot_of"], tok_out["weight"], out=comb_out)

@@ -1524,6 +1524,7 @@ struct TokensArgs {
 
 constexpr int kPosCache = 4;   // tokens per thread kept in registers between reduce and write
 constexpr int kCombineCols = 4;   // feature columns per lane per pass of the conditioning combine
+constexpr int kCombineRound = 8;  // kept tiles of one token whose loads the combine issues together
 constexpr int kCondOneCta = 2048;   // at most this many conditioning tokens: one CTA per tile tests them all
 
 __device__ __forceinline__ bool cond_keep(const int* cond, int b, int M, int m, const int ext[6]) {
@@ -1823,6 +1824,32 @@ __global__ void __launch_bounds__(kThreads) cond_count_kernel(const unsigned cha
 // of a conditioning token's per-tile outputs, fp32 accumulation, one store.
 // One warp per (b, m); its lanes look up the tiles' slots 32 at a time and
 // then walk the feature dimension.
+
+// 4 contiguous features as fp32 (a 4-feature row start is 8- or 16-byte aligned).
+__device__ __forceinline__ void load_feat4(const __nv_bfloat16* q, float (&v)[4]) {
+    const uint2 u = *reinterpret_cast<const uint2*>(q);
+    v[0] = __uint_as_float(u.x << 16);
+    v[1] = __uint_as_float(u.x & 0xffff0000u);
+    v[2] = __uint_as_float(u.y << 16);
+    v[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+__device__ __forceinline__ void load_feat4(const float* q, float (&v)[4]) {
+    const float4 u = *reinterpret_cast<const float4*>(q);
+    v[0] = u.x;
+    v[1] = u.y;
+    v[2] = u.z;
+    v[3] = u.w;
+}
+__device__ __forceinline__ void store_feat4(__nv_bfloat16* q, const float (&v)[4]) {
+    uint2 u;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(u.x) : "f"(v[1]), "f"(v[0]));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(u.y) : "f"(v[3]), "f"(v[2]));
+    *reinterpret_cast<uint2*>(q) = u;
+}
+__device__ __forceinline__ void store_feat4(float* q, const float (&v)[4]) {
+    *reinterpret_cast<float4*>(q) = make_float4(v[0], v[1], v[2], v[3]);
+}
+
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(kThreads) cond_combine_kernel(int T, int BM, int M, int D, const Tin* tile_out,
                                                                 const int* slot_of, const float* weight, Tout* out) {
@@ -1832,44 +1859,61 @@ __global__ void __launch_bounds__(kThreads) cond_combine_kernel(int T, int BM, i
     const int bm = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (bm >= BM) return;
     const float w = weight[bm];
+    // With D a multiple of 4 a lane takes 4 contiguous features, one load
+    // per tile; otherwise features lane, lane + 32, ... one at a time.
+    const bool vec = D % kCombineCols == 0;
     for (int d0 = 0; d0 < D; d0 += 32 * kCombineCols) {
         float acc[kCombineCols];
 #pragma unroll
         for (int i = 0; i < kCombineCols; ++i) acc[i] = 0.0f;
+        const int dv = d0 + lane * kCombineCols;
         for (int t0 = 0; t0 < T; t0 += 32) {
             const int t = t0 + lane;
             const int slot = t < T ? slot_of[(long long)t * BM + bm] : -1;
             unsigned kept = __ballot_sync(0xffffffffu, slot >= 0);
             while (kept) {
-                // up to four kept tiles per round, lowest first: their loads
-                // are issued together, then added in increasing tile order
-                float v[4][kCombineCols];
-                bool has[4];   // warp-uniform: `kept` is a ballot
+                // up to kCombineRound kept tiles per round, lowest first: their
+                // loads are issued together, then added in increasing tile order
+                float v[kCombineRound][kCombineCols];
+                bool has[kCombineRound];   // warp-uniform: `kept` is a ballot
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < kCombineRound; ++j) {
                     has[j] = kept != 0;
                     const int src = has[j] ? __ffs(kept) - 1 : 0;
                     kept &= kept - 1;
                     const int st = __shfl_sync(0xffffffffu, slot, src);
                     const long long row = ((long long)(t0 + src) * BM + (bm - bm % M) + st) * D;   // (t, b, st)
+                    if (vec) {
+                        if (has[j] && dv < D) {
+                            load_feat4(tile_out + row + dv, v[j]);
+                        } else {
 #pragma unroll
-                    for (int i = 0; i < kCombineCols; ++i) {
-                        const int d = d0 + i * 32 + lane;
-                        v[j][i] = (has[j] && d < D) ? to_f32(tile_out[row + d]) : 0.0f;
+                            for (int i = 0; i < kCombineCols; ++i) v[j][i] = 0.0f;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kCombineCols; ++i) {
+                            const int d = d0 + i * 32 + lane;
+                            v[j][i] = (has[j] && d < D) ? to_f32(tile_out[row + d]) : 0.0f;
+                        }
                     }
                 }
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
+                for (int j = 0; j < kCombineRound; ++j)
                     if (has[j]) {
 #pragma unroll
                         for (int i = 0; i < kCombineCols; ++i) acc[i] = fmaf(w, v[j][i], acc[i]);
                     }
             }
         }
+        if (vec) {
+            if (dv < D) store_feat4(out + (long long)bm * D + dv, acc);
+        } else {
 #pragma unroll
-        for (int i = 0; i < kCombineCols; ++i) {
-            const int d = d0 + i * 32 + lane;
-            if (d < D) out[(long long)bm * D + d] = from_f32<Tout>(acc[i]);
+            for (int i = 0; i < kCombineCols; ++i) {
+                const int d = d0 + i * 32 + lane;
+                if (d < D) out[(long long)bm * D + d] = from_f32<Tout>(acc[i]);
+            }
         }
     }
 }
