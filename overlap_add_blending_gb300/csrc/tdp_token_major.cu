@@ -25,6 +25,7 @@
 #include <algorithm>
 #include <climits>
 #include <cstdint>
+#include <type_traits>
 
 #include "tdp.h"
 #include "tdp_geometry.h"
@@ -151,14 +152,42 @@ __device__ __forceinline__ long long row_token(const tdp_plan_t& p, const TileRo
 
 // ------------------------------------------------------------------ extract
 // Pass 1 reads the unit's C x xbu latent block column-wise (a warp reads 32
-// neighbouring columns of one channel row) and stores 16-byte channel chunks
-// per column; pass 2 writes each column's chunks to every tile token that
-// holds it (a warp writes whole tokens).  The next unit's latent block is
-// loaded into registers while the current one is written out.
-template <typename E>   // raw element: uint16_t (bf16) or uint32_t (fp32); a bit copy
+// neighbouring columns, or column pairs, of one channel row) and stores
+// 16-byte channel chunks per column; pass 2 writes each column's chunks to
+// every tile token that holds it (a warp writes whole tokens).  The next
+// unit's latent block is loaded into registers while the current one is
+// written out.
+//
+// PAIR (even W and column blocks): an item is two neighbouring columns,
+// loaded 4 bytes (bf16) or 8 bytes (fp32) at a time, and the shared rows
+// swizzle by the column pair, so that the 8 even (or odd) columns a
+// quarter-warp stores still fall in 8 bank groups.
+template <typename E> struct PairOf;
+template <> struct PairOf<uint16_t> { using type = uint32_t; };
+template <> struct PairOf<uint32_t> { using type = uint2; };
+
+__device__ __forceinline__ void split_pair(const uint32_t (&v)[8], uint4& c0, uint4& c1) {
+    c0 = make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410), __byte_perm(v[4], v[5], 0x5410),
+                    __byte_perm(v[6], v[7], 0x5410));
+    c1 = make_uint4(__byte_perm(v[0], v[1], 0x7632), __byte_perm(v[2], v[3], 0x7632), __byte_perm(v[4], v[5], 0x7632),
+                    __byte_perm(v[6], v[7], 0x7632));
+}
+__device__ __forceinline__ void split_pair(const uint2 (&v)[4], uint4& c0, uint4& c1) {
+    c0 = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
+    c1 = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
+}
+
+template <bool PAIR>
+__device__ __forceinline__ int swz_extract(int j, int x, int mask, int n) {
+    return swz(j, PAIR ? (x >> 1) : x, mask, n);
+}
+
+template <typename E, bool PAIR>   // raw element: uint16_t (bf16) or uint32_t (fp32); a bit copy
 __global__ void __launch_bounds__(kTmThreads, 3) extract_tokens_kernel(const __grid_constant__ tdp_plan_t p,
                                                                        const TmArgs a) {
     constexpr int VEC = 16 / sizeof(E);
+    constexpr int NI = PAIR ? kTmItems / 2 : kTmItems;   // items per thread
+    using L = typename std::conditional<PAIR, typename PairOf<E>::type, E>::type;
     __shared__ uint4 sbuf[kTmChunks];
     const E* __restrict__ src = static_cast<const E*>(a.src);
     uint4* __restrict__ dst = static_cast<uint4*>(a.dst);
@@ -168,34 +197,36 @@ __global__ void __launch_bounds__(kTmThreads, 3) extract_tokens_kernel(const __g
     const int tq = tid / J, tr = tid % J;
     const int sx2 = kTmThreads / J, sj2 = kTmThreads % J;
 
-    E v[kTmItems][VEC];
-    int ix[kTmItems], ij[kTmItems];
+    L v[NI][VEC];
+    int ix[NI], ij[NI];   // item: column (or column pair) and chunk
     // pass 1: a thread's first (column, chunk) of a block of xbu columns and its step
     int c_xbu = -1, x1 = 0, j1 = 0, sx1 = 0, sj1 = 0;
 
     auto load = [&](const Unit& U) {
+        const int ncol = PAIR ? U.xbu / 2 : U.xbu;   // items per chunk index
         if (U.xbu != c_xbu) {
             c_xbu = U.xbu;
-            x1 = tid % c_xbu;
-            j1 = tid / c_xbu;
-            sx1 = kTmThreads % c_xbu;
-            sj1 = kTmThreads / c_xbu;
+            x1 = tid % ncol;
+            j1 = tid / ncol;
+            sx1 = kTmThreads % ncol;
+            sj1 = kTmThreads / ncol;
         }
         const E* base = src + latent_row(p, a, U);
         int x = x1, j = j1;
 #pragma unroll
-        for (int r = 0; r < kTmItems; ++r) {
+        for (int r = 0; r < NI; ++r) {
             ix[r] = x;
             ij[r] = j < J ? j : -1;
             if (ij[r] >= 0) {
-                const E* s = base + (long long)j * VEC * a.fhw + x;
+                const L* s = reinterpret_cast<const L*>(base + (long long)j * VEC * a.fhw + (PAIR ? 2 * x : x));
+                const long long step = a.fhw / (PAIR ? 2 : 1);   // one channel row, in loads
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) v[r][e] = __ldg(s + e * a.fhw);
+                for (int e = 0; e < VEC; ++e) v[r][e] = __ldg(s + e * step);
             }
             x += sx1;
             j += sj1;
-            if (x >= U.xbu) {
-                x -= U.xbu;
+            if (x >= ncol) {
+                x -= ncol;
                 ++j;
             }
         }
@@ -209,18 +240,26 @@ __global__ void __launch_bounds__(kTmThreads, 3) extract_tokens_kernel(const __g
     load(U);
     while (true) {
 #pragma unroll
-        for (int r = 0; r < kTmItems; ++r) {
+        for (int r = 0; r < NI; ++r) {
             if (ij[r] < 0) continue;
-            uint4 w;
-            if constexpr (VEC == 8) {
-                w.x = (uint32_t)v[r][0] | ((uint32_t)v[r][1] << 16);
-                w.y = (uint32_t)v[r][2] | ((uint32_t)v[r][3] << 16);
-                w.z = (uint32_t)v[r][4] | ((uint32_t)v[r][5] << 16);
-                w.w = (uint32_t)v[r][6] | ((uint32_t)v[r][7] << 16);
+            if constexpr (PAIR) {
+                uint4 c0, c1;
+                split_pair(v[r], c0, c1);
+                const int x0c = 2 * ix[r];
+                sbuf[x0c * J + swz_extract<PAIR>(ij[r], x0c, a.pmask, J)] = c0;
+                sbuf[(x0c + 1) * J + swz_extract<PAIR>(ij[r], x0c + 1, a.pmask, J)] = c1;
             } else {
-                w = make_uint4(v[r][0], v[r][1], v[r][2], v[r][3]);
+                uint4 w;
+                if constexpr (VEC == 8) {
+                    w.x = (uint32_t)v[r][0] | ((uint32_t)v[r][1] << 16);
+                    w.y = (uint32_t)v[r][2] | ((uint32_t)v[r][3] << 16);
+                    w.z = (uint32_t)v[r][4] | ((uint32_t)v[r][5] << 16);
+                    w.w = (uint32_t)v[r][6] | ((uint32_t)v[r][7] << 16);
+                } else {
+                    w = make_uint4(v[r][0], v[r][1], v[r][2], v[r][3]);
+                }
+                sbuf[ix[r] * J + swz_extract<PAIR>(ij[r], ix[r], a.pmask, J)] = w;
             }
-            sbuf[ix[r] * J + swz(ij[r], ix[r], a.pmask, J)] = w;
         }
         __syncthreads();
         const Unit cur = U;
@@ -246,7 +285,7 @@ __global__ void __launch_bounds__(kTmThreads, 3) extract_tokens_kernel(const __g
                     int x = max(w0, cur.x0) + tq, j = tr;
                     while (x < sb) {
                         const int xl = x - cur.x0;
-                        dst[(row + x) * J + j] = sbuf[xl * J + swz(j, xl, a.pmask, J)];
+                        dst[(row + x) * J + j] = sbuf[xl * J + swz_extract<PAIR>(j, xl, a.pmask, J)];
                         x += sx2;
                         j += sj2;
                         if (j >= J) {
@@ -501,8 +540,13 @@ tdp_status tdp_extract_tokens(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_
     if (st != TDP_OK) return st;
     a.src = latent;
     a.dst = tokens;
-    return esz == 2 ? tm_launch(extract_tokens_kernel<uint16_t>, *plan, a, stream)
-                    : tm_launch(extract_tokens_kernel<uint32_t>, *plan, a, stream);
+    // column pairs: every row and every column block start on an even column
+    const bool pair = plan->dims[2] % 2 == 0 && a.xb % 2 == 0;
+    if (esz == 2)
+        return pair ? tm_launch(extract_tokens_kernel<uint16_t, true>, *plan, a, stream)
+                    : tm_launch(extract_tokens_kernel<uint16_t, false>, *plan, a, stream);
+    return pair ? tm_launch(extract_tokens_kernel<uint32_t, true>, *plan, a, stream)
+                : tm_launch(extract_tokens_kernel<uint32_t, false>, *plan, a, stream);
 }
 
 tdp_status tdp_blend_tokens(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_dtype, const void* tokens,
