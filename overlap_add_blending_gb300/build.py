@@ -5,7 +5,7 @@
 Three translation units (host planner, channel-first kernels, token-major
 kernels) compiled in parallel and
 linked into overlap_add_blending_gb300/libtdp.so.  The CUDA runtime is
-linked statically, so the library needs only the driver at run time.
+linked statically, so the library needs only the CUDA driver at run time.
 """
 from __future__ import annotations
 
