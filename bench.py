@@ -66,8 +66,8 @@ def config_dict(wl, note: str) -> dict:
                         f"W={wl.dims[2]}, tiles (frames {wl.tiling[0][0]}/{wl.tiling[0][1]}, height "
                         f"{wl.tiling[1][0]}/{wl.tiling[1][1]}, width {wl.tiling[2][0]}/{wl.tiling[2][1]}), "
                         f"{wl.num_cond} conditioning tokens ({wl.num_cond_negative} with negative time)",
-            "step": "extract, tokens (positions + cond select), window_sum, blend on one stream; "
-                    "per-tile op: identity, outside",
+            "step": "extract, with tokens (positions + cond select) and window_sum beside it on a side "
+                    "stream, then blend; per-tile op: identity, outside",
             "l2": note}
 
 
@@ -509,7 +509,7 @@ def run_tdp(args, rank: int, world: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)   # about 0.5 s timed: several clock samples
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["tdp", "reference"], default="tdp")
     ap.add_argument("--no-cpu-baseline", action="store_true")
