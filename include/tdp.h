@@ -361,7 +361,8 @@ tdp_status tdp_extract_tokens(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_
  * `out_dtype` (round to nearest even for bf16); every element of `out` is
  * written.  tokens: device, packed token-major, `in_dtype`.
  * out: device [B, C, F, H, W].  C * sizeof(in_dtype) must be a multiple of
- * 16 bytes and at most 16 KiB (else TDP_ERR_UNSUPPORTED).
+ * 16 bytes and at most 16 KiB -- 8 KiB when C * sizeof(in_dtype) / 16 is not
+ * a multiple of 4, 4 KiB when it is odd (else TDP_ERR_UNSUPPORTED).
  * Asynchronous on `stream`.
  */
 tdp_status tdp_blend_tokens(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_dtype,
