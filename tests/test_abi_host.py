@@ -206,3 +206,28 @@ def test_search_layouts_capacity_and_errors(T):
     assert lib.tdp_search_layouts(C_.byref(d), 0, C_.byref(fr), 4, 4, 0, None, 0, C_.byref(n)) == 1
     assert lib.tdp_search_layouts(C_.byref(d), 3, C_.byref(fr), 4, 4, 8, None, 0, C_.byref(n)) == 1
     assert lib.tdp_search_layouts(C_.byref(d), 3, C_.byref(fr), 4, 4, 0, None, 2, C_.byref(n)) == 1
+
+
+def test_token_major_calls_reject_before_any_cuda_call(T):
+    """Argument errors of tdp_extract_tokens / tdp_blend_tokens return before
+    the library touches CUDA (fake, never dereferenced 16-byte-aligned pointers)."""
+    import ctypes as C_
+    lib = T._lib
+    p = T.plan((2, 4, 6), ((1, 0), (1, 0), (1, 0)))
+    ok, bad = C_.c_void_p(4096), C_.c_void_p(4104)   # 16-byte aligned / 8-byte aligned
+    BF16, F32 = T.BF16, T.F32
+    ex, bl = lib.tdp_extract_tokens, lib.tdp_blend_tokens
+    assert ex(C_.byref(p), 1, 3, BF16, ok, ok, None) == 6          # 6-byte tokens
+    assert bl(C_.byref(p), 1, 3, BF16, ok, BF16, ok, None) == 6
+    assert bl(C_.byref(p), 1, 2056, BF16, ok, BF16, ok, None) == 6  # 257 chunks per token, odd
+    assert ex(C_.byref(p), 1, 8208, BF16, ok, ok, None) == 6        # past 16 KiB per token
+    assert ex(C_.byref(p), 1, 8, BF16, bad, ok, None) == 4          # alignment
+    assert bl(C_.byref(p), 1, 8, BF16, ok, F32, bad, None) == 4
+    assert ex(C_.byref(p), 1, 8, BF16, None, ok, None) == 1         # null pointer
+    assert ex(C_.byref(p), 1, 8, 7, ok, ok, None) == 1              # unknown dtype
+    assert ex(C_.byref(p), 0, 8, BF16, None, None, None) == 0       # empty batch: nothing to do
+    assert bl(C_.byref(p), 1, 0, BF16, None, BF16, None, None) == 0
+    q = T.Plan()
+    C_.memmove(C_.byref(q), C_.byref(p), C_.sizeof(p))
+    q.stride[2] += 1                                                # not what tdp_plan produces
+    assert ex(C_.byref(q), 1, 8, BF16, ok, ok, None) == 1
