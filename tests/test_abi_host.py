@@ -231,3 +231,20 @@ def test_token_major_calls_reject_before_any_cuda_call(T):
     C_.memmove(C_.byref(q), C_.byref(p), C_.sizeof(p))
     q.stride[2] += 1                                                # not what tdp_plan produces
     assert ex(C_.byref(q), 1, 8, BF16, ok, ok, None) == 1
+
+
+def test_bench_algorithmic_bytes_of_the_4k_workload(T):
+    """Extract reads the latent and writes the tiles; blend reads the tiles
+    and writes the latent.  On the 4k workload the tile sizes per axis are
+    9 + 9 frames, 4 x 23 rows and 4 x 39 columns, so the tiles hold
+    18 * 92 * 156 tokens of 128 bf16 channels."""
+    import bench
+    wl = WORKLOADS["4k"]
+    p = T.plan(wl.dims, wl.tiling)
+    latent = 16 * 68 * 120 * 128
+    tiles = 18 * 92 * 156 * 128
+    assert p.tiles_numel(1, 128) == tiles
+    ab = bench.algorithmic_bytes(wl, tiles)
+    assert ab["extract"] == ab["blend"] == 2 * (latent + tiles) == 99_557_376
+    assert ab["total"] == 199_114_752
+    assert round(ab["overlap_factor"], 5) == 1.97868
