@@ -88,7 +88,7 @@ def read_peak() -> tuple:
 
 
 # The sources the profiled kernels (extract, blend, tokens) are built from.
-PROFILED_SOURCES = ("tdp_kernels.cu", "tdp_geometry.h")
+PROFILED_SOURCES = ("tdp_kernels.cu", "tdp_stream.cuh", "tdp_geometry.h")
 
 
 def source_digest() -> str:

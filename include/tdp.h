@@ -382,6 +382,57 @@ tdp_status tdp_blend_tokens(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dt
 tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum_out,
                           cudaStream_t stream);
 
+/*
+ * tdp_launch_geometry -- how tdp_extract (blend == 0) or tdp_blend
+ * (blend == 1) lays out a call with these sizes on a GPU with `sm_count`
+ * SMs.  Host only; touches no GPU.  It describes a launch, not a step of
+ * the method: it lets the kernels' index arithmetic be checked on the CPU
+ * and a benchmark report the launch configuration.
+ *   streaming       1 when the 16-byte streaming kernel takes the call (each
+ *                   output 16-byte chunk is written by one thread with one
+ *                   store); 0 when the general kernel does, and then every
+ *                   other field is 0
+ *   band_rows       latent rows per unit of work; nbands units per
+ *                   (b, c, frame) plane
+ *   units           B*C*F*nbands; unit u = (f * nbands + band) * B*C + b*C + c
+ *   grid            CTAs; CTA i takes units [cta_start[i], cta_start[i+1])
+ *   stages, stage_bytes  the shared-memory ring of staged units (each stage
+ *                   holds its data between two 32-byte guards); one producer
+ *                   warp fills it with bulk copies ahead of the compute warps
+ *   max_runs        blend: staged tile-row runs per unit at most
+ *   shared_bytes    dynamic shared memory per CTA
+ *   off_hdr, off_data  shared offsets of the run-base entries and the ring
+ *   chunks_per_row  blend: 16-byte output chunks per latent row
+ *   column_terms    blend: most column tiles touching one output chunk
+ *   rows_per_thread blend: consecutive band rows each thread computes (its
+ *                   chunk column of rows [g * n, (g + 1) * n) of every band,
+ *                   g = thread / chunks_per_row)
+ *   threads         compute threads of a CTA (the launch adds one producer
+ *                   warp)
+ *   run_slot        blend: shared bytes of each staged run's slot (run r of
+ *                   a unit sits at r * run_slot in its stage)
+ * For extract, in_dtype is the latent's type and out_dtype must equal it.
+ * cta_start: host int32 array of cta_start_len entries, or NULL; filled
+ *            with grid + 1 entries when cta_start_len > grid.
+ * tables:    host buffer of tables_bytes bytes, or NULL; receives the plan
+ *            tables passed with the launch (table_bytes of them, at most
+ *            tables_bytes) and, in table_offsets (8 int32, or NULL), the
+ *            16-byte word offsets of its sections: bands, frames, rows,
+ *            row-tile starts, frame-tile constants, column-tile constants,
+ *            runs, chunks.
+ */
+typedef struct {
+    int32_t streaming;
+    int32_t band_rows, nbands, units, grid, stages, stage_bytes, max_runs, shared_bytes;
+    int32_t off_hdr, off_data, chunks_per_row, column_terms, rows_per_thread, threads, run_slot;
+    int32_t table_bytes;
+} tdp_launch_geometry_t;
+
+tdp_status tdp_launch_geometry(const tdp_plan_t* plan, int32_t B, int32_t C, int32_t blend, tdp_dtype in_dtype,
+                               tdp_dtype out_dtype, int32_t sm_count, tdp_launch_geometry_t* geometry,
+                               int32_t* cta_start, int32_t cta_start_len, void* tables, int32_t tables_bytes,
+                               int32_t* table_offsets);
+
 /* Diagnostic word of the current device: nonzero when a kernel gave up
  * waiting for its staged copies (bounded wait) and skipped its work.
  * Reads it synchronously into *code and, when `clear` is nonzero, resets

@@ -24,6 +24,7 @@ LIB = os.path.join(PKG, "libtdp.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["tdp_plan.cpp", "tdp_kernels.cu", "tdp_token_major.cu"]
+HEADERS = ["tdp_geometry.h", "tdp_stream.cuh"]
 
 
 def _nvcc() -> str:
@@ -46,7 +47,7 @@ def _flags(verbose: bool):
 def build(verbose: bool = False, force: bool = False) -> str:
     """Compile (if any source is newer than the library) and return its path."""
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
-    deps = srcs + [os.path.join(CSRC, "tdp_geometry.h"), os.path.join(INCLUDE, "tdp.h")]
+    deps = srcs + [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "tdp.h")]
     if not force and os.path.exists(LIB):
         mtime = os.path.getmtime(LIB)
         if all(os.path.getmtime(d) <= mtime for d in deps):

@@ -25,6 +25,7 @@
 #include <climits>
 #include <cstdint>
 #include <cstring>
+#include <vector>
 
 #include "tdp.h"
 #include "tdp_geometry.h"
@@ -2126,8 +2127,15 @@ ItemCosts item_costs(const tdp_plan_t& p, int band_rows, int nbands, int BC) {
 static_assert(sizeof(tdp_plan_t) + sizeof(BlendArgs) <= 4096, "blend kernel parameters stay within 4 KB");
 
 template <typename Tin, typename Tout>
+tdp_status launch_blend_stream(const tdp_plan_t& p, int BC, const void* tiles, long long tiles_numel, void* out,
+                               cudaStream_t stream, bool* taken);
+
+template <typename Tin, typename Tout>
 tdp_status launch_blend(const tdp_plan_t& p, int BC, const void* tiles, long long tiles_numel, void* out,
                         cudaStream_t stream) {
+    bool taken = false;
+    const tdp_status sst = launch_blend_stream<Tin, Tout>(p, BC, tiles, tiles_numel, out, stream, &taken);
+    if (sst != TDP_OK || taken) return sst;
     int band_rows = p.dims[1];
     BlendLayout L;
     for (;;) {
@@ -2207,6 +2215,8 @@ tdp_status launch_blend(const tdp_plan_t& p, int BC, const void* tiles, long lon
     return go(blend_fast_kernel<Tin, Tout, 1, 2>, true);
 }
 
+#include "tdp_stream.cuh"
+
 }  // namespace
 
 namespace tdp {
@@ -2226,6 +2236,11 @@ tdp_status tdp_extract(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype d
     if (!latent || !tiles) return TDP_ERR_INVALID_ARG;
     if (!aligned16(latent) || !aligned16(tiles)) return TDP_ERR_ALIGNMENT;
     const tdp_plan_t& p = *plan;
+    if ((long long)B * C > INT_MAX) return TDP_ERR_INVALID_ARG;
+    bool taken = false;
+    const tdp_status sst = esz == 2 ? launch_extract_stream<uint16_t>(p, B * C, latent, tiles, stream, &taken)
+                                    : launch_extract_stream<uint32_t>(p, B * C, latent, tiles, stream, &taken);
+    if (sst != TDP_OK || taken) return sst;
     int band_rows = p.dims[1];
     ExtractLayout L;
     for (;;) {
@@ -2357,6 +2372,51 @@ tdp_status tdp_cond_combine(const tdp_plan_t* plan, int32_t B, int32_t M, int32_
     if (ob) return go(cond_combine_kernel<float, __nv_bfloat16>, static_cast<const float*>(tile_cond_out),
                       static_cast<__nv_bfloat16*>(out));
     return go(cond_combine_kernel<float, float>, static_cast<const float*>(tile_cond_out), static_cast<float*>(out));
+}
+
+tdp_status tdp_launch_geometry(const tdp_plan_t* plan, int32_t B, int32_t C, int32_t blend, tdp_dtype in_dtype,
+                               tdp_dtype out_dtype, int32_t sm_count, tdp_launch_geometry_t* geometry,
+                               int32_t* cta_start, int32_t cta_start_len, void* tables, int32_t tables_bytes,
+                               int32_t* table_offsets) {
+    if (!tdp::plan_is_valid(plan) || !geometry || B < 1 || C < 1 || sm_count < 1 || cta_start_len < 0 ||
+        tables_bytes < 0)
+        return TDP_ERR_INVALID_ARG;
+    const int isz = dtype_size(in_dtype), osz = dtype_size(out_dtype);
+    if (!isz || !osz || (!blend && isz != osz)) return TDP_ERR_INVALID_ARG;
+    if ((long long)B * C > INT_MAX) return TDP_ERR_INVALID_ARG;
+    std::memset(geometry, 0, sizeof(*geometry));
+    int kt = 0;
+    if (!stream_eligible(*plan, blend != 0, isz, osz, &kt)) return TDP_OK;
+    static thread_local StreamLaunch L;   // 9 KB: kept off the caller's stack
+    const tdp_status st = stream_geometry(*plan, blend != 0, B * C, isz, osz, sm_count, L);
+    if (st == TDP_ERR_UNSUPPORTED) return TDP_OK;
+    if (st != TDP_OK) return st;
+    geometry->streaming = 1;
+    geometry->band_rows = L.a.band_rows;
+    geometry->nbands = L.a.nbands;
+    geometry->units = L.a.n_units;
+    geometry->grid = L.grid;
+    geometry->stages = L.a.nstages;
+    geometry->stage_bytes = L.a.stage_bytes;
+    geometry->max_runs = L.a.max_runs;
+    geometry->shared_bytes = L.smem;
+    geometry->off_hdr = L.a.off_hdr;
+    geometry->off_data = L.a.off_data;
+    geometry->chunks_per_row = blend ? L.a.cpr : 0;
+    geometry->column_terms = blend ? kt : 0;
+    geometry->rows_per_thread = blend ? L.a.rbh : 0;
+    geometry->threads = 32 * (blend ? kStreamBlendWarps : kStreamExtractWarps);
+    geometry->run_slot = blend ? L.a.run_slot : 0;
+    geometry->table_bytes = 16 * L.a.t_words;
+    if (tables) std::memcpy(tables, L.tb.w, static_cast<size_t>(std::min(tables_bytes, 16 * L.a.t_words)));
+    if (table_offsets) {
+        const int32_t offs[8] = {L.a.t_band, L.a.t_frame, L.a.t_row, L.a.t_hs, L.a.t_fcon, L.a.t_wcon, L.a.t_runs,
+                                 L.a.t_chunk};
+        std::memcpy(table_offsets, offs, sizeof(offs));
+    }
+    if (cta_start && cta_start_len > L.grid)
+        for (int i = 0; i <= L.grid; ++i) cta_start[i] = L.sp.start[i];
+    return TDP_OK;
 }
 
 tdp_status tdp_device_error(uint32_t* code, int32_t clear) {

@@ -149,6 +149,22 @@ _lib.tdp_last_cuda_error.restype = C.c_int32
 _lib.tdp_plan_struct_size.argtypes = []
 _lib.tdp_plan_struct_size.restype = C.c_size_t
 
+
+class LaunchGeometry(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in (
+        "streaming", "band_rows", "nbands", "units", "grid", "stages", "stage_bytes", "max_runs", "shared_bytes",
+        "off_hdr", "off_data", "chunks_per_row", "column_terms", "rows_per_thread", "threads", "run_slot",
+        "table_bytes")]
+
+    def as_dict(self) -> dict:
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+_lib.tdp_launch_geometry.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int32, C.c_int, C.c_int, C.c_int32,
+                                     _P(LaunchGeometry), _P(C.c_int32), C.c_int32, C.c_void_p, C.c_int32,
+                                     _P(C.c_int32)]
+_lib.tdp_launch_geometry.restype = C.c_int
+
 if _lib.tdp_plan_struct_size() != C.sizeof(Plan):
     raise ImportError("tdp_plan_t layout mismatch between libtdp.so and the binding")
 
@@ -156,7 +172,8 @@ EXPORTS = ("tdp_plan", "tdp_tile_offset", "tdp_tiles_numel", "tdp_tile_box", "td
            "tdp_balanced_tile_split", "tdp_search_layouts",
            "tdp_extract", "tdp_positions", "tdp_cond_select", "tdp_tokens", "tdp_cond_combine", "tdp_blend",
            "tdp_extract_tokens", "tdp_blend_tokens", "tdp_window_sum",
-           "tdp_device_error", "tdp_status_str", "tdp_last_cuda_error", "tdp_plan_struct_size")
+           "tdp_launch_geometry", "tdp_device_error", "tdp_status_str", "tdp_last_cuda_error",
+           "tdp_plan_struct_size")
 
 
 def _check(status: int, what: str) -> None:
@@ -194,6 +211,28 @@ def plan_stats(p: Plan, ranks: int = 1) -> PlanStats:
     _check(_lib.tdp_plan_stats(C.byref(p), ranks, C.byref(a), C.byref(s), C.byref(tf), C.byref(im), C.byref(mw)),
            "tdp_plan_stats")
     return PlanStats(a.value, s.value, tf.value, im.value, mw.value)
+
+
+def launch_geometry(p: Plan, B: int, C_: int, blend: bool, in_dtype: torch.dtype, out_dtype: torch.dtype,
+                    sm_count: int, tables: bool = False):
+    """tdp_launch_geometry: (geometry dict, per-CTA first units) of a tdp_extract
+    (blend False) or tdp_blend call on a GPU with `sm_count` SMs; with
+    tables=True also (the launch's plan tables as bytes, their section
+    offsets in 16-byte words).  Host only."""
+    g = LaunchGeometry()
+    starts = (C.c_int32 * 1025)()
+    buf = (C.c_uint8 * 65536)()
+    offs = (C.c_int32 * 8)()
+    _check(_lib.tdp_launch_geometry(C.byref(p), B, C_, 1 if blend else 0, _dtype_code(in_dtype),
+                                    _dtype_code(out_dtype), sm_count, C.byref(g), starts, len(starts),
+                                    buf if tables else None, len(buf) if tables else 0, offs),
+           "tdp_launch_geometry")
+    d = g.as_dict()
+    st = [int(v) for v in starts[:d["grid"] + 1]] if d["streaming"] else []
+    if not tables:
+        return d, st
+    names = ("band", "frame", "row", "hs", "fcon", "wcon", "runs", "chunk")
+    return d, st, bytes(buf[:d["table_bytes"]]), dict(zip(names, [int(v) for v in offs]))
 
 
 def balanced_tile_split(ranks: int) -> Tuple[int, int]:
