@@ -399,7 +399,9 @@ tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum
  *   stages, stage_bytes  the shared-memory ring of staged units (each stage
  *                   holds its data between two 32-byte guards); one producer
  *                   warp fills it with bulk copies ahead of the compute warps
- *   max_runs        blend: staged tile-row runs per unit at most
+ *   max_runs        blend: staged tile-row runs per stage at most (a stage
+ *                   holds one covering frame tile's runs of a band; a unit
+ *                   of a frame two tiles cover takes two stages)
  *   shared_bytes    dynamic shared memory per CTA
  *   off_hdr, off_data  shared offsets of the run-base entries and the ring
  *   chunks_per_row  blend: 16-byte output chunks per latent row

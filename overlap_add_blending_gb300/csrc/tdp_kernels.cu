@@ -65,6 +65,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// After the last mbar_init of a CTA (once: each fence costs hundreds of
+// cycles): makes the initialised barriers visible to the async proxy.
+__device__ __forceinline__ void mbar_init_done() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -481,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 5) extract_kernel(const __grid_const
     };
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        mbar_init_done();
         for (int s = 0; s < S - 1 && first + s < last; ++s) {
             issue(s);
             ahead.next();
@@ -959,6 +965,7 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
             mbar_init(&empty[q], kConsumerWarps);
         }
         mbar_init(csync, kBlendConsumers);
+        mbar_init_done();
     }
     __syncthreads();
 
@@ -1238,7 +1245,10 @@ __global__ void __launch_bounds__(kThreads) blend_generic_kernel(const __grid_co
     const BlendBox c = blend_box(p, a, fb);
     const uintptr_t limit = reinterpret_cast<uintptr_t>(tiles + a.tiles_numel) & ~uintptr_t(15);
 
-    if (threadIdx.x == 0) mbar_init(bar, 32);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 32);
+        mbar_init_done();
+    }
     __syncthreads();
     if (threadIdx.x < 32) {
         blend_build_stage_table<Tin>(p, a, c, table);

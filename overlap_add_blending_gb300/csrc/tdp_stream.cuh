@@ -40,6 +40,8 @@ constexpr int kStreamBlendWarps = 16;
 constexpr int kStreamExtractThreads = 32 * (kStreamExtractWarps + 1);
 constexpr int kStreamBlendThreads = 32 * (kStreamBlendWarps + 1);
 constexpr uint32_t kErrDrain = 4u;          // copies still in flight after a timeout did not land in time
+constexpr int kStreamMaxStageRuns = 64;     // blend: runs per stage, two per producer lane
+
 constexpr int kStreamMaxStages = 8;
 constexpr int kStreamMaxGrid = 256;        // CTAs the split table holds (one per SM)
 constexpr int kStreamTableWords = 512;     // 16-byte words of plan tables passed with a launch
@@ -234,6 +236,7 @@ __device__ __forceinline__ StreamSmem stream_prologue(const StreamArgs& a, const
             mbar_init(&m.full[s], full_count);
             mbar_init(&m.empty[s], warps);
         }
+        mbar_init_done();
     }
     __syncthreads();
     pdl_wait();
@@ -245,7 +248,9 @@ __device__ __forceinline__ StreamSmem stream_prologue(const StreamArgs& a, const
 // copy by the producer warp's lane 0.
 // Writing: for every covering (frame tile, row tile, column tile), the run
 // of that tile's rows inside the band is a contiguous span of the packed
-// tiles.  Warp w takes spans w, w + 24, ...; lane l writes the span's
+// tiles.  The spans of successive units are dealt to the warps round robin
+// (a unit's first span goes to the warp after the one that took the
+// previous unit's last); lane l writes the span's
 // 8-byte groups l, l + 32, ... (coalesced 256-byte warp stores) from its
 // first 8-byte boundary on.  A group is four bf16 elements (two fp32), each
 // loaded from the staged band at its own address -- the shared load does
@@ -298,6 +303,7 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
     unsigned char* tiles = static_cast<unsigned char*>(a.dst);
     UnitCursor c;
     c.init(first, a.BC, a.nbands);
+    int rot = 0;   // the warp that takes the unit's first span: the spans are dealt round robin across units
     for (int k = 0; k < n; ++k, c.next()) {
         const int s = k % S;
         if (!mbar_wait_bounded(&m.full[s], (k / S) & 1)) {
@@ -309,8 +315,11 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
         const int nr = b.NHB * nw, nspans = fe.n * nr;
         const RunEnt* band_runs = m.runs + c.band * a.runs_per_band;
         const uint32_t band_off = static_cast<uint32_t>(a.off_data + s * a.stage_bytes + kStreamPad);
+        int spn = warp - rot;
+        if (spn < 0) spn += kWarps;
+        rot = (rot + nspans) % kWarps;
 #pragma unroll 1
-        for (int spn = warp; spn < nspans; spn += kWarps) {
+        for (; spn < nspans; spn += kWarps) {
             const int fa = spn >= nr ? 1 : 0, rr = spn - fa * nr;
             const int iw = rr % nw;
             const RunEnt re = band_runs[rr];
@@ -374,15 +383,17 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
 }
 
 // =================================================================== blend
-// Staging: the unit's runs -- one per (covering frame tile, row tile meeting
-// the band, column tile) -- each into its own fixed slot of the stage, as
-// the 16-byte chunks around it, one bulk copy per run by the producer
-// warp's lanes (lane l takes runs l, l + 32, ...).  A run's base entry (the
+// Staging: one stage per covering frame tile of the unit (a unit of a frame
+// two tiles cover takes two consecutive stages).  A stage holds the frame
+// tile's runs -- one per (row tile meeting the band, column tile) -- each in
+// its own fixed slot, as the 16-byte chunks around it, one bulk copy per run
+// by the producer warp's lanes (lane l takes runs l, l + 32, ...).  A run's base entry (the
 // shared offset of its slice's tile element (0, 0), as if the whole slice
 // were staged) goes to the run-base table; elements in the tile buffer's
-// last, partial 16 bytes are loaded plainly.  Each lane raises the stage's
-// transaction count by its bulk bytes before its copies and arrives after
-// them (32 arrivals), which also publishes its entries and plain loads.
+// last, partial 16 bytes are loaded plainly.  Lane 0 then arrives once on
+// the stage's barrier with the stage's bulk bytes (publishing the warp's
+// entries and plain loads) before the lanes issue their copies: one
+// arrival per stage, as every arrival on one barrier is serialised.
 // Compute: a thread owns one 16-byte output chunk column j (E = 16 / sizeof
 // (Tout) latent columns) for the whole kernel and a block of rbh
 // consecutive rows of every band: rows [rg * rbh, (rg + 1) * rbh), row
@@ -472,7 +483,7 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
     constexpr int kWarps = kStreamBlendWarps, kThreads = 32 * kStreamBlendWarps;   // compute threads
     constexpr int q1 = KT > 1 ? 1 : 0, q2 = KT > 2 ? 2 : 0;
     extern __shared__ __align__(128) unsigned char smem[];
-    const StreamSmem m = stream_prologue(a, tb, smem, 32, kWarps);
+    const StreamSmem m = stream_prologue(a, tb, smem, 1, kWarps);
     const int first = sp.start[blockIdx.x], last = sp.start[blockIdx.x + 1];
     if (first >= last) return;
     const int S = a.nstages, n = last - first;
@@ -487,42 +498,62 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
         const uintptr_t limit = (base + static_cast<uintptr_t>(a.src_bytes)) & ~uintptr_t(15);
         UnitCursor cs;
         cs.init(first, a.BC, a.nbands);
-        int k = 0;
+        int j = 0;   // stages filled so far
         bool ok = true;
-        for (; k < n; ++k, cs.next()) {
-            const int s = k % S;
-            const bool lane_ok = k < S || mbar_wait_backoff(&m.empty[s], ((k / S) - 1) & 1);
-            if (!__all_sync(0xffffffffu, lane_ok)) { ok = false; break; }
+        for (int k = 0; k < n && ok; ++k, cs.next()) {
             const BandEnt b = m.bands[cs.band];
             const FrameEnt fe = m.frames[cs.f];
-            const int nr = b.NHB * nw, nruns = fe.n * nr;
+            const int nr = b.NHB * nw;
             const RunEnt* band_runs = m.runs + cs.band * a.runs_per_band;
-            const uint32_t stage_off = static_cast<uint32_t>(a.off_data + s * a.stage_bytes + kStreamPad);
-            int* hdr = hdr0 + s * a.max_runs;
-            fence_proxy_async();   // the compute warps' reads of this stage come before the copies' writes
-            for (int r = lane; r < nruns; r += 32) {
-                const int fa = r >= nr ? 1 : 0;
-                const RunEnt re = band_runs[r - fa * nr];
-                const uintptr_t g0 = base + static_cast<uintptr_t>(run_e0(re, m.fcon[fe.lo + fa], a.BC, cs.bc, cs.f)) * esz;
-                const uintptr_t g1 = g0 + static_cast<uintptr_t>(re.len) * esz;
-                const uintptr_t lo = g0 & ~uintptr_t(15);
-                const uintptr_t up = (g1 + 15) & ~uintptr_t(15);
-                uintptr_t hi = up <= limit ? up : (g1 & ~uintptr_t(15));   // bulk part; past it, the buffer's tail
-                if (hi < lo) hi = lo;
-                const uint32_t slot = stage_off + static_cast<uint32_t>(r * a.run_slot);
-                hdr[r] = static_cast<int>(slot + static_cast<uint32_t>(g0 - lo)) - re.vrow * esz;
-                for (uintptr_t t = (hi > g0 ? hi : g0); t < g1; t += esz)
-                    *reinterpret_cast<Tin*>(smem + slot + static_cast<uint32_t>(t - lo)) = *reinterpret_cast<const Tin*>(t);
-                if (hi > lo) {
-                    mbar_expect_tx(&m.full[s], static_cast<uint32_t>(hi - lo));
-                    bulk_copy_g2s(smem + slot, reinterpret_cast<const void*>(lo), static_cast<uint32_t>(hi - lo), &m.full[s]);
+            for (int fa = 0; fa < fe.n; ++fa, ++j) {
+                const int s = j % S;
+                const bool lane_ok = j < S || mbar_wait_backoff(&m.empty[s], ((j / S) - 1) & 1);
+                if (!__all_sync(0xffffffffu, lane_ok)) { ok = false; break; }
+                const FrameCon fc = m.fcon[fe.lo + fa];
+                const uint32_t stage_off = static_cast<uint32_t>(a.off_data + s * a.stage_bytes + kStreamPad);
+                int* hdr = hdr0 + s * a.max_runs;
+                // each lane's runs (at most kRunsPerLane of them): entries and plain tail loads first
+                constexpr int kRunsPerLane = kStreamMaxStageRuns / 32;
+                uintptr_t cp_lo[kRunsPerLane];
+                uint32_t cp_n[kRunsPerLane], cp_slot[kRunsPerLane];
+                uint32_t bytes = 0;
+#pragma unroll
+                for (int i = 0; i < kRunsPerLane; ++i) {
+                    const int r = lane + 32 * i;
+                    cp_n[i] = 0;
+                    if (r >= nr) continue;
+                    const RunEnt re = band_runs[r];
+                    const uintptr_t g0 = base + static_cast<uintptr_t>(run_e0(re, fc, a.BC, cs.bc, cs.f)) * esz;
+                    const uintptr_t g1 = g0 + static_cast<uintptr_t>(re.len) * esz;
+                    const uintptr_t lo = g0 & ~uintptr_t(15);
+                    const uintptr_t up = (g1 + 15) & ~uintptr_t(15);
+                    uintptr_t hi = up <= limit ? up : (g1 & ~uintptr_t(15));   // bulk part; past it, the buffer's tail
+                    if (hi < lo) hi = lo;
+                    const uint32_t slot = stage_off + static_cast<uint32_t>(r * a.run_slot);
+                    hdr[r] = static_cast<int>(slot + static_cast<uint32_t>(g0 - lo)) - re.vrow * esz;
+                    for (uintptr_t t = (hi > g0 ? hi : g0); t < g1; t += esz)
+                        *reinterpret_cast<Tin*>(smem + slot + static_cast<uint32_t>(t - lo)) =
+                            *reinterpret_cast<const Tin*>(t);
+                    cp_lo[i] = lo;
+                    cp_n[i] = static_cast<uint32_t>(hi - lo);
+                    cp_slot[i] = slot;
+                    bytes += cp_n[i];
                 }
+                // one arrival announces the stage's bytes (and publishes the
+                // warp's entries and plain loads), then the copies
+                bytes = __reduce_add_sync(0xffffffffu, bytes);
+                __syncwarp();
+                fence_proxy_async();   // the compute warps' reads of this stage come before the copies' writes
+                if (lane == 0) mbar_arrive_expect_tx(&m.full[s], bytes);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < kRunsPerLane; ++i)
+                    if (cp_n[i]) bulk_copy_g2s(smem + cp_slot[i], reinterpret_cast<const void*>(cp_lo[i]), cp_n[i], &m.full[s]);
             }
-            mbar_arrive(&m.full[s]);
         }
         if (!ok && lane == 0) {
             atomicOr(&g_device_error, kErrBlendWait);
-            drain_stages(m.full, S, max(0, k - S), k);   // the copies still in flight
+            drain_stages(m.full, S, max(0, j - S), j);   // the copies still in flight
         }
         return;
     }
@@ -538,16 +569,20 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
     unsigned char* out = static_cast<unsigned char*>(a.dst);
     UnitCursor c;
     c.init(first, a.BC, a.nbands);
+    int j = 0;   // the unit's first stage
     for (int k = 0; k < n; ++k, c.next()) {
-        const int s = k % S;
-        if (!mbar_wait_bounded(&m.full[s], (k / S) & 1)) {
+        const FrameEnt fe = m.frames[c.f];
+        const int s0 = j % S, s1 = (j + 1) % S;
+        bool landed = mbar_wait_bounded(&m.full[s0], (j / S) & 1);
+        if (landed && fe.n > 1) landed = mbar_wait_bounded(&m.full[s1], ((j + 1) / S) & 1);
+        if (!landed) {
             if (lane == 0) atomicOr(&g_device_error, kErrBlendWait);
             return;   // no release: the producer gives up and drains
         }
         if (active) {
             const BandEnt b = m.bands[c.band];
-            const FrameEnt fe = m.frames[c.f];
-            const int* hdr = hdr0 + s * a.max_runs;
+            const int* hdr_f0 = hdr0 + s0 * a.max_runs;
+            const int* hdr_f1 = hdr0 + s1 * a.max_runs;
             unsigned char* oplane = out + ((((long long)c.bc * F + c.f) * H) * W + (long long)jc * E) * osz;
             const int h1 = min(b.hb1, b.hb0 + r_lo + a.rbh);
 #pragma unroll 1
@@ -563,7 +598,7 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
                     const int fa = pi >= re.n ? 1 : 0, jh = pi - fa * re.n;
                     const int ih = re.lo + jh;
                     const float wfh = __fmul_rn(fa ? fe.w[1] : fe.w[0], jh ? re.w[1] : re.w[0]);
-                    const int* hrun = hdr + (fa * b.NHB + (ih - b.ihlo)) * nw;
+                    const int* hrun = (fa ? hdr_f1 : hdr_f0) + (ih - b.ihlo) * nw;
                     const int yo = h - m.hs[ih];
                     float2 inner[E / 2];
 #pragma unroll
@@ -584,7 +619,11 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&m.empty[s]);
+        if (lane == 0) {
+            mbar_arrive(&m.empty[s0]);
+            if (fe.n > 1) mbar_arrive(&m.empty[s1]);
+        }
+        j += fe.n;
     }
 }
 
@@ -664,9 +703,9 @@ inline int stream_table_words(const tdp_plan_t& p, bool blend, StreamArgs& a) {
 }
 
 // Shared layout for one band height: barriers, tables, run-base entries
-// (blend), then the ring of stages, sized to the largest unit (a band's
-// runs times the plan's most covering frame tiles for blend; the band's
-// latent rows for extract).  False when the tables or two stages do not
+// (blend), then the ring of stages, each sized to the largest staged piece
+// (blend: one frame tile's runs of a band; extract: the band's latent
+// rows).  False when the tables or two stages do not
 // fit.  a.cpr and a.esz must be set.
 inline bool stream_layout(const tdp_plan_t& p, bool blend, int band_rows, StreamArgs& a, int& smem) {
     const int H = p.dims[1], W = p.dims[2];
@@ -676,7 +715,8 @@ inline bool stream_layout(const tdp_plan_t& p, bool blend, int band_rows, Stream
     for (int bi = 0; bi < a.nbands; ++bi)
         nhb_max = std::max(nhb_max, host_nhb(p, bi * band_rows, std::min(H, bi * band_rows + band_rows)));
     a.runs_per_band = nhb_max * p.num_tiles[2];
-    a.max_runs = blend ? p.max_cover[0] * a.runs_per_band : 0;
+    a.max_runs = blend ? a.runs_per_band : 0;   // one frame tile's runs per stage
+    if (a.max_runs > kStreamMaxStageRuns) return false;
     a.run_slot = blend ? host_run_slot(p, band_rows, a.nbands, a.esz) : 0;
     const long long data = blend ? (long long)a.max_runs * a.run_slot : (long long)band_rows * W * a.esz;
     if (data > INT_MAX / 8) return false;

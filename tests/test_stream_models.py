@@ -273,28 +273,33 @@ def model_blend(p, g, starts, B, C, in_esz, out_esz, tiles_bytes, ctas):
     out = np.full(BC * F * H * W, np.nan)
     count = np.zeros(BC * F * H * cpr, np.int64)
     for cta in ctas:
+        j = 0   # stages filled so far: one per covering frame tile of a unit
         for k, u in enumerate(range(starts[cta], starts[cta + 1])):
-            s = k % S
             bc, f, band = unit_decode(u, BC, nb)
             hb0, hb1 = band * br, min(H, band * br + br)
             flo, fhi = cover(p, 0, f)
             ihlo, ihhi = cover(p, 1, hb0)[0], cover(p, 1, hb1 - 1)[1]
             NHB = ihhi - ihlo + 1
             nruns = (fhi - flo + 1) * NHB * nw
-            assert nruns <= max_runs and off_hdr + (s + 1) * max_runs * 4 <= off_data
+            stages = [(j + fa) % S for fa in range(fhi - flo + 1)]
+            assert len(stages) <= 2 and len(set(stages)) == len(stages), "a unit's stages collide"
+            j += len(stages)
+            assert NHB * nw <= max_runs
+            for s in stages:
+                assert off_hdr + (s + 1) * max_runs * 4 <= off_data
             smem = np.full(total, 0xFF, np.uint8)   # NaN in bf16 and fp32 wherever nothing was staged
-            stage_off = off_data + s * SB + PAD
             hdr = np.zeros(nruns, np.int64)
             slot = g["run_slot"]
             for r in range(nruns):
                 iw, q = r % nw, r // nw
                 jh, fa = q % NHB, q // NHB
+                s = stages[fa]
                 e0, ln, sw, ws, r0, vrow = run_geom(p, BC, bc, f, hb0, hb1, flo + fa, ihlo + jh, iw)
                 g0 = e0 * in_esz
                 g1 = g0 + ln * in_esz
                 lo = g0 & ~15
                 up = (g1 + 15) & ~15
-                off = stage_off + r * slot
+                off = off_data + s * SB + PAD + (r - fa * NHB * nw) * slot
                 assert off % 16 == 0 and up - lo <= slot, "a run overflows its slot"
                 assert off + slot <= off_data + (s + 1) * SB - PAD, "a slot leaves its stage"
                 assert 0 <= lo and g1 <= len(tiles_bytes)
