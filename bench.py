@@ -4,23 +4,32 @@
 One step is one pass of every step of the path on the 4K-class workload
 (bf16 latent B=1, C=128, F=16, H=68, W=120; tiles 2x4x4 with overlaps
 2/8/12; 256 conditioning tokens, 64 with a negative time start):
-    tdp_extract, tdp_tokens (positions and conditioning selection in one
-    launch, plus the per-token count), tdp_window_sum, tdp_blend, in order
-    on one stream (the blend's persistent grid fills every SM, so the short
-    token kernels gain nothing from a second stream).
+    tdp_tokens (positions and conditioning selection in one launch, plus
+    the per-token count) and tdp_window_sum on a side stream beside
+    tdp_extract, then tdp_blend once both are done.
 The per-tile op between extract and blend is the caller's (here identity,
-outside the path).  Inputs are resident in HBM when the timed region starts;
-L2 is flushed (a 256 MiB write) before every step and before the blend,
-outside the timed spans.
+outside the path).  Inputs are resident in HBM when the timed region
+starts.  Steps run back to back over rotating device copies of the inputs
+and outputs whose total exceeds twice the L2, so no step finds its data in
+L2 (no flush inside the timed region).  Each kernel is also timed alone
+the same way, and once per launch after an L2 flush (that figure includes
+the launch latency).
 
 Headline: algorithmic extract+blend bytes per step / step time (GB/s):
     latent read + tile write (extract) + tile read + latent write (blend).
+The roofline fraction divides the dominant kernel's achieved GB/s by the
+measured HBM copy bandwidth in MEASURED_PEAKS.json (else a fallback,
+named in the line).  The line also carries the other workloads
+("configs": tiny, stage-1, full-res, the geometry sweep), the CPU oracle's
+throughput on one thread and on every core, and an end-to-end figure
+through host buffers.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tdp|reference]
 
-Under torchrun every rank runs its own replica (the tiles of the method are
-independent; there is no data-path collective) and rank 0 prints one JSON
-line with the max-over-ranks step time.
+Defaults: N=1, K=10000 steps, W=10.  Under torchrun every rank runs its own
+replica (the tiles of the method are independent; there is no data-path
+collective) and rank 0 prints one JSON line with the max-over-ranks step
+time.
 """
 from __future__ import annotations
 
@@ -45,7 +54,7 @@ from overlap_add_blending_gb300.workloads import WORKLOADS  # noqa: E402
 WORKLOAD = WORKLOADS["4k"]
 METRIC = "tile extract+blend HBM GB/s (fraction of GB300 peak) and latent elems/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_STEP = 5  # extract, tokens (2: per-tile kernel, per-token count), window sum, blend
+KERNELS_PER_STEP = 4  # extract, tokens (the per-token count in the same cooperative launch), window sum, blend
 
 
 def esz(dtype: str) -> int:
@@ -66,8 +75,9 @@ def config_dict(wl, note: str) -> dict:
                         f"W={wl.dims[2]}, tiles (frames {wl.tiling[0][0]}/{wl.tiling[0][1]}, height "
                         f"{wl.tiling[1][0]}/{wl.tiling[1][1]}, width {wl.tiling[2][0]}/{wl.tiling[2][1]}), "
                         f"{wl.num_cond} conditioning tokens ({wl.num_cond_negative} with negative time)",
-            "step": "extract, with tokens (positions + cond select) and window_sum beside it on a side "
-                    "stream, then blend; per-tile op: identity, outside",
+            "step": "extract on the main stream, tokens (positions + cond select) and window_sum on a side "
+                    "stream (ordered only by the blend's wait for them), then blend; per-tile op: identity, "
+                    "outside",
             "l2": note}
 
 
@@ -164,81 +174,301 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- oracle timing
-def oracle_step(wl, X, gen, cond, channels: int):
-    """One step of the CPU oracle on the first `channels` channels."""
-    from oracle import tdp_oracle as O
-    plan = O.make_plan(wl.dims, wl.tiling)
-    x = X[:, :channels]
-    tiles = O.extract(plan, x)
-    O.positions(plan, gen)
-    O.cond_select(plan, gen, cond)
-    y = O.blend(plan, tiles)
-    O.max_abs_deviation(plan)
-    return y
-
-
-def oracle_inputs(wl, channels: int):
+def oracle_inputs(wl, c0: int, c1: int):
+    """The workload's seeded latent, channels [c0, c1), rounded to the path's
+    dtype and widened to float64, plus the gen / cond positions."""
     import torch
-    Xf = inputs.latent((wl.B, wl.C) + wl.dims, seed=0)[:, :channels]
-    X = torch.from_numpy(np.ascontiguousarray(Xf)).to(torch.bfloat16).double().numpy()
+    Xf = inputs.latent((wl.B, wl.C) + wl.dims, seed=0)[:, c0:c1]
+    X = torch.from_numpy(np.ascontiguousarray(Xf))
+    X = (X.to(torch.bfloat16) if wl.dtype == "bf16" else X).double().numpy()
     gen = inputs.grid_positions(wl.B, *wl.dims)
     cond = inputs.cond_positions(wl.B, wl.num_cond, *wl.dims, n_negative=wl.num_cond_negative, seed=2)
     return X, gen, cond
 
 
-def sample_bytes(wl, channels: int) -> float:
-    frac = channels / wl.C
+def oracle_step(wl, X, gen, cond, tokens: bool = True):
+    """One step of the CPU oracle on the channels of X (extract, blend; with
+    `tokens` also positions, conditioning selection and the window sum)."""
+    from oracle import tdp_oracle as O
+    plan = O.make_plan(wl.dims, wl.tiling)
+    tiles = O.extract(plan, X)
+    if tokens:
+        O.positions(plan, gen)
+        O.cond_select(plan, gen, cond)
+        O.max_abs_deviation(plan)
+    return O.blend(plan, tiles)
+
+
+def step_bytes(wl, channels: int) -> float:
+    """Algorithmic extract+blend bytes of one step on `channels` channels."""
     from oracle import tdp_oracle as O
     plan = O.make_plan(wl.dims, wl.tiling)
     tiles = sum(int(np.prod(plan.shape(t))) for t in range(plan.num_tiles)) * wl.B * wl.C
-    return algorithmic_bytes(wl, tiles)["total"] * frac
+    return algorithmic_bytes(wl, tiles)["total"] * channels / wl.C
 
 
-def cpu_baseline(wl, budget_s: float = 10.0, channels: int = 16) -> dict:
-    X, gen, cond = oracle_inputs(wl, channels)
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_worker(name, c0, c1, tokens, warm, steps, budget_s, ready, go, out):
+    """One CPU process of the oracle timing: warm-up, then `steps` steps (or
+    as many as fit in `budget_s` when steps is 0) on channels [c0, c1)."""
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    sys.path.insert(0, ROOT)
+    wl = WORKLOADS[name]
+    X, gen, cond = oracle_inputs(wl, c0, c1)
     t0 = time.perf_counter()
-    n = 0
-    while True:
-        oracle_step(wl, X, gen, cond, channels)
-        n += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": sample_bytes(wl, channels) * n / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} oracle steps (extract, positions, cond select, blend, window sum; float64 NumPy, "
-                      f"one thread) on {channels} of {wl.C} channels of the 4k-class workload, "
-                      f"{dt:.1f} s; bytes scaled to the sample"}
+    for _ in range(max(1, warm)):
+        oracle_step(wl, X, gen, cond, tokens)
+    per = (time.perf_counter() - t0) / max(1, warm)
+    n = steps if steps > 0 else max(1, int(budget_s / max(per, 1e-6)))
+    ready.put(n)
+    go.wait(600)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        oracle_step(wl, X, gen, cond, tokens)
+    out.put((c0, c1, n, t0, time.perf_counter()))
+
+
+def oracle_timing(wl, channels: int, procs: int, warm: int = 1, steps: int = 0, budget_s: float = 10.0) -> dict:
+    """The oracle, as it stands, on `channels` channels of the workload split
+    over `procs` spawned processes (one thread each; process 0 also runs the
+    per-step token and window work).  Every process runs the same number of
+    steps; the time is from the first start to the last end."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")   # never fork a process that holds a CUDA context
+    procs = max(1, min(procs, channels))
+    bounds = [channels * i // procs for i in range(procs + 1)]
+    ready, out, go = ctx.Queue(), ctx.Queue(), ctx.Event()
+    ps = [ctx.Process(target=_oracle_worker, args=(wl.name, bounds[i], bounds[i + 1], i == 0, warm, steps,
+                                                   budget_s, ready, go, out), daemon=True)
+          for i in range(procs)]
+    for q in ps:
+        q.start()
+    def collect(q, n, limit_s):
+        got, t0 = [], time.perf_counter()
+        while len(got) < n:
+            try:
+                got.append(q.get(timeout=1.0))
+            except Exception:
+                if any(x.exitcode not in (None, 0) for x in ps) or time.perf_counter() - t0 > limit_s:
+                    raise RuntimeError("an oracle timing process failed or timed out")
+        return got
+
+    try:
+        collect(ready, len(ps), 600)   # every process warm (each sized its own step count)
+        go.set()
+        res = collect(out, len(ps), 900)
+    finally:
+        for q in ps:
+            q.join(timeout=30)
+            if q.is_alive():
+                q.terminate()
+    wall = max(r[4] for r in res) - min(r[3] for r in res)
+    nbytes = sum(step_bytes(wl, r[1] - r[0]) * r[2] for r in res)
+    steps_done = min(r[2] for r in res)
+    return {"gbs": nbytes / wall / 1e9, "wall_s": wall, "steps": steps_done, "procs": procs,
+            "ms_per_step": 1e3 * wall / max(1, steps_done), "bytes": nbytes}
+
+
+def cpu_baseline(wl) -> dict:
+    """The oracle on this host: one thread on 16 channels, and every core on
+    all channels (one process per core, disjoint channel slices)."""
+    one = oracle_timing(wl, 16, 1, budget_s=8.0)
+    cores = host_cores()
+    allc = oracle_timing(wl, wl.C, cores, budget_s=10.0)
+    return {"value": allc["gbs"], "unit": "GB/s", "cores": allc["procs"], "nproc": cores, "kind": "oracle",
+            "one_thread": {"value": one["gbs"], "unit": "GB/s", "cores": 1,
+                           "sample": f"{one['steps']} steps on 16 of {wl.C} channels, {one['wall_s']:.1f} s"},
+            "sample": f"{allc['steps']} oracle steps (extract and blend on every channel; positions, cond select "
+                      f"and window sum once per step) of the full {wl.C}-channel workload, float64 NumPy, "
+                      f"channels split over {allc['procs']} processes of one thread, {allc['wall_s']:.1f} s"}
 
 
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return 0
     wl = WORKLOAD
-    channels = 16
-    X, gen, cond = oracle_inputs(wl, channels)
-    for _ in range(args.warmup):
-        oracle_step(wl, X, gen, cond, channels)
-    times = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        oracle_step(wl, X, gen, cond, channels)
-        times.append(time.perf_counter() - t0)
-    ms = 1e3 * sum(times) / len(times)
-    value = sample_bytes(wl, channels) / (ms * 1e-3) / 1e9
+    channels = 16                     # per step: a bounded sample of the workload
+    procs = min(channels, host_cores())
+    r = oracle_timing(wl, channels, procs, warm=args.warmup, steps=args.steps)
+    value = r["gbs"]
+    ms = r["ms_per_step"]
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_dict(wl, "n/a (CPU)"),
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"each step: oracle extract, positions, cond select, blend and window sum "
-                                       f"on {channels} of {wl.C} channels (float64 NumPy, one thread); "
-                                       f"bytes scaled to the sample"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": procs, "nproc": host_cores(),
+                             "kind": "oracle",
+                             "sample": f"each step: oracle extract and blend on {channels} of {wl.C} channels "
+                                       f"(one channel per process, {procs} processes of one thread), positions, "
+                                       f"cond select and window sum once; float64 NumPy; bytes scaled to the "
+                                       f"sample"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
 # ----------------------------------------------------------------------------- GPU arm
+L2_BYTES = 129 * 1024 * 1024
+
+
+class Sets:
+    """Rotating device copies of one workload's inputs and outputs: step k
+    uses set k mod n, and n sets together hold more than twice L2, so a
+    set's data has left L2 by the time it is used again."""
+
+    def __init__(self, wl, p, dev, dt, tokens: bool, min_sets: int = 3, max_sets: int = 4096):
+        import torch
+        lat_shape = (wl.B, wl.C) + wl.dims
+        X = torch.from_numpy(inputs.latent(lat_shape, seed=0)).to(dt).to(dev)
+        gen = torch.from_numpy(inputs.grid_positions(wl.B, *wl.dims)).to(dev)
+        cond = torch.from_numpy(inputs.cond_positions(wl.B, max(wl.num_cond, 0), *wl.dims,
+                                                      n_negative=wl.num_cond_negative, seed=2)).to(dev)
+        tn = p.tiles_numel(wl.B, wl.C)
+        e = X.element_size()
+        per = 2 * X.numel() * e + tn * e + ((gen.numel() + cond.numel()) * 4 + 6 * wl.B * p.tokens_numel() * 4
+                                            if tokens else 0)
+        self.n = int(min(max_sets, max(min_sets, -(-2 * L2_BYTES // per))))
+        self.set_bytes = per
+        self.X = X.unsqueeze(0).repeat((self.n,) + (1,) * X.dim()).contiguous()
+        self.tiles = torch.empty((self.n, tn), dtype=dt, device=dev)
+        self.out = torch.empty_like(self.X)
+        self.maxdev = torch.empty((self.n, 4), dtype=torch.float32, device=dev)
+        self.tok = []
+        if tokens:
+            self.gen = gen.unsqueeze(0).repeat((self.n,) + (1,) * gen.dim()).contiguous()
+            self.cond = cond.unsqueeze(0).repeat((self.n,) + (1,) * cond.dim()).contiguous()
+            self.tok = [{} for _ in range(self.n)]
+        self.X0 = X
+
+
+def time_b2b(fn, n_sets: int, launches: int, stream, head_s: float, others=()) -> float:
+    """Mean ms of fn(i) over `launches` back-to-back calls, i = call mod
+    n_sets, between two events on `stream`; the host gets `head_s` of head
+    start (a GPU sleep) so that it never starves the GPU.  Streams in
+    `others` start their work after the first event too (fn must make
+    `stream` wait for their last work before the second)."""
+    import torch
+    torch.cuda._sleep(int(head_s * 2.0e9))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for o in others:
+        o.wait_event(a)
+    for k in range(launches):
+        fn(k % n_sets)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / launches
+
+
+def host_rate(fn, n_sets: int, calls: int = 20) -> float:
+    """Host seconds per enqueue of fn (sizes the GPU head start)."""
+    import torch
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(calls):
+        fn(k % n_sets)
+    dt = (time.perf_counter() - t0) / calls
+    torch.cuda.synchronize()
+    return dt
+
+
+def time_after_flush(fn, flush, stream, reps: int = 20) -> float:
+    """Median ms of one call between two events, each call after an L2 flush
+    outside its events (the single-launch figure, launch latency included)."""
+    import torch
+    for _ in range(3):
+        flush.zero_()
+        fn()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    for e in ev:
+        flush.zero_()
+        e[0].record(stream)
+        fn()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    return float(np.median([e[0].elapsed_time(e[1]) for e in ev]))
+
+
+def run_config(name, dev, stream, launches: int) -> dict:
+    """extract, blend (and tokens where the workload has conditioning
+    tokens) of one named workload, back to back over rotating sets."""
+    import torch
+    from overlap_add_blending_gb300 import tdp
+    wl = WORKLOADS[name]
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    p = tdp.plan(wl.dims, wl.tiling, wl.compat)
+    ab = algorithmic_bytes(wl, p.tiles_numel(wl.B, wl.C))
+    tokens = wl.num_cond > 0
+    S = Sets(wl, p, dev, dt, tokens)
+    ext = lambda i: tdp.extract(p, S.X[i], S.tiles[i])
+    bl = lambda i: tdp.blend(p, S.tiles[i], wl.B, wl.C, S.out[i])
+    tok = lambda i: tdp.tokens(p, S.gen[i], S.cond[i], True, True, S.tok[i])
+    for i in range(S.n):
+        ext(i)
+        bl(i)
+        if tokens:
+            tok(i)
+    torch.cuda.synchronize()
+    same = (torch.equal(S.out[S.n - 1], S.X0) if dt == torch.bfloat16 else
+            torch.allclose(S.out[S.n - 1], S.X0, rtol=1e-5, atol=1e-5))
+    if not same:
+        raise SystemExit(f"{name}: the identity round trip does not return the latent")
+    head = 3 * launches * max(host_rate(ext, S.n), host_rate(bl, S.n))
+    e_ms = time_b2b(ext, S.n, launches, stream, head)
+    b_ms = time_b2b(bl, S.n, launches, stream, head)
+    r = {"workload": f"{wl.dtype} B={wl.B} C={wl.C} (F,H,W)={wl.dims} tiling={wl.tiling}",
+         "sets": S.n, "extract_ms": e_ms, "blend_ms": b_ms,
+         "extract_gbs": ab["extract"] / (e_ms * 1e-3) / 1e9, "blend_gbs": ab["blend"] / (b_ms * 1e-3) / 1e9,
+         "gbs": ab["total"] / ((e_ms + b_ms) * 1e-3) / 1e9,
+         "latent_elems_per_s": ab["latent_elems"] / ((e_ms + b_ms) * 1e-3),
+         "algorithmic_bytes": ab["total"], "overlap_factor": round(ab["overlap_factor"], 5)}
+    if tokens:
+        t_head = 3 * launches * host_rate(tok, S.n)
+        t_ms = time_b2b(tok, S.n, launches, stream, t_head)
+        r["tokens_ms"] = t_ms
+        r["num_cond"] = wl.num_cond
+    st = tdp.plan_stats(p, 4)
+    r["stats"] = {"decoded_area": st.decoded_area, "seams": st.seams, "imbalance_r4": st.imbalance,
+                  "max_window_sum": st.max_window_sum}
+    del S
+    torch.cuda.empty_cache()
+    return r
+
+
+def sweep_figures(dev) -> dict:
+    """The geometry sweep: strips against the 3x5 grid (layout statistics at
+    R = 4, the device window maximum), and the window-sum excess of the 1-D
+    splits (21, n, 8) on the GPU."""
+    import torch
+    from overlap_add_blending_gb300 import tdp
+    from overlap_add_blending_gb300.workloads import SPLITS_1D
+    out = {}
+    m = torch.empty(4, dtype=torch.float32, device=dev)
+    for name in ("strips", "grid"):
+        wl = WORKLOADS[name]
+        p = tdp.plan(wl.dims, wl.tiling, wl.compat)
+        st = tdp.plan_stats(p, 4)
+        tdp.window_sum(p, m)
+        torch.cuda.synchronize()
+        out[name] = {"overlap_factor": st.decoded_area, "seams": st.seams, "imbalance_r4": st.imbalance,
+                     "max_window_sum": st.max_window_sum, "device_max_abs_dev": float(m[0].item())}
+    for dim, n, ov in SPLITS_1D:
+        p = tdp.plan((1, 1, dim), ((1, 0), (1, 0), (n, ov)), compat=True)
+        st = tdp.plan_stats(p, 1)
+        tdp.window_sum(p, m)
+        torch.cuda.synchronize()
+        out[f"1d_{dim}_{n}_{ov}"] = {"max_window_sum": st.max_window_sum,
+                                     "excess": st.max_window_sum - 1.0,
+                                     "device_max_abs_dev": float(m[0].item())}
+    return out
+
+
 def run_tdp(args, rank: int, world: int):
     import torch
     import torch.distributed as dist
@@ -254,140 +484,109 @@ def run_tdp(args, rank: int, world: int):
     dt = torch.bfloat16
     p = tdp.plan(wl.dims, wl.tiling)
     ab = algorithmic_bytes(wl, p.tiles_numel(wl.B, wl.C))
-
-    # resident inputs and outputs
-    X = torch.from_numpy(inputs.latent((wl.B, wl.C) + wl.dims, seed=0)).to(dt).to(dev)
-    gen_np = inputs.grid_positions(wl.B, *wl.dims)
-    cond_np = inputs.cond_positions(wl.B, wl.num_cond, *wl.dims, n_negative=wl.num_cond_negative, seed=2)
-    gen = torch.from_numpy(gen_np).to(dev)
-    cond = torch.from_numpy(cond_np).to(dev)
-    tiles = torch.empty(p.tiles_numel(wl.B, wl.C), dtype=dt, device=dev)
-    out = torch.empty_like(X)
-    tok_out = {}
-    maxdev = torch.empty(4, dtype=torch.float32, device=dev)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     side = torch.cuda.Stream(device=dev)
-    fork, join = torch.cuda.Event(), torch.cuda.Event()
+    join = torch.cuda.Event()
+    S = Sets(wl, p, dev, dt, tokens=True)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
-    # The token kernels and the window maximum do not read the latent or the
-    # tiles: they run on a side stream beside extract (they feed the per-tile
-    # model, not the blend's inputs), and the main stream waits for them
-    # before the blend.
-    def side_work(g=gen, c=cond, m=maxdev):
-        fork.record(stream)
-        side.wait_event(fork)
-        tdp.tokens(p, g, c, True, True, tok_out, stream=side)
-        tdp.window_sum(p, m, stream=side)
+    # One step on set i: the token kernels and the window maximum on a side
+    # stream, extract on the main stream, then the blend once the side work
+    # is done (in use, the per-tile model between extract and blend takes the
+    # tiles and the token outputs).  The side kernels read only their own
+    # step's positions, so the side stream is not ordered after the previous
+    # step's kernels: it runs ahead and its kernels overlap the main stream's.
+    def side_work(i):
+        tdp.tokens(p, S.gen[i], S.cond[i], True, True, S.tok[i], stream=side)
+        tdp.window_sum(p, S.maxdev[i], stream=side)
         join.record(side)
 
-    def path(x=X, g=gen, c=cond, o=out, m=maxdev):
-        side_work(g, c, m)
-        tdp.extract(p, x, tiles)
+    def step(i):
+        side_work(i)
+        tdp.extract(p, S.X[i], S.tiles[i])
         stream.wait_event(join)
-        tdp.blend(p, tiles, wl.B, wl.C, o)
+        tdp.blend(p, S.tiles[i], wl.B, wl.C, S.out[i])
 
-    # One step: extract with the token and window kernels beside it on the
-    # side stream, then the blend.  Events on the main stream: ev0 start,
-    # ev1 extract done, ev2 side work joined, ev3 / ev4 around the blend.  L2
-    # is flushed before the step and again before the blend, outside the
-    # timed spans: in use, the per-tile model runs between the two phases.
-    def timed_step(ev):
-        ev[0].record(stream)
-        side_work()
-        tdp.extract(p, X, tiles)
-        ev[1].record(stream)
-        stream.wait_event(join)
-        ev[2].record(stream)
-        flush.zero_()
-        ev[3].record(stream)
-        tdp.blend(p, tiles, wl.B, wl.C, out)
-        ev[4].record(stream)
-
-    # host enqueue time of one step, to size the head start given to the host
-    path()
+    for i in range(S.n):
+        step(i)
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(3):
-        path()
-    enqueue_s = (time.perf_counter() - t0) / 3
-    torch.cuda.synchronize()
-    sleep_cycles = int(max(200e-6, 3 * enqueue_s) * 2.0e9)
+    for i in range(S.n):
+        if not torch.equal(S.out[i], S.X0):
+            raise SystemExit("the identity round trip is not exact")
+    enqueue_s = host_rate(step, S.n)
 
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     gpu_index = visible[local].strip() if len(visible) > local and visible[local].strip() else str(local)
     sampler = ClockSampler(gpu_index)
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        path()
+    for k in range(args.warmup):
+        step(k % S.n)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
 
+    # The timed region: K steps back to back, step k on set k mod n (no flush:
+    # the sets together are larger than L2), between two events.
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     wall0 = time.perf_counter()
-    for k in range(K):
-        flush.zero_()
-        torch.cuda._sleep(sleep_cycles)      # the host enqueues the whole step meanwhile
-        timed_step(evs[k])
+    chunk = 200                      # steps per head start: the sleep covers their enqueue
+    total_ms = 0.0
+    for k0 in range(0, K, chunk):
+        kk = min(chunk, K - k0)
+        total_ms += kk * time_b2b(lambda i, k0=k0: step((k0 + i) % S.n), S.n, kk, stream,
+                                  max(200e-6, 1.5 * kk * enqueue_s), others=(side,))
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    step_ms = total_ms / K
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     clocks = sampler.stop()
 
-    # step = (extract beside tokens + window sum) + blend
-    step = np.array([evs[k][0].elapsed_time(evs[k][2]) + evs[k][3].elapsed_time(evs[k][4]) for k in range(K)])
-    seg = np.array([[evs[k][0].elapsed_time(evs[k][1]), evs[k][1].elapsed_time(evs[k][2]),
-                     evs[k][3].elapsed_time(evs[k][4])] for k in range(K)])  # ms
-    step_ms = float(step.mean())
-    per_kernel_ms = seg.mean(axis=0)
-    # extract: its own span (sharing the GPU with the side kernels); the
-    # token kernels' cost is what they add after extract ends
-    names = ["extract", "tokens_and_window_sum_after_extract", "blend"]
+    # Per kernel: each alone, back to back over the rotating sets (its mean
+    # launch time), and once after an L2 flush (the single-launch figure,
+    # launch latency included).
+    L = min(K, 200)
+    ext = lambda i: tdp.extract(p, S.X[i], S.tiles[i])
+    bl = lambda i: tdp.blend(p, S.tiles[i], wl.B, wl.C, S.out[i])
+
+    def side_only(i):
+        tdp.tokens(p, S.gen[i], S.cond[i], True, True, S.tok[i])
+        tdp.window_sum(p, S.maxdev[i])
+
+    kern_ms = {}
+    for name, fn in (("extract", ext), ("blend", bl), ("tokens_and_window_sum", side_only)):
+        kern_ms[name] = time_b2b(fn, S.n, L, stream, max(200e-6, 3 * L * host_rate(fn, S.n)))
+    single_ms = {"extract": time_after_flush(lambda: ext(0), flush, stream),
+                 "blend": time_after_flush(lambda: bl(0), flush, stream)}
 
     # The next row after the step (not part of it): the conditioning-token
     # combine, on the step's selection, with D = C features per token.
+    tok0 = S.tok[0]
     comb_in = torch.randn((p.T, wl.B, wl.num_cond, wl.C), device=dev).to(dt)
     comb_out = torch.empty((wl.B, wl.num_cond, wl.C), dtype=dt, device=dev)
-    for _ in range(3):
-        tdp.cond_combine(p, comb_in, tok_out["slot_of"], tok_out["weight"], out=comb_out)
-    cev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(20)]
-    torch.cuda._sleep(20 * sleep_cycles)   # the host enqueues all 20 launches meanwhile
-    for e in cev:
-        e[0].record(stream)
-        tdp.cond_combine(p, comb_in, tok_out["slot_of"], tok_out["weight"], out=comb_out)
-        e[1].record(stream)
+    comb = lambda i: tdp.cond_combine(p, comb_in, tok0["slot_of"], tok0["weight"], out=comb_out)
+    comb(0)
+    comb_ms = time_b2b(comb, 1, 20, stream, max(200e-6, 3 * 20 * host_rate(comb, 1)))
+
+    # The token-major pair (tiles as [B, N_t, C] token sequences), back to back
+    # over the same rotating sets.
+    tm_tiles = torch.empty_like(S.tiles)
+    tm_out = torch.empty_like(S.out)
+    tmx = lambda i: tdp.extract_tokens(p, S.X[i], tm_tiles[i])
+    tmb = lambda i: tdp.blend_tokens(p, tm_tiles[i], wl.B, wl.C, tm_out[i])
+    for i in range(S.n):
+        tmx(i)
+        tmb(i)
     torch.cuda.synchronize()
-    comb_ms = float(np.median([e[0].elapsed_time(e[1]) for e in cev]))
+    if not torch.equal(tm_out[0], S.X0):
+        raise SystemExit("token-major round trip is not exact")
+    tmx_ms = time_b2b(tmx, S.n, L, stream, max(200e-6, 3 * L * host_rate(tmx, S.n)))
+    tmb_ms = time_b2b(tmb, S.n, L, stream, max(200e-6, 3 * L * host_rate(tmb, S.n)))
+    del tm_tiles, tm_out
 
-    # The next row after that: the token-major pair (tiles as [B, N_t, C] token
-    # sequences), each launch timed alone after an L2 flush outside its events.
-    tm_tiles = torch.empty_like(tiles)
-    tm_out = torch.empty_like(X)
-
-    def time_alone(fn, reps: int = 20) -> float:
-        for _ in range(3):
-            flush.zero_()
-            fn()
-        ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
-        for e in ev2:
-            flush.zero_()
-            e[0].record(stream)
-            fn()
-            e[1].record(stream)
-        torch.cuda.synchronize()
-        return float(np.median([e[0].elapsed_time(e[1]) for e in ev2]))
-
-    tmx_ms = time_alone(lambda: tdp.extract_tokens(p, X, tm_tiles))
-    tmb_ms = time_alone(lambda: tdp.blend_tokens(p, tm_tiles, wl.B, wl.C, tm_out))
-
-    # The host planner (the last next row): the layout search for this
-    # latent at 8 ranks, frame tiling and overlaps as in the workload.
+    # The host planner: the layout search for this latent at 8 ranks.
     t0 = time.perf_counter()
     for _ in range(20):
         cands = tdp.search_layouts(wl.dims, 8, wl.tiling[0], wl.tiling[1][1], wl.tiling[2][1])
@@ -395,21 +594,16 @@ def run_tdp(args, rank: int, world: int):
     picks = {c["role"]: list(c["counts"]) for c in cands if c["role"] in ("coarse", "fine", "balanced")}
 
     # e2e: host buffers in, blended latent out, through the same C-ABI calls.
-    # Steps are pipelined over two device buffer sets: step k's inputs go up
-    # on one copy stream while step k-1 computes, and step k-1's result comes
-    # down on another while step k computes.  Timed from the first upload to
-    # the last download, over K steps.
-    X_h = X.cpu().pin_memory()
-    gen_h = gen.cpu().pin_memory()
-    cond_h = cond.cpu().pin_memory()
-    out_h = [torch.empty(out.shape, dtype=dt, pin_memory=True) for _ in range(2)]
+    # Two device buffer sets; step k's inputs go up on one copy stream while
+    # step k-1 computes, and step k-1's result comes down on another.  Timed
+    # from the first upload to the last download, over K steps.
+    X_h = S.X0.cpu().pin_memory()
+    gen_h = S.gen[0].cpu().pin_memory()
+    cond_h = S.cond[0].cpu().pin_memory()
+    out_h = [torch.empty(S.X0.shape, dtype=dt, pin_memory=True) for _ in range(2)]
     dev_h = [torch.empty(1, dtype=torch.float32, pin_memory=True) for _ in range(2)]
     h2d = X_h.numel() * X_h.element_size() + gen_h.numel() * 4 + cond_h.numel() * 4
     d2h = out_h[0].numel() * out_h[0].element_size() + 4
-    ref_out = out.cpu()
-    bufs = [(X, gen, cond, out, maxdev),
-            (torch.empty_like(X), torch.empty_like(gen), torch.empty_like(cond), torch.empty_like(out),
-             torch.empty_like(maxdev))]
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     in_ready, in_free, out_ready, out_free = ([torch.cuda.Event() for _ in range(2)] for _ in range(4))
     for i in range(2):
@@ -418,22 +612,22 @@ def run_tdp(args, rank: int, world: int):
 
     def e2e_step(k):
         i = k % 2
-        x, g, c, o, m = bufs[i]
         up.wait_event(in_free[i])
         with torch.cuda.stream(up):
-            x.copy_(X_h, non_blocking=True)
-            g.copy_(gen_h, non_blocking=True)
-            c.copy_(cond_h, non_blocking=True)
+            S.X[i].copy_(X_h, non_blocking=True)
+            S.gen[i].copy_(gen_h, non_blocking=True)
+            S.cond[i].copy_(cond_h, non_blocking=True)
         in_ready[i].record(up)
         stream.wait_event(in_ready[i])
+        side.wait_event(in_ready[i])
         stream.wait_event(out_free[i])
-        path(x, g, c, o, m)
+        step(i)
         in_free[i].record(stream)
         out_ready[i].record(stream)
         down.wait_event(out_ready[i])
         with torch.cuda.stream(down):
-            out_h[i].copy_(o, non_blocking=True)
-            dev_h[i].copy_(m[:1], non_blocking=True)
+            out_h[i].copy_(S.out[i], non_blocking=True)
+            dev_h[i].copy_(S.maxdev[i][:1], non_blocking=True)
         out_free[i].record(down)
 
     for k in range(min(3, args.warmup)):
@@ -442,29 +636,40 @@ def run_tdp(args, rank: int, world: int):
     t_first, t_last = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     up.wait_stream(stream)
     with torch.cuda.stream(up):
-        torch.cuda._sleep(sleep_cycles)   # the host enqueues ahead meanwhile
+        torch.cuda._sleep(int(max(200e-6, 1.5 * min(K, 200) * enqueue_s) * 2.0e9))
     t_first.record(up)
+    side.wait_event(t_first)
     for k in range(K):
         e2e_step(k)
     down.wait_stream(stream)
     t_last.record(down)
     torch.cuda.synchronize()
+    ref_out = S.X0.cpu()
     for i in range(2):
         if not torch.equal(out_h[i], ref_out):
             raise SystemExit("e2e: a downloaded result differs from the device-resident step's")
     e2e_ms = t_first.elapsed_time(t_last) / K
 
+    # every config of the workload table, and the sweep's figures
+    configs = {}
+    if rank == 0 and not args.no_configs:
+        for name in ("tiny", "stage1", "fullres", "strips", "grid"):
+            configs[name] = run_config(name, dev, stream, launches=100)
+        configs["sweep"] = sweep_figures(dev)
 
-    # replicas: slowest rank's times, every rank's work
-    mx, job_bytes = combine([step_ms, e2e_ms] + [float(v) for v in per_kernel_ms], ab["total"], device=dev)
-    step_ms, e2e_ms, per_kernel_ms = mx[0], mx[1], np.array(mx[2:])
+    names = ["extract", "blend", "tokens_and_window_sum"]
+    mx, job_bytes = combine([step_ms, e2e_ms] + [kern_ms[n] for n in names], ab["total"], device=dev)
+    step_ms, e2e_ms = mx[0], mx[1]
+    kern_ms = dict(zip(names, mx[2:]))
 
     if rank != 0:
         return 0
     peak, peak_src = read_peak()
-    kern = {n: {"ms": float(per_kernel_ms[i])} for i, n in enumerate(names)}
-    kern["extract"]["gbs"] = ab["extract"] / (kern["extract"]["ms"] * 1e-3) / 1e9
-    kern["blend"]["gbs"] = ab["blend"] / (kern["blend"]["ms"] * 1e-3) / 1e9
+    kern = {n: {"ms": float(kern_ms[n])} for n in names}
+    for n in ("extract", "blend"):
+        kern[n]["gbs"] = ab[n] / (kern[n]["ms"] * 1e-3) / 1e9
+        kern[n]["single_launch_after_flush_ms"] = single_ms[n]
+        kern[n]["single_launch_after_flush_gbs"] = ab[n] / (single_ms[n] * 1e-3) / 1e9
     dom = "blend" if kern["blend"]["ms"] >= kern["extract"]["ms"] else "extract"
     achieved = kern[dom]["gbs"]
     traffic = recorded_traffic(dom)
@@ -473,13 +678,18 @@ def run_tdp(args, rank: int, world: int):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": config_dict(wl, "flushed (256 MiB write, outside the events) before every step and again "
-                                  "before the blend"),
+        "config": config_dict(wl, f"inputs larger than L2: step k uses set k mod {S.n} of rotating device "
+                                  f"copies ({S.set_bytes / 1e6:.0f} MB each: latent, tiles, output, token "
+                                  f"buffers), so every set has left the 129 MB L2 before its next use; no "
+                                  f"flush inside the timed region"),
         "latent_elems_per_s": world * ab["latent_elems"] / (step_ms * 1e-3),
         "extract_blend_gbs": ab["total"] / ((kern["extract"]["ms"] + kern["blend"]["ms"]) * 1e-3) / 1e9,
         "algorithmic_bytes": {"extract": ab["extract"], "blend": ab["blend"],
                               "overlap_factor": round(ab["overlap_factor"], 5)},
         "kernels": kern,
+        "kernel_timing": "each kernel alone, back to back over the rotating sets (mean per launch, "
+                         f"{L} launches between two events); single_launch_after_flush: median of 20 launches, "
+                         "each after a 256 MiB write outside its events (includes the launch latency)",
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src},
         "e2e": {"value": job_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
@@ -487,13 +697,14 @@ def run_tdp(args, rank: int, world: int):
                 "pipelined": "two buffer sets; uploads, steps and downloads on three streams; "
                              "first upload to last download over K steps"},
         "gpu_launches": KERNELS_PER_STEP * K,
+        "configs": configs,
         "next_rows": {"cond_combine": {"ms": comb_ms, "workload": f"T={p.T} tiles, B={wl.B}, M={wl.num_cond} "
-                                       f"conditioning tokens, D={wl.C} bf16 features; median of 20, not in the step"},
+                                       f"conditioning tokens, D={wl.C} bf16 features; back to back, one set"},
                       "token_major": {
                           "extract_tokens": {"ms": tmx_ms, "gbs": ab["extract"] / (tmx_ms * 1e-3) / 1e9},
                           "blend_tokens": {"ms": tmb_ms, "gbs": ab["blend"] / (tmb_ms * 1e-3) / 1e9},
                           "workload": "the step's latent and tiles with each tile as [B, N_t, C] tokens; "
-                                      "median of 20 launches, each after an L2 flush; not in the step"},
+                                      "back to back over the rotating sets"},
                       "layout_search": {"us": search_us, "ranks": 8, "candidates": len(cands), "picks": picks,
                                         "workload": "host layout search for this latent, frame tiling and "
                                                     "overlaps; mean of 20 calls"}},
@@ -509,10 +720,11 @@ def run_tdp(args, rank: int, world: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)   # about 0.5 s timed: several clock samples
+    ap.add_argument("--steps", type=int, default=10000)   # about 0.6 s timed: several clock samples
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["tdp", "reference"], default="tdp")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' figures")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

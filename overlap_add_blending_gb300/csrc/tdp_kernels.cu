@@ -25,6 +25,8 @@
 #include <climits>
 #include <cstdint>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <vector>
 
 #include "tdp.h"
@@ -231,20 +233,23 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 
 // ------------------------------------------------------------------ shared loads by address
 // 32-bit shared-window byte addresses keep the hot loops' address math to
-// one add per access.
+// one add per access.  Each load names memory as clobbered: without that,
+// the compiler may treat the asm as touching no memory and move it across
+// ordinary C++ stores to shared memory (tables a thread writes and then
+// reads back), which volatile alone does not forbid.
 __device__ __forceinline__ int lds_s32(uint32_t addr) {
     int v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
 __device__ __forceinline__ float lds_f32(uint32_t addr) {
     float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
     unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
     return v;
 }
 // One staged element as fp32 (bf16 is widened exactly).
@@ -1531,6 +1536,10 @@ struct TokensArgs {
     int* num_kept;
     int* tile_cond;
     int* slot_of;      // [T, B, M]: position in the tile's kept list, or -1 (NULL: not written)
+    // per-token count and weight after a grid-wide barrier (cooperative
+    // launch only; NULL: the count kernel follows instead)
+    int* count;
+    float* weight;
 };
 
 constexpr int kPosCache = 4;   // tokens per thread kept in registers between reduce and write
@@ -1598,7 +1607,7 @@ __device__ __forceinline__ bool keep_token(const int2 (&c)[3], const int ext[6])
 // the chunks' kept counts meet through distributed shared memory, and it
 // writes its kept tokens, compacted in their original order.  Every plan
 // read here is uniform across the CTA, so the plan stays a parameter.
-__global__ void __launch_bounds__(kThreads) tokens_kernel(const __grid_constant__ tdp_plan_t p, const TokensArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) tokens_kernel(const __grid_constant__ tdp_plan_t p, const TokensArgs a) {
     __shared__ int ext_sh[6];
     __shared__ int scan_sh[33];
     __shared__ int kept_sh;
@@ -1807,6 +1816,27 @@ __global__ void __launch_bounds__(kThreads) tokens_kernel(const __grid_constant_
     }
     if (rank == 0 && threadIdx.x == 0 && a.num_kept) a.num_kept[row] = total;   // 0 when M = 0 (rank 0 knows it)
     cluster.barrier_wait();  // no CTA leaves while a peer may read its shared memory
+
+    // Launched cooperatively: once every tile's keep flags are written, the
+    // grid counts the tiles keeping each conditioning token (what the count
+    // kernel otherwise does in a launch of its own).
+    if (a.count) {
+        cg::this_grid().sync();
+        const int BM = a.B * a.M, T = p.total_tiles;
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < BM; i += gridDim.x * blockDim.x) {
+            int c = 0, u = 0;
+            for (; u + 16 <= T; u += 16) {   // 16 independent loads in flight
+                int k[16];
+#pragma unroll
+                for (int v = 0; v < 16; ++v) k[v] = a.keep[(long long)(u + v) * BM + i];
+#pragma unroll
+                for (int v = 0; v < 16; ++v) c += k[v];
+            }
+            for (; u < T; ++u) c += a.keep[(long long)u * BM + i];
+            a.count[i] = c;
+            a.weight[i] = c ? 1.0f / static_cast<float>(c) : 0.0f;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kThreads) cond_count_kernel(const unsigned char* keep, int T, int BM,
@@ -2068,26 +2098,37 @@ tdp_status set_smem(K kernel, int bytes) {
 // its predecessor in the stream finishes; see pdl_wait) and, with
 // cluster > 1, clusters of that many CTAs.
 template <typename K, typename... Args>
-tdp_status launch(K kernel, long long blocks, int threads, int smem, cudaStream_t stream, int cluster, Args... args) {
+tdp_status launch_ex(K kernel, long long blocks, int threads, int smem, cudaStream_t stream, int cluster,
+                     bool cooperative, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     unsigned n = 1;
     if (cluster > 1) {
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        n = 2;
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
     return cuda_status(cudaLaunchKernelEx(&cfg, kernel, args...));
+}
+
+template <typename K, typename... Args>
+tdp_status launch(K kernel, long long blocks, int threads, int smem, cudaStream_t stream, int cluster, Args... args) {
+    return launch_ex(kernel, blocks, threads, smem, stream, cluster, false, args...);
 }
 
 template <typename K, typename... Args>
@@ -2317,6 +2358,39 @@ tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum
     return launch(window_sum_kernel, blocks, kThreads, smem, stream, 1, p, max_abs_dev, sum_out, tables);
 }
 
+// CTAs of tokens_kernel that can be resident at once on the current device
+// (whole 8-CTA clusters), or 0 if the device cannot say; queried once per
+// device.
+static long long tokens_coop_capacity() {
+    static std::mutex mu;
+    static std::map<int, long long> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int coop = 0;
+    long long cap = 0;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kCluster, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kCluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, tokens_kernel, &cfg) == cudaSuccess)
+            cap = (long long)clusters * kCluster;
+    }
+    (void)cudaGetLastError();
+    cache[dev] = cap;
+    return cap;
+}
+
 tdp_status tdp_tokens(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos, int32_t normalize,
                       int32_t* tile_pos, int32_t* offsets, int32_t M, const int32_t* cond_pos,
                       int32_t* tile_extent, uint8_t* keep, int32_t* count, float* weight, int32_t* kept_idx,
@@ -2332,7 +2406,15 @@ tdp_status tdp_tokens(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos,
     const long long blocks = (long long)kCluster * plan->total_tiles * B;
     if (blocks > INT_MAX || (long long)B * M > INT_MAX) return TDP_ERR_INVALID_ARG;
     TokensArgs a{gen_pos, B, normalize ? 1 : 0, tile_pos, offsets, M, cond_pos, tile_extent, keep, kept_idx,
-                 num_kept, tile_cond_pos, slot_of};
+                 num_kept, tile_cond_pos, slot_of, nullptr, nullptr};
+    if (M > 0 && blocks <= tokens_coop_capacity()) {
+        // every CTA resident at once: the count follows a grid barrier in the same launch
+        TokensArgs ac = a;
+        ac.count = count;
+        ac.weight = weight;
+        if (launch_ex(tokens_kernel, blocks, kThreads, 0, stream, kCluster, true, *plan, ac) == TDP_OK) return TDP_OK;
+        (void)cudaGetLastError();   // refused: the two-launch form below
+    }
     tdp_status st = launch_cluster(tokens_kernel, blocks, stream, *plan, a);
     if (st != TDP_OK || M == 0) return st;
     const int BM = B * M;
