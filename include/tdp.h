@@ -331,6 +331,48 @@ tdp_status tdp_blend(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_
                      const void* tiles, tdp_dtype out_dtype, void* out, cudaStream_t stream);
 
 /*
+ * tdp_shard_plan -- the sharded blend's layout for one of `ranks` ranks
+ * (host only).
+ *
+ * Source: "Tiled Data Parallelism (TDP)", What it is (tiles go to ranks
+ * round robin, tile t to rank t mod R, and one all_reduce sums the ranks'
+ * blended full-size buffers).  Reading: the same sum is formed without a
+ * reduction over full-size buffers -- the latent's rows are split into R
+ * disjoint output slabs, rank r blends its slab alone (tdp_blend_slab) from
+ * every tile that meets it, and the tiles it needs but does not own (its
+ * halo) come from their owners; the slabs concatenated along H are the
+ * blend, bit for bit.
+ *   row0, row1: rank `rank`'s slab, rows [row0, row1) of H, with
+ *               row_r = floor(r * H / ranks) (empty when ranks > H)
+ *   owned[t]:   1 iff t mod ranks == rank
+ *   needed[t]:  1 iff tile t's rows [start_h, end_h) meet [row0, row1)
+ * owned and needed: host uint8 arrays of plan->total_tiles entries, or
+ * NULL.  ranks >= 1 and 0 <= rank < ranks, else TDP_ERR_INVALID_ARG.
+ */
+tdp_status tdp_shard_plan(const tdp_plan_t* plan, int32_t ranks, int32_t rank, int32_t* row0,
+                          int32_t* row1, uint8_t* owned, uint8_t* needed);
+
+/*
+ * tdp_blend_slab -- step 5 restricted to output rows [row0, row1).
+ *
+ * Source: as tdp_blend; the slab split is the reading of tdp_shard_plan.
+ *   out[b, c, f, h - row0, w] = the tdp_blend sum at (b, c, f, h, w),
+ *                               row0 <= h < row1
+ * with the same fp32 weights, grouping and order as tdp_blend, so that the
+ * slab equals those rows of tdp_blend bit for bit.
+ * tiles: device, packed as for tdp_blend (tdp_tiles_numel elements of
+ *        `in_dtype`); only the tiles whose rows meet [row0, row1) are read,
+ *        the others may hold anything.
+ * out:   device [B, C, F, row1 - row0, W] of `out_dtype`, every element
+ *        written.
+ * 0 <= row0 <= row1 <= H, else TDP_ERR_INVALID_ARG; row0 == row1 is a
+ * no-op.  Asynchronous on `stream`.
+ */
+tdp_status tdp_blend_slab(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_dtype,
+                          const void* tiles, int32_t row0, int32_t row1, tdp_dtype out_dtype, void* out,
+                          cudaStream_t stream);
+
+/*
  * tdp_extract_tokens -- step 2 into token-major tiles.
  *
  * Source: "Tiled Data Parallelism (TDP)", What it is and When to use it

@@ -1859,6 +1859,54 @@ __global__ void __launch_bounds__(kThreads) cond_count_kernel(const unsigned cha
     weight[i] = c ? 1.0f / static_cast<float>(c) : 0.0f;
 }
 
+// =================================================================== slab blend
+// Output rows [row0, row1) of the blend, one element per thread (grid
+// stride), for the sharded blend: per covering (frame tile, row tile) pair,
+// in order, inner = sum over the covering column tiles, in order, of
+// fmaf(r_w, value, inner), then acc = fmaf(r_f * r_h (rounded), inner,
+// acc) -- the grouping and order of every blend kernel, so the slab equals
+// those rows of the full blend bit for bit.  Only tiles meeting the slab's
+// rows are read.
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kThreads) blend_slab_kernel(const __grid_constant__ tdp_plan_t p, const Tin* tiles,
+                                                              int BC, int row0, int row1, Tout* out) {
+    pdl_launch_dependents();
+    pdl_wait();   // the tiles may come from the previous kernel
+    const int F = p.dims[0], W = p.dims[2], R = row1 - row0;
+    const long long n = (long long)BC * F * R * W;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int w = static_cast<int>(e % W);
+        long long q = e / W;
+        const int h = row0 + static_cast<int>(q % R);
+        q /= R;
+        const int f = static_cast<int>(q % F);
+        const long long bc = q / F;
+        int flo, fhi, hlo, hhi, wlo, whi;
+        tdp::axis_cover(p, 0, f, flo, fhi);
+        tdp::axis_cover(p, 1, h, hlo, hhi);
+        tdp::axis_cover(p, 2, w, wlo, whi);
+        float acc = 0.0f;
+        for (int i_f = flo; i_f <= fhi; ++i_f) {
+            const float rf = tdp::axis_weight(p, 0, i_f, f);
+            const int sf = tdp::tile_size(p, 0, i_f), zf = f - p.start[0][i_f];
+            for (int i_h = hlo; i_h <= hhi; ++i_h) {
+                const float wfh = __fmul_rn(rf, tdp::axis_weight(p, 1, i_h, h));
+                const int sh = tdp::tile_size(p, 1, i_h), y = h - p.start[1][i_h];
+                float inner = 0.0f;
+                for (int i_w = wlo; i_w <= whi; ++i_w) {
+                    const int sw = tdp::tile_size(p, 2, i_w);
+                    const long long off = (long long)BC * tdp::tile_prefix_volume(p, i_f, i_h, i_w) +
+                                          ((bc * sf + zf) * sh + y) * sw + (w - p.start[2][i_w]);
+                    inner = fmaf(tdp::axis_weight(p, 2, i_w, w), to_f32(tiles[off]), inner);
+                }
+                acc = fmaf(wfh, inner, acc);
+            }
+        }
+        out[e] = from_f32<Tout>(acc);
+    }
+}
+
 // =================================================================== K6: conditioning combine
 // out[b, m, :] = sum over tiles t keeping token m (slot_of[t, b, m] >= 0),
 // in increasing t, of weight[b, m] * tile_out[t, b, slot, :]: the 1/k blend
@@ -2332,6 +2380,30 @@ tdp_status tdp_blend(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_
     if (in_dtype == TDP_F32 && out_dtype == TDP_BF16)
         return launch_blend<float, __nv_bfloat16>(*plan, BC, tiles, n, out, stream);
     return launch_blend<float, float>(*plan, BC, tiles, n, out, stream);
+}
+
+tdp_status tdp_blend_slab(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_dtype, const void* tiles,
+                          int32_t row0, int32_t row1, tdp_dtype out_dtype, void* out, cudaStream_t stream) {
+    if (!tdp::plan_is_valid(plan) || B < 0 || C < 0) return TDP_ERR_INVALID_ARG;
+    if (!dtype_size(in_dtype) || !dtype_size(out_dtype)) return TDP_ERR_INVALID_ARG;
+    if (row0 < 0 || row1 < row0 || row1 > plan->dims[1]) return TDP_ERR_INVALID_ARG;
+    if (B == 0 || C == 0 || row0 == row1) return TDP_OK;
+    if (!tiles || !out) return TDP_ERR_INVALID_ARG;
+    if (!aligned16(tiles) || !aligned16(out)) return TDP_ERR_ALIGNMENT;
+    if ((long long)B * C > INT_MAX) return TDP_ERR_INVALID_ARG;
+    const int BC = B * C;
+    const long long n = (long long)BC * plan->dims[0] * (row1 - row0) * plan->dims[2];
+    const long long blocks = std::min<long long>((n + kThreads - 1) / kThreads, 8LL * std::max(1, sm_count()));
+    auto go = [&](auto tin, auto tout) {
+        using Ti = decltype(tin);
+        using To = decltype(tout);
+        return launch(blend_slab_kernel<Ti, To>, blocks, kThreads, 0, stream, 1, *plan, static_cast<const Ti*>(tiles),
+                      BC, row0, row1, static_cast<To*>(out));
+    };
+    if (in_dtype == TDP_BF16 && out_dtype == TDP_BF16) return go(__nv_bfloat16(), __nv_bfloat16());
+    if (in_dtype == TDP_BF16 && out_dtype == TDP_F32) return go(__nv_bfloat16(), 0.0f);
+    if (in_dtype == TDP_F32 && out_dtype == TDP_BF16) return go(0.0f, __nv_bfloat16());
+    return go(0.0f, 0.0f);
 }
 
 tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum_out, cudaStream_t stream) {

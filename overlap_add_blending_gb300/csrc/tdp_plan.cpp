@@ -149,6 +149,25 @@ tdp_status tdp_tile_box(const tdp_plan_t* plan, int32_t t, int32_t start[3], int
     return TDP_OK;
 }
 
+// Slab r of R: rows [floor(r H / R), floor((r + 1) H / R)); tiles owned
+// round robin; a tile is needed where its rows meet the slab.
+tdp_status tdp_shard_plan(const tdp_plan_t* plan, int32_t ranks, int32_t rank, int32_t* row0,
+                          int32_t* row1, uint8_t* owned, uint8_t* needed) {
+    if (!tdp::plan_is_valid(plan) || ranks < 1 || rank < 0 || rank >= ranks) return TDP_ERR_INVALID_ARG;
+    const tdp_plan_t& p = *plan;
+    const int64_t H = p.dims[1];
+    const int r0 = static_cast<int>(H * rank / ranks), r1 = static_cast<int>(H * (rank + 1) / ranks);
+    if (row0) *row0 = r0;
+    if (row1) *row1 = r1;
+    for (int t = 0; t < p.total_tiles; ++t) {
+        int i_f, i_h, i_w;
+        tdp::tile_coords(p, t, i_f, i_h, i_w);
+        if (owned) owned[t] = (t % ranks == rank) ? 1 : 0;
+        if (needed) needed[t] = (r0 < r1 && p.start[1][i_h] < r1 && p.end[1][i_h] > r0) ? 1 : 0;
+    }
+    return TDP_OK;
+}
+
 tdp_status tdp_plan_stats(const tdp_plan_t* plan, int32_t ranks, double* decoded_area,
                           int32_t* seams, double* tile_fraction, double* imbalance,
                           double* max_window_sum) {

@@ -115,6 +115,12 @@ _lib.tdp_extract.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int, C.c_void_p
 _lib.tdp_extract.restype = C.c_int
 _lib.tdp_blend.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]
 _lib.tdp_blend.restype = C.c_int
+_lib.tdp_shard_plan.argtypes = [_P(Plan), C.c_int32, C.c_int32, _P(C.c_int32), _P(C.c_int32), C.c_void_p,
+                                C.c_void_p]
+_lib.tdp_shard_plan.restype = C.c_int
+_lib.tdp_blend_slab.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_int32, C.c_int32, C.c_int,
+                                C.c_void_p, C.c_void_p]
+_lib.tdp_blend_slab.restype = C.c_int
 _lib.tdp_extract_tokens.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p]
 _lib.tdp_extract_tokens.restype = C.c_int
 _lib.tdp_blend_tokens.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_int, C.c_void_p,
@@ -171,6 +177,7 @@ if _lib.tdp_plan_struct_size() != C.sizeof(Plan):
 EXPORTS = ("tdp_plan", "tdp_tile_offset", "tdp_tiles_numel", "tdp_tile_box", "tdp_plan_stats",
            "tdp_balanced_tile_split", "tdp_search_layouts",
            "tdp_extract", "tdp_positions", "tdp_cond_select", "tdp_tokens", "tdp_cond_combine", "tdp_blend",
+           "tdp_shard_plan", "tdp_blend_slab",
            "tdp_extract_tokens", "tdp_blend_tokens", "tdp_window_sum",
            "tdp_launch_geometry", "tdp_device_error", "tdp_status_str", "tdp_last_cuda_error",
            "tdp_plan_struct_size")
@@ -312,6 +319,40 @@ def blend(p: Plan, tiles: torch.Tensor, B: int, C_: int, out: Optional[torch.Ten
         raise ValueError("out has the wrong shape")
     _check(_lib.tdp_blend(C.byref(p), B, C_, _dtype_code(tiles.dtype), _dev(tiles, "tiles"),
                           _dtype_code(out.dtype), _dev(out, "out"), _stream(stream)), "tdp_blend")
+    return out
+
+
+@dataclass
+class Shard:
+    row0: int
+    row1: int
+    owned: Tuple[int, ...]      # tiles this rank owns (t mod ranks == rank)
+    needed: Tuple[int, ...]     # tiles whose rows meet the rank's slab
+
+
+def shard_plan(p: Plan, ranks: int, rank: int) -> Shard:
+    """tdp_shard_plan: rank `rank`'s output slab and its owned / needed tiles."""
+    r0, r1 = C.c_int32(), C.c_int32()
+    owned = (C.c_uint8 * max(1, p.T))()
+    needed = (C.c_uint8 * max(1, p.T))()
+    _check(_lib.tdp_shard_plan(C.byref(p), ranks, rank, C.byref(r0), C.byref(r1), owned, needed), "tdp_shard_plan")
+    return Shard(r0.value, r1.value, tuple(t for t in range(p.T) if owned[t]),
+                 tuple(t for t in range(p.T) if needed[t]))
+
+
+def blend_slab(p: Plan, tiles: torch.Tensor, B: int, C_: int, row0: int, row1: int,
+               out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
+               stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """tdp_blend_slab: packed tiles -> rows [row0, row1) of the blend, [B, C, F, row1-row0, W]."""
+    if tiles.numel() != p.tiles_numel(B, C_):
+        raise ValueError("tiles has the wrong number of elements for this plan and batch")
+    shape = (B, C_, p.dims[0], row1 - row0, p.dims[2])
+    if out is None:
+        out = torch.empty(shape, dtype=out_dtype or tiles.dtype, device=tiles.device)
+    if tuple(out.shape) != shape:
+        raise ValueError("out has the wrong shape")
+    _check(_lib.tdp_blend_slab(C.byref(p), B, C_, _dtype_code(tiles.dtype), _dev(tiles, "tiles"), row0, row1,
+                               _dtype_code(out.dtype), _dev(out, "out"), _stream(stream)), "tdp_blend_slab")
     return out
 
 
