@@ -477,8 +477,16 @@ tdp_status tdp_launch_geometry(const tdp_plan_t* plan, int32_t B, int32_t C, int
                                int32_t* cta_start, int32_t cta_start_len, void* tables, int32_t tables_bytes,
                                int32_t* table_offsets);
 
-/* Diagnostic word of the current device: nonzero when a kernel gave up
- * waiting for its staged copies (bounded wait) and skipped its work.
+/* Diagnostic word of the current device, an OR of
+ *   1  an extract kernel gave up waiting for its staged copies (bounded
+ *      wait, about 1 s) and skipped its work: its output is incomplete;
+ *   2  a blend kernel gave up likewise;
+ *   4  after such a give-up, copies the kernel had issued did not land
+ *      within a second bounded wait before it exited: they may still write
+ *      into shared memory that a later kernel owns, so no later output on
+ *      the device can be trusted;
+ *   8  (debug builds only, TDP_DEBUG_CHECKS) an index check of a global or
+ *      shared access failed; the access was skipped.
  * Reads it synchronously into *code and, when `clear` is nonzero, resets
  * it.  Returns TDP_ERR_CUDA if the read fails. */
 tdp_status tdp_device_error(uint32_t* code, int32_t clear);

@@ -45,8 +45,18 @@ constexpr int kCluster = 8;                  // CTAs cooperating on one tile's t
 constexpr uint64_t kWaitNs = 1000ull * 1000 * 1000;  // give up on staged copies after 1 s
 constexpr uint32_t kSuspendHintNs = 20000;           // a polling thread sleeps up to 20 us per try
 constexpr uint32_t kBackoffNs = 200;                 // sleep between polls of a waiter off the critical path
-constexpr uint32_t kErrExtractWait = 1u;
-constexpr uint32_t kErrBlendWait = 2u;
+// Bits of the device error word (tdp_device_error).
+constexpr uint32_t kErrExtractWait = 1u;   // an extract kernel gave up waiting for its staged copies
+constexpr uint32_t kErrBlendWait = 2u;     // a blend kernel gave up waiting
+constexpr uint32_t kErrDrain = 4u;         // copies still in flight after a give-up did not land in time
+constexpr uint32_t kErrIndex = 8u;         // (debug builds) an index check failed; the access was skipped
+
+// Debug builds (TDP_DEBUG_CHECKS=1) check the global and shared indices of
+// the hot kernels' accesses; release builds compile the checks away.
+#ifndef TDP_DEBUG_CHECKS
+#define TDP_DEBUG_CHECKS 0
+#endif
+constexpr bool kDebugChecks = TDP_DEBUG_CHECKS != 0;
 constexpr int kExtractStages = 3;               // staged bands per extract CTA (2 in flight)
 constexpr int kExtractSmemBudget = 64 * 1024;   // staged bands + slot table
 constexpr int kBlendSmemBudget = 64 * 1024;     // ring of staged tile rows + tables (3 CTAs per SM)
@@ -57,6 +67,28 @@ constexpr int kBlendConsumers = 256;            // blend threads that compute (8
 constexpr int kBlendThreads = kBlendConsumers + 32;   // + one producer warp
 
 __device__ unsigned int g_device_error = 0;
+
+// Debug builds: records a failed index check (kErrIndex) and tells the
+// caller to skip the access.  Release builds: always false, no code.
+__device__ __forceinline__ bool index_bad(bool bad) {
+    if constexpr (kDebugChecks) {
+        if (bad) {
+            atomicOr(&g_device_error, kErrIndex);
+            return true;
+        }
+    }
+    return false;
+}
+
+// Debug builds: a byte range outside [lo, hi) of some buffer.
+__device__ __forceinline__ bool range_bad(const void* p, long long bytes, const void* lo, long long size) {
+    if constexpr (kDebugChecks) {
+        const char* a = static_cast<const char*>(p);
+        const char* b = static_cast<const char*>(lo);
+        return index_bad(bytes < 0 || a < b || a + bytes > b + size);
+    }
+    return false;
+}
 
 thread_local int t_last_cuda_error = 0;
 
@@ -237,17 +269,34 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 // the compiler may treat the asm as touching no memory and move it across
 // ordinary C++ stores to shared memory (tables a thread writes and then
 // reads back), which volatile alone does not forbid.
+extern __shared__ __align__(16) unsigned char tdp_dynamic_smem[];   // the CTA's dynamic shared memory
+
+// Debug builds: a shared-window byte range outside the CTA's dynamic shared
+// memory (every table and stage the kernels read by address lives there).
+__device__ __forceinline__ bool smem_addr_bad(uint32_t addr, uint32_t bytes) {
+    if constexpr (kDebugChecks) {
+        uint32_t size;
+        asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(size));
+        const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(tdp_dynamic_smem));
+        return index_bad(addr < base || addr + bytes > base + size);
+    }
+    return false;
+}
+
 __device__ __forceinline__ int lds_s32(uint32_t addr) {
+    if (smem_addr_bad(addr, 4)) return 0;
     int v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
 __device__ __forceinline__ float lds_f32(uint32_t addr) {
+    if (smem_addr_bad(addr, 4)) return 0.0f;
     float v;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    if (smem_addr_bad(addr, 2)) return 0u;
     unsigned short v;
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
     return v;
@@ -352,6 +401,7 @@ struct ExtractArgs {
     const void* latent;
     void* tiles;
     long long latent_numel;
+    long long tiles_numel;
     int BC;          // B * C
     int band_rows;
     int nbands;
@@ -373,7 +423,10 @@ __device__ __forceinline__ int small_div(int e, float inv_sw) {
 // 32 elements for 4-byte types, tracking the source index incrementally.
 template <typename E>
 __device__ __forceinline__ void extract_copy_slot_warp(E* __restrict__ dst, const E* __restrict__ src,
-                                                       const ExtractSlot& e, int W, int lane) {
+                                                       const ExtractSlot& e, int W, int lane, const E* tiles_lo,
+                                                       long long tiles_n) {
+    // (debug builds) every store of the slot stays inside the tile buffer
+    auto bad = [&](const void* q, int bytes) { return range_bad(q, bytes, tiles_lo, tiles_n * (long long)sizeof(E)); };
     const int sw = e.sw;
     const int len = e.rows * sw;
     const int wrap = W - sw;
@@ -381,10 +434,10 @@ __device__ __forceinline__ void extract_copy_slot_warp(E* __restrict__ dst, cons
         const int head = static_cast<int>((reinterpret_cast<uintptr_t>(dst) >> 1) & 1);  // odd start
         const int body = len - head;
         const int npairs = body >> 1;
-        if (lane == 0 && head) dst[0] = src[0];
+        if (lane == 0 && head && !bad(dst, 2)) dst[0] = src[0];
         if (lane == 31 && (body & 1)) {
             const int last = len - 1, row = last / sw;
-            dst[last] = src[row * W + (last - row * sw)];
+            if (!bad(dst + last, 2)) dst[last] = src[row * W + (last - row * sw)];
         }
         const int e0 = head + 2 * lane;
         const int r0 = small_div(e0, e.inv_sw);
@@ -418,6 +471,7 @@ __device__ __forceinline__ void extract_copy_slot_warp(E* __restrict__ dst, cons
             x3 = x2; a3 = a2;
             advance(x3, a3);
             const uint32_t w0 = pair(x, sa), w1 = pair(x1, a1), w2 = pair(x2, a2), w3 = pair(x3, a3);
+            if (kDebugChecks && (bad(dp, 4) || bad(dp + 96, 4))) return;
             dp[0] = w0;
             dp[32] = w1;
             dp[64] = w2;
@@ -429,6 +483,7 @@ __device__ __forceinline__ void extract_copy_slot_warp(E* __restrict__ dst, cons
         }
 #pragma unroll 1
         for (; it < nit; ++it) {
+            if (bad(dp, 4)) return;
             *dp = pair(x, sa);
             dp += 32;
             advance(x, sa);
@@ -441,6 +496,7 @@ __device__ __forceinline__ void extract_copy_slot_warp(E* __restrict__ dst, cons
         const int step = dq * W + dr;
 #pragma unroll 4
         for (int j = lane; j < len; j += 32) {
+            if (bad(dst + j, 4) || index_bad(a < 0)) return;
             dst[j] = src[a];
             x += dr;
             a += step;
@@ -539,14 +595,16 @@ __global__ void __launch_bounds__(kThreads, 5) extract_kernel(const __grid_const
         if (!cta_wait(&bar[s], (k / S) & 1)) {
             if (threadIdx.x == 0) {  // let every issued copy land before the CTA exits
                 atomicOr(&g_device_error, kErrExtractWait);
-                for (int j = k; j < k + S && first + j < last; ++j) mbar_wait_bounded(&bar[j % S], (j / S) & 1);
+                for (int j = k; j < k + S && first + j < last; ++j)
+                    if (!mbar_wait_bounded(&bar[j % S], (j / S) & 1)) atomicOr(&g_device_error, kErrDrain);
             }
             return;
         }
         const E* band = stage0 + s * stage_elems + shift;
         for (int sl = warp; sl < nslots; sl += nwarps) {
             const ExtractSlot e = slots[sl];
-            extract_copy_slot_warp<E>(tiles + e.dst0 + (long long)cur.bc * e.vol, band + e.src, e, W, lane);
+            extract_copy_slot_warp<E>(tiles + e.dst0 + (long long)cur.bc * e.vol, band + e.src, e, W, lane, tiles,
+                                      a.tiles_numel);
         }
         __syncthreads();  // stage s is free again; the slot table may be rebuilt
     }
@@ -1022,7 +1080,9 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
         if (!ok) {
             // a consumer stopped: let every issued copy land, then leave
             if (lane == 0) atomicOr(&g_device_error, kErrBlendWait);
-            for (int j = kfree; j < kst; ++j) mbar_wait_bounded(&full[j % kBlendQueue], (j / kBlendQueue) & 1);
+            for (int j = kfree; j < kst; ++j)
+                if (!mbar_wait_bounded(&full[j % kBlendQueue], (j / kBlendQueue) & 1) && lane == 0)
+                    atomicOr(&g_device_error, kErrDrain);
         }
         return;
     }
@@ -1187,6 +1247,13 @@ __global__ void __launch_bounds__(kBlendThreads, 3) blend_fast_kernel(const __gr
                 const Run R = runs[ri];
                 const int r = max(R.r0, rb0), r1 = min(R.r1, rb1);
                 if (r >= r1) continue;
+                if constexpr (kDebugChecks) {
+                    // the run's stores are affine in the row: its first and last row bound them all
+                    const long long out_bytes = (long long)a.BC * F * H * W * (long long)sizeof(Tout);
+                    if (range_bad(dcol + (long long)r * W, U * (int)sizeof(Tout), out, out_bytes) ||
+                        range_bad(dcol + (long long)(r1 - 1) * W, U * (int)sizeof(Tout), out, out_bytes))
+                        continue;
+                }
                 if (R.nc == 1) {
                     if (R.ones) {
                         if constexpr (sizeof(Tin) == sizeof(Tout)) {
@@ -1278,7 +1345,7 @@ __global__ void __launch_bounds__(kThreads) blend_generic_kernel(const __grid_co
     if (!cta_wait(bar, 0)) {
         if (threadIdx.x == 0) {
             atomicOr(&g_device_error, kErrBlendWait);
-            mbar_wait_bounded(bar, 0);
+            if (!mbar_wait_bounded(bar, 0)) atomicOr(&g_device_error, kErrDrain);
         }
         return;
     }
@@ -1869,7 +1936,8 @@ __global__ void __launch_bounds__(kThreads) cond_count_kernel(const unsigned cha
 // rows are read.
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(kThreads) blend_slab_kernel(const __grid_constant__ tdp_plan_t p, const Tin* tiles,
-                                                              int BC, int row0, int row1, Tout* out) {
+                                                              long long tiles_numel, int BC, int row0, int row1,
+                                                              Tout* out) {
     pdl_launch_dependents();
     pdl_wait();   // the tiles may come from the previous kernel
     const int F = p.dims[0], W = p.dims[2], R = row1 - row0;
@@ -1898,6 +1966,7 @@ __global__ void __launch_bounds__(kThreads) blend_slab_kernel(const __grid_const
                     const int sw = tdp::tile_size(p, 2, i_w);
                     const long long off = (long long)BC * tdp::tile_prefix_volume(p, i_f, i_h, i_w) +
                                           ((bc * sf + zf) * sh + y) * sw + (w - p.start[2][i_w]);
+                    if (index_bad(off < 0 || off >= tiles_numel)) continue;
                     inner = fmaf(tdp::axis_weight(p, 2, i_w, w), to_f32(tiles[off]), inner);
                 }
                 acc = fmaf(wfh, inner, acc);
@@ -2351,7 +2420,8 @@ tdp_status tdp_extract(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype d
     const int nbands = (p.dims[1] + band_rows - 1) / band_rows;
     const long long items = (long long)B * C * p.dims[0] * nbands;
     if (items > INT_MAX || (long long)B * C > INT_MAX) return TDP_ERR_INVALID_ARG;
-    ExtractArgs a{latent, tiles, (long long)B * C * p.dims[0] * p.dims[1] * p.dims[2], B * C, band_rows, nbands,
+    ExtractArgs a{latent, tiles, (long long)B * C * p.dims[0] * p.dims[1] * p.dims[2],
+                  (long long)B * C * tdp::total_volume(p), B * C, band_rows, nbands,
                   static_cast<int>(items), L.off_slots, L.off_data, L.stage_bytes};
     auto go = [&](auto kernel) -> tdp_status {
         tdp_status st = set_smem(kernel, L.total);
@@ -2398,7 +2468,7 @@ tdp_status tdp_blend_slab(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtyp
         using Ti = decltype(tin);
         using To = decltype(tout);
         return launch(blend_slab_kernel<Ti, To>, blocks, kThreads, 0, stream, 1, *plan, static_cast<const Ti*>(tiles),
-                      BC, row0, row1, static_cast<To*>(out));
+                      (long long)BC * tdp::total_volume(*plan), BC, row0, row1, static_cast<To*>(out));
     };
     if (in_dtype == TDP_BF16 && out_dtype == TDP_BF16) return go(__nv_bfloat16(), __nv_bfloat16());
     if (in_dtype == TDP_BF16 && out_dtype == TDP_F32) return go(__nv_bfloat16(), 0.0f);

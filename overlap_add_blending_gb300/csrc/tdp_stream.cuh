@@ -39,7 +39,6 @@ constexpr int kStreamExtractWarps = 24;   // compute warps; one more warp stages
 constexpr int kStreamBlendWarps = 16;
 constexpr int kStreamExtractThreads = 32 * (kStreamExtractWarps + 1);
 constexpr int kStreamBlendThreads = 32 * (kStreamBlendWarps + 1);
-constexpr uint32_t kErrDrain = 4u;          // copies still in flight after a timeout did not land in time
 constexpr int kStreamMaxStageRuns = 64;     // blend: runs per stage, two per producer lane
 
 constexpr int kStreamMaxStages = 8;
@@ -118,6 +117,7 @@ struct StreamArgs {
     const void* src;          // extract: latent; blend: packed tiles
     void* dst;                // extract: packed tiles; blend: latent
     long long src_bytes;      // size of the source buffer (blend: its last 16-byte chunk may be partial)
+    long long dst_bytes;      // size of the destination buffer (index checks of debug builds)
     int F, H, W, nw;          // latent frames, rows, columns; column tiles
     int BC, band_rows, nbands, n_units;
     int nstages, stage_bytes;
@@ -288,9 +288,11 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
             const BandEnt b = m.bands[cs.band];
             const uint32_t bytes = static_cast<uint32_t>((b.hb1 - b.hb0) * W * esz);
             const unsigned char* g = lat + (((long long)cs.bc * F + cs.f) * H + b.hb0) * (long long)W * esz;
+            const bool in = !range_bad(g, bytes, a.src, a.src_bytes) &&
+                            !index_bad(static_cast<int>(bytes) > a.stage_bytes - 2 * kStreamPad);
             fence_proxy_async();   // the compute warps' reads of this stage come before the copy's writes
-            mbar_arrive_expect_tx(&m.full[s], bytes);
-            bulk_copy_g2s(smem + a.off_data + s * a.stage_bytes + kStreamPad, g, bytes, &m.full[s]);
+            mbar_arrive_expect_tx(&m.full[s], in ? bytes : 0u);
+            if (in) bulk_copy_g2s(smem + a.off_data + s * a.stage_bytes + kStreamPad, g, bytes, &m.full[s]);
         }
         if (!ok) {
             atomicOr(&g_device_error, kErrExtractWait);
@@ -315,6 +317,7 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
         const int nr = b.NHB * nw, nspans = fe.n * nr;
         const RunEnt* band_runs = m.runs + c.band * a.runs_per_band;
         const uint32_t band_off = static_cast<uint32_t>(a.off_data + s * a.stage_bytes + kStreamPad);
+        const uint32_t band_end = band_off + static_cast<uint32_t>((b.hb1 - b.hb0) * W * esz);   // (index checks)
         int spn = warp - rot;
         if (spn < 0) spn += kWarps;
         rot = (rot + nspans) % kWarps;
@@ -348,6 +351,13 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
                     // first one past the tile row on, W - w_t columns further
                     const int k1 = sw - x;
                     uint2 v;
+                    if constexpr (kDebugChecks) {
+                        // the group's loads rise from ad to its last element's; its store is 8 bytes
+                        const uint32_t last = ad + static_cast<uint32_t>((EPQ - 1) * esz) + (k1 <= EPQ - 1 ? wrap : 0u);
+                        if (index_bad(ad < band_off || last + esz > band_end) ||
+                            range_bad(dst, 8, tiles, a.dst_bytes))
+                            break;
+                    }
                     if constexpr (esz == 2) {
                         const uint32_t e0 = *reinterpret_cast<const uint16_t*>(smem + ad);
                         const uint32_t e1 = *reinterpret_cast<const uint16_t*>(smem + ad + 2u + (k1 <= 1 ? wrap : 0u));
@@ -374,7 +384,9 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
             const int eh = lane < 8 ? lane : hd + EPQ * nq + (lane - 8);
             if ((lane < 8 && lane < hd && lane < len) || (lane >= 8 && lane - 8 < tl)) {
                 const int y = small_div(eh, wc.inv_sw), x = eh - y * sw;
-                g0[eh] = *reinterpret_cast<const E*>(smem + src0 + static_cast<uint32_t>((y * W + x) * esz));
+                const uint32_t sa = src0 + static_cast<uint32_t>((y * W + x) * esz);
+                if (!index_bad(sa < band_off || sa + esz > band_end) && !range_bad(g0 + eh, esz, tiles, a.dst_bytes))
+                    g0[eh] = *reinterpret_cast<const E*>(smem + sa);
             }
         }
         __syncwarp();
@@ -441,9 +453,11 @@ __device__ __forceinline__ void col_terms(const ChunkEnt& c, ColTerms<Tin, E, KT
 // inner += r_w * (term q's masked window at shared offset `ad`), per fp32 pair.
 template <typename Tin, int E, int KT>
 __device__ __forceinline__ void add_term(const unsigned char* smem, uint32_t ad, const ColTerms<Tin, E, KT>& t, int q,
-                                         float2 (&inner)[E / 2]) {
+                                         float2 (&inner)[E / 2], uint32_t lo, uint32_t hi) {
     constexpr int esz = static_cast<int>(sizeof(Tin));
     constexpr int NW = ColTerms<Tin, E, KT>::NW;
+    // (debug builds) the window's aligned words inside the ring [lo, hi)
+    if (index_bad((ad & ~3u) < lo || (ad & ~3u) + 4u * (NW + 1) > hi)) return;
     uint32_t w[NW];
     lds_words_at<esz, NW>(smem, ad, w);
 #pragma unroll
@@ -530,6 +544,17 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
                     uintptr_t hi = up <= limit ? up : (g1 & ~uintptr_t(15));   // bulk part; past it, the buffer's tail
                     if (hi < lo) hi = lo;
                     const uint32_t slot = stage_off + static_cast<uint32_t>(r * a.run_slot);
+                    if constexpr (kDebugChecks) {
+                        // the run's slot inside the stage and the table, its bytes inside the tile buffer
+                        const uint32_t stage_end = stage_off + static_cast<uint32_t>(a.stage_bytes - 2 * kStreamPad);
+                        const uintptr_t top = hi > g1 ? hi : g1;   // the bulk part or the plain tail, whichever ends later
+                        if (index_bad(r >= a.max_runs || slot + static_cast<uint32_t>(top - lo) > stage_end) ||
+                            range_bad(reinterpret_cast<const void*>(lo), static_cast<long long>(hi - lo), a.src,
+                                      a.src_bytes) ||
+                            range_bad(reinterpret_cast<const void*>(g0), static_cast<long long>(g1 - g0), a.src,
+                                      a.src_bytes))
+                            continue;
+                    }
                     hdr[r] = static_cast<int>(slot + static_cast<uint32_t>(g0 - lo)) - re.vrow * esz;
                     for (uintptr_t t = (hi > g0 ? hi : g0); t < g1; t += esz)
                         *reinterpret_cast<Tin*>(smem + slot + static_cast<uint32_t>(t - lo)) =
@@ -567,6 +592,8 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
     ColTerms<Tin, E, KT> tm;
     if (active) col_terms<Tin, E, KT>(m.chunks[jc], tm);
     unsigned char* out = static_cast<unsigned char*>(a.dst);
+    const uint32_t ring_lo = static_cast<uint32_t>(a.off_data);   // (index checks) the staged data
+    const uint32_t ring_hi = ring_lo + static_cast<uint32_t>(S * a.stage_bytes);
     UnitCursor c;
     c.init(first, a.BC, a.nbands);
     int j = 0;   // the unit's first stage
@@ -604,18 +631,19 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
 #pragma unroll
                     for (int mm = 0; mm < E / 2; ++mm) inner[mm] = make_float2(0.0f, 0.0f);
                     add_term<Tin, E, KT>(smem, static_cast<uint32_t>(hrun[tm.iw[0]] + yo * tm.swb[0] + tm.xob[0]), tm, 0,
-                                         inner);
+                                         inner, ring_lo, ring_hi);
                     if (KT > 1 && tm.nq > 1)
                         add_term<Tin, E, KT>(smem, static_cast<uint32_t>(hrun[tm.iw[q1]] + yo * tm.swb[q1] + tm.xob[q1]),
-                                             tm, q1, inner);
+                                             tm, q1, inner, ring_lo, ring_hi);
                     if (KT > 2 && tm.nq > 2)
                         add_term<Tin, E, KT>(smem, static_cast<uint32_t>(hrun[tm.iw[q2]] + yo * tm.swb[q2] + tm.xob[q2]),
-                                             tm, q2, inner);
+                                             tm, q2, inner, ring_lo, ring_hi);
                     const float2 w2 = make_float2(wfh, wfh);
 #pragma unroll
                     for (int mm = 0; mm < E / 2; ++mm) acc[mm] = __ffma2_rn(w2, inner[mm], acc[mm]);
                 }
-                store_chunk<Tout, E>(oplane + (long long)h * W * osz, acc);
+                if (!range_bad(oplane + (long long)h * W * osz, 16, out, a.dst_bytes))
+                    store_chunk<Tout, E>(oplane + (long long)h * W * osz, acc);
             }
         }
         __syncwarp();
@@ -993,6 +1021,7 @@ tdp_status launch_extract_stream(const tdp_plan_t& p, int BC, const void* latent
     L.a.src = latent;
     L.a.dst = tiles;
     L.a.src_bytes = (long long)BC * p.dims[0] * p.dims[1] * p.dims[2] * esz;
+    L.a.dst_bytes = (long long)BC * tdp::total_volume(p) * esz;
     *taken = true;
     return launch(extract_stream_kernel<E>, L.grid, kStreamExtractThreads, L.smem, stream, 1, L.a, L.sp, L.tb);
 }
@@ -1012,6 +1041,7 @@ tdp_status launch_blend_stream(const tdp_plan_t& p, int BC, const void* tiles, l
         L.a.src = tiles;
         L.a.dst = out;
         L.a.src_bytes = tiles_numel * isz;
+        L.a.dst_bytes = (long long)BC * p.dims[0] * p.dims[1] * p.dims[2] * osz;
         *taken = true;
         return launch(kernel, L.grid, kStreamBlendThreads, L.smem, stream, 1, L.a, L.sp, L.tb);
     };

@@ -15,9 +15,12 @@ from typing import Optional, Sequence, Tuple
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtdp.so")
+# TDP_DEBUG_CHECKS=1: the build with device index checks (build.py --debug)
+_DEBUG = os.environ.get("TDP_DEBUG_CHECKS") == "1"
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtdp_debug.so" if _DEBUG else "libtdp.so")
 if not os.path.exists(_LIB_PATH):
-    raise ImportError(f"{_LIB_PATH} is missing: build it with `python -m overlap_add_blending_gb300.build`")
+    raise ImportError(f"{_LIB_PATH} is missing: build it with `python -m overlap_add_blending_gb300.build"
+                      f"{' --debug' if _DEBUG else ''}`")
 _lib = C.CDLL(_LIB_PATH)
 
 MAX_PER_AXIS = 64
