@@ -54,7 +54,7 @@ from overlap_add_blending_gb300.workloads import WORKLOADS  # noqa: E402
 WORKLOAD = WORKLOADS["4k"]
 METRIC = "tile extract+blend HBM GB/s (fraction of GB300 peak) and latent elems/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_STEP = 4  # extract, tokens (the per-token count in the same cooperative launch), window sum, blend
+KERNELS_PER_STEP = 5  # extract, tokens (2: per-tile kernel, per-token count), window sum, blend
 
 
 def esz(dtype: str) -> int:

@@ -25,8 +25,6 @@
 #include <climits>
 #include <cstdint>
 #include <cstring>
-#include <map>
-#include <mutex>
 #include <vector>
 
 #include "tdp.h"
@@ -1603,10 +1601,6 @@ struct TokensArgs {
     int* num_kept;
     int* tile_cond;
     int* slot_of;      // [T, B, M]: position in the tile's kept list, or -1 (NULL: not written)
-    // per-token count and weight after a grid-wide barrier (cooperative
-    // launch only; NULL: the count kernel follows instead)
-    int* count;
-    float* weight;
 };
 
 constexpr int kPosCache = 4;   // tokens per thread kept in registers between reduce and write
@@ -1884,26 +1878,6 @@ __global__ void __launch_bounds__(kThreads, 4) tokens_kernel(const __grid_consta
     if (rank == 0 && threadIdx.x == 0 && a.num_kept) a.num_kept[row] = total;   // 0 when M = 0 (rank 0 knows it)
     cluster.barrier_wait();  // no CTA leaves while a peer may read its shared memory
 
-    // Launched cooperatively: once every tile's keep flags are written, the
-    // grid counts the tiles keeping each conditioning token (what the count
-    // kernel otherwise does in a launch of its own).
-    if (a.count) {
-        cg::this_grid().sync();
-        const int BM = a.B * a.M, T = p.total_tiles;
-        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < BM; i += gridDim.x * blockDim.x) {
-            int c = 0, u = 0;
-            for (; u + 16 <= T; u += 16) {   // 16 independent loads in flight
-                int k[16];
-#pragma unroll
-                for (int v = 0; v < 16; ++v) k[v] = a.keep[(long long)(u + v) * BM + i];
-#pragma unroll
-                for (int v = 0; v < 16; ++v) c += k[v];
-            }
-            for (; u < T; ++u) c += a.keep[(long long)u * BM + i];
-            a.count[i] = c;
-            a.weight[i] = c ? 1.0f / static_cast<float>(c) : 0.0f;
-        }
-    }
 }
 
 __global__ void __launch_bounds__(kThreads) cond_count_kernel(const unsigned char* keep, int T, int BM,
@@ -2215,37 +2189,26 @@ tdp_status set_smem(K kernel, int bytes) {
 // its predecessor in the stream finishes; see pdl_wait) and, with
 // cluster > 1, clusters of that many CTAs.
 template <typename K, typename... Args>
-tdp_status launch_ex(K kernel, long long blocks, int threads, int smem, cudaStream_t stream, int cluster,
-                     bool cooperative, Args... args) {
+tdp_status launch(K kernel, long long blocks, int threads, int smem, cudaStream_t stream, int cluster, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[3];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     unsigned n = 1;
     if (cluster > 1) {
-        attr[n].id = cudaLaunchAttributeClusterDimension;
-        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
-        attr[n].val.clusterDim.y = 1;
-        attr[n].val.clusterDim.z = 1;
-        ++n;
-    }
-    if (cooperative) {
-        attr[n].id = cudaLaunchAttributeCooperative;
-        attr[n].val.cooperative = 1;
-        ++n;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n = 2;
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
     return cuda_status(cudaLaunchKernelEx(&cfg, kernel, args...));
-}
-
-template <typename K, typename... Args>
-tdp_status launch(K kernel, long long blocks, int threads, int smem, cudaStream_t stream, int cluster, Args... args) {
-    return launch_ex(kernel, blocks, threads, smem, stream, cluster, false, args...);
 }
 
 template <typename K, typename... Args>
@@ -2500,39 +2463,6 @@ tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum
     return launch(window_sum_kernel, blocks, kThreads, smem, stream, 1, p, max_abs_dev, sum_out, tables);
 }
 
-// CTAs of tokens_kernel that can be resident at once on the current device
-// (whole 8-CTA clusters), or 0 if the device cannot say; queried once per
-// device.
-static long long tokens_coop_capacity() {
-    static std::mutex mu;
-    static std::map<int, long long> cache;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(dev);
-    if (it != cache.end()) return it->second;
-    int coop = 0;
-    long long cap = 0;
-    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(kCluster, 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = kCluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, tokens_kernel, &cfg) == cudaSuccess)
-            cap = (long long)clusters * kCluster;
-    }
-    (void)cudaGetLastError();
-    cache[dev] = cap;
-    return cap;
-}
-
 tdp_status tdp_tokens(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos, int32_t normalize,
                       int32_t* tile_pos, int32_t* offsets, int32_t M, const int32_t* cond_pos,
                       int32_t* tile_extent, uint8_t* keep, int32_t* count, float* weight, int32_t* kept_idx,
@@ -2548,15 +2478,7 @@ tdp_status tdp_tokens(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos,
     const long long blocks = (long long)kCluster * plan->total_tiles * B;
     if (blocks > INT_MAX || (long long)B * M > INT_MAX) return TDP_ERR_INVALID_ARG;
     TokensArgs a{gen_pos, B, normalize ? 1 : 0, tile_pos, offsets, M, cond_pos, tile_extent, keep, kept_idx,
-                 num_kept, tile_cond_pos, slot_of, nullptr, nullptr};
-    if (M > 0 && blocks <= tokens_coop_capacity()) {
-        // every CTA resident at once: the count follows a grid barrier in the same launch
-        TokensArgs ac = a;
-        ac.count = count;
-        ac.weight = weight;
-        if (launch_ex(tokens_kernel, blocks, kThreads, 0, stream, kCluster, true, *plan, ac) == TDP_OK) return TDP_OK;
-        (void)cudaGetLastError();   // refused: the two-launch form below
-    }
+                 num_kept, tile_cond_pos, slot_of};
     tdp_status st = launch_cluster(tokens_kernel, blocks, stream, *plan, a);
     if (st != TDP_OK || M == 0) return st;
     const int BM = B * M;

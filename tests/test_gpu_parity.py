@@ -273,10 +273,6 @@ def test_cond_select_random_gen_positions(T):
 
 
 # ----------------------------------------------------------------- positions + conditioning in one launch
-# "4k" (64 clusters of 8 CTAs) fits the GPU at once, so the per-token count
-# follows a grid barrier in the same launch; "4k_b3" (96 clusters) does not
-# on a 152-SM part (four 64-register CTAs per SM), so the count kernel runs
-# after it.  Both must give the same outputs.
 @pytest.mark.parametrize("case", ["4k", "4k_b3", "ragged", "random", "no_cond", "big_chunks"])
 def test_tokens_matches_separate_calls_and_oracle(T, case):
     if case in ("4k", "4k_b3", "no_cond"):
