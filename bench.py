@@ -469,6 +469,42 @@ def sweep_figures(dev) -> dict:
     return out
 
 
+def run_each_kernel_twice(channels: int) -> int:
+    """Every library kernel twice on the 4K tiling with `channels` channels
+    and nothing else (a short, fixed launch sequence for profiler captures)."""
+    import torch
+    from overlap_add_blending_gb300 import tdp
+    wl = WORKLOAD
+    dev = torch.device("cuda", 0)
+    p = tdp.plan(wl.dims, wl.tiling)
+    X = torch.from_numpy(inputs.latent((1, channels) + wl.dims, seed=0)).to(torch.bfloat16).to(dev)
+    gen = torch.from_numpy(inputs.grid_positions(1, *wl.dims)).to(dev)
+    cond = torch.from_numpy(inputs.cond_positions(1, wl.num_cond, *wl.dims, n_negative=wl.num_cond_negative,
+                                                  seed=2)).to(dev)
+    tiles = torch.empty(p.tiles_numel(1, channels), dtype=torch.bfloat16, device=dev)
+    out = torch.empty_like(X)
+    tm, tmo = torch.empty_like(tiles), torch.empty_like(X)
+    md = torch.empty(4, dtype=torch.float32, device=dev)
+    tok = {}
+    comb_in = torch.randn((p.T, 1, wl.num_cond, 128), device=dev).to(torch.bfloat16)
+    comb_out = torch.empty((1, wl.num_cond, 128), dtype=torch.bfloat16, device=dev)
+    sh = tdp.shard_plan(p, 2, 0)
+    for _ in range(2):
+        tdp.extract(p, X, tiles)
+        tdp.blend(p, tiles, 1, channels, out)
+        tdp.tokens(p, gen, cond, True, True, tok)
+        tdp.window_sum(p, md)
+        tdp.cond_combine(p, comb_in, tok["slot_of"], tok["weight"], out=comb_out)
+        tdp.extract_tokens(p, X, tm)
+        tdp.blend_tokens(p, tm, 1, channels, tmo)
+        tdp.blend_slab(p, tiles, 1, channels, sh.row0, sh.row1)
+    torch.cuda.synchronize()
+    if not (torch.equal(out, X) and torch.equal(tmo, X)) or tdp.device_error() != 0:
+        raise SystemExit("a round trip is not exact or the device error word is set")
+    print("ok")
+    return 0
+
+
 def run_tdp(args, rank: int, world: int):
     import torch
     import torch.distributed as dist
@@ -725,6 +761,8 @@ def main():
     ap.add_argument("--impl", choices=["tdp", "reference"], default="tdp")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' figures")
+    ap.add_argument("--each-kernel-twice", type=int, metavar="C", default=0,
+                    help="only run every kernel twice on the 4K tiling with C channels (profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -732,6 +770,8 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)     # rank 0 alone times the oracle
+    if args.each_kernel_twice:
+        return run_each_kernel_twice(args.each_kernel_twice)
     if world > 1:
         import torch
         import torch.distributed as dist
