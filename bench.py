@@ -55,6 +55,7 @@ WORKLOAD = WORKLOADS["4k"]
 METRIC = "tile extract+blend HBM GB/s (fraction of GB300 peak) and latent elems/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNELS_PER_STEP = 5  # extract, tokens (2: per-tile kernel, per-token count), window sum, blend
+GRAPH_STEPS = 50      # steps (or launches) per captured CUDA graph in the timed loops
 
 
 def esz(dtype: str) -> int:
@@ -366,6 +367,43 @@ def time_b2b(fn, n_sets: int, launches: int, stream, head_s: float, others=()) -
     return a.elapsed_time(b) / launches
 
 
+class GraphLoop:
+    """`calls` back-to-back calls fn(k mod n_sets), captured once in a CUDA
+    graph (launch overhead paid at capture, not per replay).  Streams in
+    `side` join the capture at its start and rejoin it at its end."""
+
+    def __init__(self, fn, n_sets: int, calls: int, side=()):
+        import torch
+        self.calls = calls
+        self.graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            fn(0)                     # first calls outside the capture (lazy set-up)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(self.graph, stream=cap):
+            for o in side:
+                o.wait_stream(cap)
+            for k in range(calls):
+                fn(k % n_sets)
+            for o in side:
+                cap.wait_stream(o)
+        torch.cuda.synchronize()
+
+    def time_ms(self, replays: int, stream) -> float:
+        """Mean ms per call over `replays` replays back to back between two events."""
+        import torch
+        self.graph.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(replays):
+            self.graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (replays * self.calls)
+
+
 def host_rate(fn, n_sets: int, calls: int = 20) -> float:
     """Host seconds per enqueue of fn (sizes the GPU head start)."""
     import torch
@@ -397,7 +435,8 @@ def time_after_flush(fn, flush, stream, reps: int = 20) -> float:
 
 def run_config(name, dev, stream, launches: int) -> dict:
     """extract, blend (and tokens where the workload has conditioning
-    tokens) of one named workload, back to back over rotating sets."""
+    tokens) of one named workload, back to back over rotating sets, replayed
+    from CUDA graphs (and, for extract and blend, also launched one by one)."""
     import torch
     from overlap_add_blending_gb300 import tdp
     wl = WORKLOADS[name]
@@ -419,19 +458,22 @@ def run_config(name, dev, stream, launches: int) -> dict:
             torch.allclose(S.out[S.n - 1], S.X0, rtol=1e-5, atol=1e-5))
     if not same:
         raise SystemExit(f"{name}: the identity round trip does not return the latent")
+    calls = max(GRAPH_STEPS, S.n)   # one graph cycles through every set
+    replays = max(1, -(-launches // calls))
+    e_ms = GraphLoop(ext, S.n, calls).time_ms(replays, stream)
+    b_ms = GraphLoop(bl, S.n, calls).time_ms(replays, stream)
     head = 3 * launches * max(host_rate(ext, S.n), host_rate(bl, S.n))
-    e_ms = time_b2b(ext, S.n, launches, stream, head)
-    b_ms = time_b2b(bl, S.n, launches, stream, head)
+    e_stream = time_b2b(ext, S.n, launches, stream, head)
+    b_stream = time_b2b(bl, S.n, launches, stream, head)
     r = {"workload": f"{wl.dtype} B={wl.B} C={wl.C} (F,H,W)={wl.dims} tiling={wl.tiling}",
          "sets": S.n, "extract_ms": e_ms, "blend_ms": b_ms,
+         "extract_stream_launch_ms": e_stream, "blend_stream_launch_ms": b_stream,
          "extract_gbs": ab["extract"] / (e_ms * 1e-3) / 1e9, "blend_gbs": ab["blend"] / (b_ms * 1e-3) / 1e9,
          "gbs": ab["total"] / ((e_ms + b_ms) * 1e-3) / 1e9,
          "latent_elems_per_s": ab["latent_elems"] / ((e_ms + b_ms) * 1e-3),
          "algorithmic_bytes": ab["total"], "overlap_factor": round(ab["overlap_factor"], 5)}
     if tokens:
-        t_head = 3 * launches * host_rate(tok, S.n)
-        t_ms = time_b2b(tok, S.n, launches, stream, t_head)
-        r["tokens_ms"] = t_ms
+        r["tokens_ms"] = GraphLoop(tok, S.n, calls).time_ms(replays, stream)
         r["num_cond"] = wl.num_cond
     st = tdp.plan_stats(p, 4)
     r["stats"] = {"decoded_area": st.decoded_area, "seams": st.seams, "imbalance_r4": st.imbalance,
@@ -540,7 +582,7 @@ def run_tdp(args, rank: int, world: int):
     def step(i):
         side_work(i)
         tdp.extract(p, S.X[i], S.tiles[i])
-        stream.wait_event(join)
+        torch.cuda.current_stream().wait_event(join)   # the main stream (or the graph's capture stream)
         tdp.blend(p, S.tiles[i], wl.B, wl.C, S.out[i])
 
     for i in range(S.n):
@@ -563,18 +605,18 @@ def run_tdp(args, rank: int, world: int):
     torch.cuda.synchronize()
 
     # The timed region: K steps back to back, step k on set k mod n (no flush:
-    # the sets together are larger than L2), between two events.
-    K = args.steps
+    # the sets together are larger than L2), between two events.  The steps
+    # run as replays of a CUDA graph of GRAPH_STEPS steps (the launch cost is
+    # paid once, at capture), so K is rounded up to a multiple of it.
+    step_graph = GraphLoop(step, S.n, GRAPH_STEPS, side=(side,))
+    replays = max(1, -(-args.steps // GRAPH_STEPS))
+    K = replays * GRAPH_STEPS
     wall0 = time.perf_counter()
-    chunk = 200                      # steps per head start: the sleep covers their enqueue
-    total_ms = 0.0
-    for k0 in range(0, K, chunk):
-        kk = min(chunk, K - k0)
-        total_ms += kk * time_b2b(lambda i, k0=k0: step((k0 + i) % S.n), S.n, kk, stream,
-                                  max(200e-6, 1.5 * kk * enqueue_s), others=(side,))
-    torch.cuda.synchronize()
+    step_ms = step_graph.time_ms(replays, stream)
     wall = time.perf_counter() - wall0
-    step_ms = total_ms / K
+    # the same steps launched one by one from the host, for comparison
+    chunk = 200                      # steps per head start: the sleep covers their enqueue
+    stream_ms = time_b2b(step, S.n, chunk, stream, max(200e-6, 1.5 * chunk * enqueue_s), others=(side,))
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -591,9 +633,10 @@ def run_tdp(args, rank: int, world: int):
         tdp.tokens(p, S.gen[i], S.cond[i], True, True, S.tok[i])
         tdp.window_sum(p, S.maxdev[i])
 
-    kern_ms = {}
+    kern_ms, kern_stream_ms = {}, {}
     for name, fn in (("extract", ext), ("blend", bl), ("tokens_and_window_sum", side_only)):
-        kern_ms[name] = time_b2b(fn, S.n, L, stream, max(200e-6, 3 * L * host_rate(fn, S.n)))
+        kern_ms[name] = GraphLoop(fn, S.n, GRAPH_STEPS).time_ms(max(1, L // GRAPH_STEPS), stream)
+        kern_stream_ms[name] = time_b2b(fn, S.n, L, stream, max(200e-6, 3 * L * host_rate(fn, S.n)))
     single_ms = {"extract": time_after_flush(lambda: ext(0), flush, stream),
                  "blend": time_after_flush(lambda: bl(0), flush, stream)}
 
@@ -702,6 +745,8 @@ def run_tdp(args, rank: int, world: int):
         return 0
     peak, peak_src = read_peak()
     kern = {n: {"ms": float(kern_ms[n])} for n in names}
+    for n in names:
+        kern[n]["stream_launch_ms"] = float(kern_stream_ms[n])
     for n in ("extract", "blend"):
         kern[n]["gbs"] = ab[n] / (kern[n]["ms"] * 1e-3) / 1e9
         kern[n]["single_launch_after_flush_ms"] = single_ms[n]
@@ -723,9 +768,12 @@ def run_tdp(args, rank: int, world: int):
         "algorithmic_bytes": {"extract": ab["extract"], "blend": ab["blend"],
                               "overlap_factor": round(ab["overlap_factor"], 5)},
         "kernels": kern,
-        "kernel_timing": "each kernel alone, back to back over the rotating sets (mean per launch, "
-                         f"{L} launches between two events); single_launch_after_flush: median of 20 launches, "
-                         "each after a 256 MiB write outside its events (includes the launch latency)",
+        "kernel_timing": f"each kernel alone, back to back over the rotating sets, replayed from a CUDA graph of "
+                         f"{GRAPH_STEPS} launches (mean per launch over {max(1, L // GRAPH_STEPS) * GRAPH_STEPS}); "
+                         "stream_launch_ms: the same launched one by one from the host; "
+                         "single_launch_after_flush: median of 20 launches, each after a 256 MiB write outside its "
+                         "events (includes the launch latency)",
+        "step_stream_launch_ms": stream_ms,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src},
         "e2e": {"value": job_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
