@@ -3,10 +3,14 @@
 
 One step is one pass of every step of the path on the 4K-class workload
 (bf16 latent B=1, C=128, F=16, H=68, W=120; tiles 2x4x4 with overlaps
-2/8/12; 256 conditioning tokens, 64 with a negative time start):
-    tdp_tokens (positions and conditioning selection in one launch, plus
-    the per-token count) and tdp_window_sum on a side stream beside
-    tdp_extract, then tdp_blend once both are done.
+2/8/12; 256 conditioning tokens, 64 with a negative time start), in
+three launches:
+    tdp_extract_and_tokens (the tiles, with the partial token extents
+    reduced in the same launch; then a short launch for the positions,
+    the conditioning selection and counts, and the window-sum maximum),
+    then tdp_blend.
+The same step through the separate calls (tdp_tokens and tdp_window_sum on
+a side stream beside tdp_extract, then tdp_blend) is timed beside it.
 The per-tile op between extract and blend is the caller's (here identity,
 outside the path).  Inputs are resident in HBM when the timed region
 starts.  Steps run back to back over rotating device copies of the inputs
@@ -54,7 +58,7 @@ from overlap_add_blending_gb300.workloads import WORKLOADS  # noqa: E402
 WORKLOAD = WORKLOADS["4k"]
 METRIC = "tile extract+blend HBM GB/s (fraction of GB300 peak) and latent elems/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_STEP = 5  # extract, tokens (2: per-tile kernel, per-token count), window sum, blend
+KERNELS_PER_STEP = 3  # extract with the partial extents, the token finish, blend
 GRAPH_STEPS = 50      # steps (or launches) per captured CUDA graph in the timed loops
 
 
@@ -76,9 +80,8 @@ def config_dict(wl, note: str) -> dict:
                         f"W={wl.dims[2]}, tiles (frames {wl.tiling[0][0]}/{wl.tiling[0][1]}, height "
                         f"{wl.tiling[1][0]}/{wl.tiling[1][1]}, width {wl.tiling[2][0]}/{wl.tiling[2][1]}), "
                         f"{wl.num_cond} conditioning tokens ({wl.num_cond_negative} with negative time)",
-            "step": "extract on the main stream, tokens (positions + cond select) and window_sum on a side "
-                    "stream (ordered only by the blend's wait for them), then blend; per-tile op: identity, "
-                    "outside",
+            "step": "tdp_extract_and_tokens (tiles, positions, cond select with counts, window-sum maximum: "
+                    "2 launches), then tdp_blend; per-tile op: identity, outside",
             "l2": note}
 
 
@@ -531,7 +534,12 @@ def run_each_kernel_twice(channels: int) -> int:
     comb_in = torch.randn((p.T, 1, wl.num_cond, 128), device=dev).to(torch.bfloat16)
     comb_out = torch.empty((1, wl.num_cond, 128), dtype=torch.bfloat16, device=dev)
     sh = tdp.shard_plan(p, 2, 0)
+    tok2 = tdp.token_outputs(p, 1, wl.num_cond, dev)
+    out2 = torch.empty_like(X)
+    ws = torch.empty(tdp.extract_and_tokens_workspace(p, 1), dtype=torch.uint8, device=dev)
     for _ in range(2):
+        tdp.extract_and_tokens(p, X, gen, cond, tiles=tiles, tok=tok2, max_dev=md, workspace=ws)
+        tdp.blend(p, tiles, 1, channels, out2)
         tdp.extract(p, X, tiles)
         tdp.blend(p, tiles, 1, channels, out)
         tdp.tokens(p, gen, cond, True, True, tok)
@@ -541,7 +549,7 @@ def run_each_kernel_twice(channels: int) -> int:
         tdp.blend_tokens(p, tm, 1, channels, tmo)
         tdp.blend_slab(p, tiles, 1, channels, sh.row0, sh.row1)
     torch.cuda.synchronize()
-    if not (torch.equal(out, X) and torch.equal(tmo, X)) or tdp.device_error() != 0:
+    if not (torch.equal(out, X) and torch.equal(out2, X) and torch.equal(tmo, X)) or tdp.device_error() != 0:
         raise SystemExit("a round trip is not exact or the device error word is set")
     print("ok")
     return 0
@@ -568,29 +576,39 @@ def run_tdp(args, rank: int, world: int):
     S = Sets(wl, p, dev, dt, tokens=True)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
-    # One step on set i: the token kernels and the window maximum on a side
-    # stream, extract on the main stream, then the blend once the side work
-    # is done (in use, the per-tile model between extract and blend takes the
-    # tiles and the token outputs).  The side kernels read only their own
-    # step's positions, so the side stream is not ordered after the previous
-    # step's kernels: it runs ahead and its kernels overlap the main stream's.
-    def side_work(i):
+    # One step on set i: the tiles, every token output and the window
+    # maximum, then (in use, after the per-tile model, which takes the tiles
+    # and the token outputs) the blend.
+    ws = torch.empty(tdp.extract_and_tokens_workspace(p, wl.B), dtype=torch.uint8, device=dev)
+
+    def step(i):
+        tdp.extract_and_tokens(p, S.X[i], S.gen[i], S.cond[i], tiles=S.tiles[i], tok=S.tok[i], max_dev=S.maxdev[i],
+                               workspace=ws)
+        tdp.blend(p, S.tiles[i], wl.B, wl.C, S.out[i])
+
+    # The same step through the separate calls: the token kernels and the
+    # window maximum on a side stream, extract on the main stream, then the
+    # blend once the side work is done.  The side kernels read only their
+    # own step's positions, so the side stream is not ordered after the
+    # previous step's kernels: it runs ahead and its kernels may overlap the
+    # main stream's.
+    def step_separate(i):
         tdp.tokens(p, S.gen[i], S.cond[i], True, True, S.tok[i], stream=side)
         tdp.window_sum(p, S.maxdev[i], stream=side)
         join.record(side)
-
-    def step(i):
-        side_work(i)
         tdp.extract(p, S.X[i], S.tiles[i])
         torch.cuda.current_stream().wait_event(join)   # the main stream (or the graph's capture stream)
         tdp.blend(p, S.tiles[i], wl.B, wl.C, S.out[i])
 
-    for i in range(S.n):
-        step(i)
-    torch.cuda.synchronize()
-    for i in range(S.n):
-        if not torch.equal(S.out[i], S.X0):
-            raise SystemExit("the identity round trip is not exact")
+    for fn in (step_separate, step):
+        for i in range(S.n):
+            fn(i)
+        torch.cuda.synchronize()
+        for i in range(S.n):
+            if not torch.equal(S.out[i], S.X0):
+                raise SystemExit("the identity round trip is not exact")
+    if tdp.device_error() != 0:
+        raise SystemExit("the device error word is set")
     enqueue_s = host_rate(step, S.n)
 
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
@@ -608,7 +626,7 @@ def run_tdp(args, rank: int, world: int):
     # the sets together are larger than L2), between two events.  The steps
     # run as replays of a CUDA graph of GRAPH_STEPS steps (the launch cost is
     # paid once, at capture), so K is rounded up to a multiple of it.
-    step_graph = GraphLoop(step, S.n, GRAPH_STEPS, side=(side,))
+    step_graph = GraphLoop(step, S.n, GRAPH_STEPS)
     replays = max(1, -(-args.steps // GRAPH_STEPS))
     K = replays * GRAPH_STEPS
     wall0 = time.perf_counter()
@@ -616,7 +634,9 @@ def run_tdp(args, rank: int, world: int):
     wall = time.perf_counter() - wall0
     # the same steps launched one by one from the host, for comparison
     chunk = 200                      # steps per head start: the sleep covers their enqueue
-    stream_ms = time_b2b(step, S.n, chunk, stream, max(200e-6, 1.5 * chunk * enqueue_s), others=(side,))
+    stream_ms = time_b2b(step, S.n, chunk, stream, max(200e-6, 1.5 * chunk * enqueue_s))
+    # the step through the separate calls, timed the same way (fewer steps)
+    sep_ms = GraphLoop(step_separate, S.n, GRAPH_STEPS, side=(side,)).time_ms(max(1, min(replays, 40)), stream)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -629,12 +649,16 @@ def run_tdp(args, rank: int, world: int):
     ext = lambda i: tdp.extract(p, S.X[i], S.tiles[i])
     bl = lambda i: tdp.blend(p, S.tiles[i], wl.B, wl.C, S.out[i])
 
+    ext_tok = lambda i: tdp.extract_and_tokens(p, S.X[i], S.gen[i], S.cond[i], tiles=S.tiles[i], tok=S.tok[i],
+                                               max_dev=S.maxdev[i], workspace=ws)
+
     def side_only(i):
         tdp.tokens(p, S.gen[i], S.cond[i], True, True, S.tok[i])
         tdp.window_sum(p, S.maxdev[i])
 
     kern_ms, kern_stream_ms = {}, {}
-    for name, fn in (("extract", ext), ("blend", bl), ("tokens_and_window_sum", side_only)):
+    for name, fn in (("extract", ext), ("blend", bl), ("extract_and_tokens", ext_tok),
+                     ("tokens_and_window_sum", side_only)):
         kern_ms[name] = GraphLoop(fn, S.n, GRAPH_STEPS).time_ms(max(1, L // GRAPH_STEPS), stream)
         kern_stream_ms[name] = time_b2b(fn, S.n, L, stream, max(200e-6, 3 * L * host_rate(fn, S.n)))
     single_ms = {"extract": time_after_flush(lambda: ext(0), flush, stream),
@@ -698,7 +722,6 @@ def run_tdp(args, rank: int, world: int):
             S.cond[i].copy_(cond_h, non_blocking=True)
         in_ready[i].record(up)
         stream.wait_event(in_ready[i])
-        side.wait_event(in_ready[i])
         stream.wait_event(out_free[i])
         step(i)
         in_free[i].record(stream)
@@ -717,7 +740,6 @@ def run_tdp(args, rank: int, world: int):
     with torch.cuda.stream(up):
         torch.cuda._sleep(int(max(200e-6, 1.5 * min(K, 200) * enqueue_s) * 2.0e9))
     t_first.record(up)
-    side.wait_event(t_first)
     for k in range(K):
         e2e_step(k)
     down.wait_stream(stream)
@@ -736,10 +758,10 @@ def run_tdp(args, rank: int, world: int):
             configs[name] = run_config(name, dev, stream, launches=100)
         configs["sweep"] = sweep_figures(dev)
 
-    names = ["extract", "blend", "tokens_and_window_sum"]
-    mx, job_bytes = combine([step_ms, e2e_ms] + [kern_ms[n] for n in names], ab["total"], device=dev)
-    step_ms, e2e_ms = mx[0], mx[1]
-    kern_ms = dict(zip(names, mx[2:]))
+    names = ["extract", "blend", "extract_and_tokens", "tokens_and_window_sum"]
+    mx, job_bytes = combine([step_ms, e2e_ms, sep_ms] + [kern_ms[n] for n in names], ab["total"], device=dev)
+    step_ms, e2e_ms, sep_ms = mx[0], mx[1], mx[2]
+    kern_ms = dict(zip(names, mx[3:]))
 
     if rank != 0:
         return 0
@@ -751,6 +773,7 @@ def run_tdp(args, rank: int, world: int):
         kern[n]["gbs"] = ab[n] / (kern[n]["ms"] * 1e-3) / 1e9
         kern[n]["single_launch_after_flush_ms"] = single_ms[n]
         kern[n]["single_launch_after_flush_gbs"] = ab[n] / (single_ms[n] * 1e-3) / 1e9
+    kern["extract_and_tokens"]["gbs"] = ab["extract"] / (kern["extract_and_tokens"]["ms"] * 1e-3) / 1e9
     dom = "blend" if kern["blend"]["ms"] >= kern["extract"]["ms"] else "extract"
     achieved = kern[dom]["gbs"]
     traffic = recorded_traffic(dom)
@@ -765,14 +788,18 @@ def run_tdp(args, rank: int, world: int):
                                   f"flush inside the timed region"),
         "latent_elems_per_s": world * ab["latent_elems"] / (step_ms * 1e-3),
         "extract_blend_gbs": ab["total"] / ((kern["extract"]["ms"] + kern["blend"]["ms"]) * 1e-3) / 1e9,
+        "step_separate_calls": {"ms": sep_ms, "gbs": job_bytes / (sep_ms * 1e-3) / 1e9,
+                                "launches": 6, "how": "tdp_tokens and tdp_window_sum on a side stream beside "
+                                                      "tdp_extract, then tdp_blend; replayed from a CUDA graph"},
         "algorithmic_bytes": {"extract": ab["extract"], "blend": ab["blend"],
                               "overlap_factor": round(ab["overlap_factor"], 5)},
         "kernels": kern,
-        "kernel_timing": f"each kernel alone, back to back over the rotating sets, replayed from a CUDA graph of "
-                         f"{GRAPH_STEPS} launches (mean per launch over {max(1, L // GRAPH_STEPS) * GRAPH_STEPS}); "
+        "kernel_timing": f"each call alone, back to back over the rotating sets, replayed from a CUDA graph of "
+                         f"{GRAPH_STEPS} calls (mean per call over {max(1, L // GRAPH_STEPS) * GRAPH_STEPS}); "
                          "stream_launch_ms: the same launched one by one from the host; "
                          "single_launch_after_flush: median of 20 launches, each after a 256 MiB write outside its "
-                         "events (includes the launch latency)",
+                         "events (includes the launch latency); gbs of the fused calls counts the latent and tile "
+                         "bytes alone",
         "step_stream_launch_ms": stream_ms,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src},

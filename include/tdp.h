@@ -286,6 +286,42 @@ tdp_status tdp_tokens(const tdp_plan_t* plan, int32_t B, const int32_t* gen_pos,
                       int32_t* tile_cond_pos, int32_t* slot_of, cudaStream_t stream);
 
 /*
+ * tdp_extract_and_tokens -- steps 2, 3 and 4 and the window maximum of
+ * step 6 in two launches: everything tdp_extract, tdp_tokens and
+ * tdp_window_sum (maximum only) write.
+ *
+ * Source: "Tiled Data Parallelism (TDP)", What it is (each tile is the
+ * latent's sub-box; masks that sum to 1), Position normalization and
+ * Shared negative (reference) positions, as for those three calls.
+ * Arguments mean what they mean there: B, C, dtype, latent and tiles as
+ * for tdp_extract; gen_pos through slot_of as for tdp_tokens (M > 0
+ * requires cond_pos, tile_extent, keep, count and weight; tile_pos NULL
+ * skips the positions); max_abs_dev as for tdp_window_sum (NULL: no
+ * maximum).  C == 0 leaves the tiles alone and still does the rest.
+ * workspace: device memory of at least tdp_extract_and_tokens_workspace
+ *            (plan, B) bytes, owned by the caller and free for the call's
+ *            duration (calls that run at the same time need their own);
+ *            its contents on entry do not matter.
+ * When the streaming extract takes the plan (and the workspace is large
+ * enough), the extract launch also reduces the partial extents of every
+ * (tile, batch) pair's token chunks, spread over its CTAs, into the
+ * workspace, and a second, short launch combines them and writes the
+ * positions, keep flags, kept lists, counts, weights and the maximum.
+ * Otherwise the separate kernels run in turn (workspace unused; it may be
+ * NULL).  Every result equals what the separate calls write, bit for bit.
+ * Asynchronous on `stream`.  Errors: as the separate calls
+ * (TDP_ERR_ALIGNMENT for any pointer not 16-byte aligned).
+ */
+int64_t tdp_extract_and_tokens_workspace(const tdp_plan_t* plan, int32_t B);   /* bytes; -1 if invalid */
+tdp_status tdp_extract_and_tokens(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype dtype,
+                                  const void* latent, void* tiles, const int32_t* gen_pos,
+                                  int32_t normalize, int32_t* tile_pos, int32_t* offsets, int32_t M,
+                                  const int32_t* cond_pos, int32_t* tile_extent, uint8_t* keep,
+                                  int32_t* count, float* weight, int32_t* kept_idx, int32_t* num_kept,
+                                  int32_t* tile_cond_pos, int32_t* slot_of, float* max_abs_dev,
+                                  void* workspace, int64_t workspace_bytes, cudaStream_t stream);
+
+/*
  * tdp_cond_combine -- the blend of the conditioning tokens' per-tile
  * outputs (the step after tdp_cond_select).
  *

@@ -208,24 +208,44 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
     return v;
 }
 
-// Exclusive block scan of v; *total gets the block sum.  Uses 33 ints of `sh`.
-__device__ int block_excl_scan(int v, int* sh, int* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+// Thread groups that run a CTA-wide step: the whole CTA (barrier 0), or
+// the first NT threads, whole warps, of a warp-specialised CTA (named
+// barrier 1, which the remaining warps never use).  Threads of a group are
+// threadIdx.x in [0, size()).
+struct CtaGroup {
+    __device__ static int size() { return static_cast<int>(blockDim.x); }
+    __device__ static void sync() { __syncthreads(); }
+};
+template <int NT>
+struct WarpsGroup {
+    static_assert(NT % 32 == 0 && NT <= 1024, "whole warps");
+    __device__ static constexpr int size() { return NT; }
+    __device__ static void sync() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
+};
+
+// Exclusive scan of v over the group; *total gets the group sum.  Uses 33
+// ints of `sh`.
+template <class G>
+__device__ int group_excl_scan(int v, int* sh, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = G::size() >> 5;
     const int incl = warp_incl_scan(v);
     if (lane == 31) sh[warp] = incl;
-    __syncthreads();
+    G::sync();
     if (warp == 0) {
         const int w = lane < nw ? sh[lane] : 0;
         const int wi = warp_incl_scan(w);
         if (lane < nw) sh[lane] = wi - w;
         if (lane == nw - 1) sh[32] = wi;
     }
-    __syncthreads();
+    G::sync();
     const int r = sh[warp] + incl - v;
     *total = sh[32];
-    __syncthreads();
+    G::sync();
     return r;
 }
+
+// Exclusive block scan of v; *total gets the block sum.  Uses 33 ints of `sh`.
+__device__ int block_excl_scan(int v, int* sh, int* total) { return group_excl_scan<CtaGroup>(v, sh, total); }
 
 // =================================================================== staging
 // A contiguous span [g0, g1) of a global buffer staged into shared memory:
@@ -1457,13 +1477,8 @@ __global__ void __launch_bounds__(kThreads) window_sum_kernel(const __grid_const
     }
 }
 
-// max |S - 1| alone (no per-element output), in one CTA.  S(f,h,w)
-// depends on (f, h, w) only through each axis's tuple of covering-tile
-// weights (for w: through inner(w)), and equal tuples give the same S bit
-// for bit, so the maximum over the whole volume is the maximum over the
-// triples of one representative index per run of equal tuples on each
-// axis.  The tables are those of window_sum_kernel; the representatives
-// follow them in shared memory.
+// Whether indices x and y of an axis have the same tuple of covering-tile
+// weights (cnt: tiles per index, w: k weights per index).
 __device__ __forceinline__ bool same_tuple(const int* cnt, const float* w, int k, int x, int y) {
     if (cnt[x] != cnt[y]) return false;
     for (int i = 0; i < cnt[x]; ++i)
@@ -1472,29 +1487,37 @@ __device__ __forceinline__ bool same_tuple(const int* cnt, const float* w, int k
 }
 
 // Compacts the first index of every run of equal tuples on an axis of n
-// indices into rep[]; returns the number of runs.  Whole CTA.
-template <typename Same>
+// indices into rep[]; returns the number of runs.  Whole group.
+template <class G, typename Same>
 __device__ int axis_runs(int n, int* rep, int* scan_sh, Same same) {
     int carry = 0;
-    for (int x0 = 0; x0 < n; x0 += blockDim.x) {
-        const int x = x0 + threadIdx.x;
+    for (int x0 = 0; x0 < n; x0 += G::size()) {
+        const int x = x0 + static_cast<int>(threadIdx.x);
         const int start = (x < n) && (x == 0 || !same(x, x - 1)) ? 1 : 0;
         int round_total;
-        const int at = carry + block_excl_scan(start, scan_sh, &round_total);
+        const int at = carry + group_excl_scan<G>(start, scan_sh, &round_total);
         if (start) rep[at] = x;
         carry += round_total;
     }
-    __syncthreads();
+    G::sync();
     return carry;
 }
 
-__global__ void __launch_bounds__(kThreads) window_max_kernel(const __grid_constant__ tdp_plan_t p, float* max_abs_dev) {
-    pdl_launch_dependents();
-    extern __shared__ __align__(16) unsigned char wsm[];
-    __shared__ int scan_sh[33];
-    __shared__ float warp_worst[kThreads / 32];
+// Shared bytes of window_max_group's tables and representatives.
+inline long long window_max_bytes(const tdp_plan_t& p) {
+    return 4LL * ((long long)p.dims[0] * p.max_cover[0] + (long long)p.dims[1] * p.max_cover[1] + p.dims[2] +
+                  p.dims[0] + p.dims[1]) +
+           4LL * ((long long)p.dims[0] + p.dims[1] + p.dims[2]);
+}
+
+// max |S - 1| over the volume by group G; the result is valid in thread 0.
+// wsm: window_max_bytes(p) bytes; scan_sh: 33 ints; warp_worst: one float
+// per warp of the group.
+template <class G>
+__device__ float window_max_group(const tdp_plan_t& p, unsigned char* wsm, int* scan_sh, float* warp_worst) {
     const int F = p.dims[0], H = p.dims[1], W = p.dims[2];
     const int kf = p.max_cover[0], kh = p.max_cover[1];
+    const int tid = static_cast<int>(threadIdx.x), nthr = G::size();
     float* wf = reinterpret_cast<float*>(wsm);          // [F][kf]
     float* wh = wf + F * kf;                             // [H][kh]
     float* winner = wh + H * kh;                         // [W]
@@ -1503,32 +1526,32 @@ __global__ void __launch_bounds__(kThreads) window_max_kernel(const __grid_const
     int* frep = hcnt + H;                                // [F] run representatives
     int* hrep = frep + F;                                // [H]
     int* wrep = hrep + H;                                // [W]
-    for (int f = threadIdx.x; f < F; f += blockDim.x) {
+    for (int f = tid; f < F; f += nthr) {
         int lo, hi;
         tdp::axis_cover(p, 0, f, lo, hi);
         fcnt[f] = hi - lo + 1;
         for (int i = lo; i <= hi; ++i) wf[f * kf + (i - lo)] = axis_weight(p, 0, i, f);
     }
-    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    for (int h = tid; h < H; h += nthr) {
         int lo, hi;
         tdp::axis_cover(p, 1, h, lo, hi);
         hcnt[h] = hi - lo + 1;
         for (int i = lo; i <= hi; ++i) wh[h * kh + (i - lo)] = axis_weight(p, 1, i, h);
     }
-    for (int w = threadIdx.x; w < W; w += blockDim.x) {
+    for (int w = tid; w < W; w += nthr) {
         int lo, hi;
         tdp::axis_cover(p, 2, w, lo, hi);
         float inner = 0.0f;
         for (int k = lo; k <= hi; ++k) inner = fmaf(axis_weight(p, 2, k, w), 1.0f, inner);
         winner[w] = inner;
     }
-    __syncthreads();
-    const int nf = axis_runs(F, frep, scan_sh, [&](int x, int y) { return same_tuple(fcnt, wf, kf, x, y); });
-    const int nh = axis_runs(H, hrep, scan_sh, [&](int x, int y) { return same_tuple(hcnt, wh, kh, x, y); });
-    const int nwc = axis_runs(W, wrep, scan_sh,
-                              [&](int x, int y) { return __float_as_uint(winner[x]) == __float_as_uint(winner[y]); });
+    G::sync();
+    const int nf = axis_runs<G>(F, frep, scan_sh, [&](int x, int y) { return same_tuple(fcnt, wf, kf, x, y); });
+    const int nh = axis_runs<G>(H, hrep, scan_sh, [&](int x, int y) { return same_tuple(hcnt, wh, kh, x, y); });
+    const int nwc = axis_runs<G>(W, wrep, scan_sh,
+                                 [&](int x, int y) { return __float_as_uint(winner[x]) == __float_as_uint(winner[y]); });
     float worst = 0.0f;
-    for (int idx = threadIdx.x; idx < nh * nwc; idx += blockDim.x) {   // (row class, column class)
+    for (int idx = tid; idx < nh * nwc; idx += nthr) {   // (row class, column class)
         const int hi = idx / nwc, h = hrep[hi];
         const float in_w = winner[wrep[idx - hi * nwc]];
         for (int fi = 0; fi < nf; ++fi) {
@@ -1543,11 +1566,28 @@ __global__ void __launch_bounds__(kThreads) window_max_kernel(const __grid_const
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) worst = fmaxf(worst, __shfl_xor_sync(0xffffffffu, worst, o));
-    if ((threadIdx.x & 31) == 0) warp_worst[threadIdx.x >> 5] = worst;
-    __syncthreads();
+    if ((tid & 31) == 0) warp_worst[tid >> 5] = worst;
+    G::sync();
+    float m = 0.0f;
+    if (tid == 0)
+        for (int i = 0; i < (nthr >> 5); ++i) m = fmaxf(m, warp_worst[i]);
+    return m;
+}
+
+// max |S - 1| alone (no per-element output), in one CTA.  S(f,h,w)
+// depends on (f, h, w) only through each axis's tuple of covering-tile
+// weights (for w: through inner(w)), and equal tuples give the same S bit
+// for bit, so the maximum over the whole volume is the maximum over the
+// triples of one representative index per run of equal tuples on each
+// axis.  The tables are those of window_sum_kernel; the representatives
+// follow them in shared memory.
+__global__ void __launch_bounds__(kThreads) window_max_kernel(const __grid_constant__ tdp_plan_t p, float* max_abs_dev) {
+    pdl_launch_dependents();
+    extern __shared__ __align__(16) unsigned char wsm[];
+    __shared__ int scan_sh[33];
+    __shared__ float warp_worst[kThreads / 32];
+    const float m = window_max_group<CtaGroup>(p, wsm, scan_sh, warp_worst);
     if (threadIdx.x == 0) {
-        float m = 0.0f;
-        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) m = fmaxf(m, warp_worst[i]);
         pdl_wait();   // the plan alone went in; the result may still be read by the previous kernel
         *max_abs_dev = m;
     }
@@ -1880,12 +1920,9 @@ __global__ void __launch_bounds__(kThreads, 4) tokens_kernel(const __grid_consta
 
 }
 
-__global__ void __launch_bounds__(kThreads) cond_count_kernel(const unsigned char* keep, int T, int BM,
-                                                              int* count, float* weight) {
-    pdl_launch_dependents();
-    pdl_wait();   // the keep flags of the previous kernel
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= BM) return;
+// count[i] = sum over tiles t of keep[t, i]; weight[i] = 1 / count[i] (IEEE
+// fp32), 0 for a token no tile kept.
+__device__ __forceinline__ void count_one(const unsigned char* keep, int T, int BM, int i, int* count, float* weight) {
     int c = 0;
     int t = 0;
     for (; t + 16 <= T; t += 16) {   // 16 independent loads in flight
@@ -1898,6 +1935,381 @@ __global__ void __launch_bounds__(kThreads) cond_count_kernel(const unsigned cha
     for (; t < T; ++t) c += keep[(long long)t * BM + i];
     count[i] = c;
     weight[i] = c ? 1.0f / static_cast<float>(c) : 0.0f;
+}
+
+__global__ void __launch_bounds__(kThreads) cond_count_kernel(const unsigned char* keep, int T, int BM,
+                                                              int* count, float* weight) {
+    pdl_launch_dependents();
+    pdl_wait();   // the keep flags of the previous kernel
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < BM) count_one(keep, T, BM, i, count, weight);
+}
+
+// =================================================================== token steps in two launches
+// tdp_extract_and_tokens splits the token steps at the extent: the extract
+// launch reduces the partial extents of every (tile, batch) pair's K1 token
+// chunks, spread over its CTAs (extent_chunk), and a second launch
+// (tokens_finish_kernel) combines them and does the rest: positions,
+// selection, counts and the window maximum.  Neither launch waits on
+// another CTA; the partials pass through the caller's workspace.
+constexpr int kJobTokenBatch = 4;   // tokens whose loads a thread keeps in flight
+constexpr int kChunkShInts = 8;     // shared ints of an extent chunk
+constexpr int kChunkTokens = 4 * 32 * 24;   // tokens of an extent chunk (one batch per extract compute thread)
+constexpr int kFinishTokens = 4 * kThreads; // tokens of a finishing chunk (one batch per thread)
+
+// Chunks of pair (t, b) in the extract launch (K1) and the finishing launch
+// (K2): as many as the largest tile needs, so that a chunk is one batch.
+inline int extent_chunks(const tdp_plan_t& p, int per_chunk) {
+    long long n = 1;
+    for (int t = 0; t < p.total_tiles; ++t) {
+        int i_f, i_h, i_w;
+        tdp::tile_coords(p, t, i_f, i_h, i_w);
+        n = std::max(n, (long long)tdp::tile_size(p, 0, i_f) * tdp::tile_size(p, 1, i_h) * tdp::tile_size(p, 2, i_w));
+    }
+    return static_cast<int>((n + per_chunk - 1) / per_chunk);
+}
+
+// Chunks per (tile, batch) pair in the extract launch: one batch of loads
+// per compute thread each, and at least as many chunks as spread the pairs
+// over `grid` CTAs.
+inline int extent_chunks_k1(const tdp_plan_t& p, long long J, int grid) {
+    return std::max(extent_chunks(p, kChunkTokens), static_cast<int>(std::max(1LL, grid / std::max(1LL, J))));
+}
+
+// Tokens [j0, j1) of the tile's token walk: min start and max end per axis
+// over this thread's share (j0 + thread, + G::size(), ...), kJobTokenBatch
+// tokens' loads in flight.
+template <class G>
+__device__ __forceinline__ void extent_partial(const tdp_plan_t& p, const TileTokens& tt, const int* gen_b, long long N,
+                                               int j0, int j1, int (&mn)[3], int (&mx)[3]) {
+    const int nthr = G::size();
+    TokenWalk tw;
+    tw.init(tt, j0 + static_cast<int>(threadIdx.x), nthr);
+    for (int j = j0 + static_cast<int>(threadIdx.x); j < j1; j += kJobTokenBatch * nthr) {
+        long long n[kJobTokenBatch];
+#pragma unroll
+        for (int u = 0; u < kJobTokenBatch; ++u) {
+            n[u] = j + u * nthr < j1 ? tw.token(p, tt) : -1;
+            tw.next(tt);
+        }
+        int2 v[kJobTokenBatch][3];
+#pragma unroll
+        for (int u = 0; u < kJobTokenBatch; ++u)
+            if (n[u] >= 0) {
+#pragma unroll
+                for (int d = 0; d < 3; ++d) v[u][d] = *reinterpret_cast<const int2*>(gen_b + ((long long)d * N + n[u]) * 2);
+            }
+#pragma unroll
+        for (int u = 0; u < kJobTokenBatch; ++u)
+            if (n[u] >= 0) {
+#pragma unroll
+                for (int d = 0; d < 3; ++d) {
+                    mn[d] = min(mn[d], v[u][d].x);
+                    mx[d] = max(mx[d], v[u][d].y);
+                }
+            }
+    }
+}
+
+// Chunk q of the extract launch by group G: pair j = q / K1 = (tile j / B,
+// batch j % B), part q % K1 of its token walk; writes its min start / max
+// end per axis to partials[q] ((INT_MAX, INT_MIN) for an empty part).
+// jsh: kChunkShInts ints of shared memory, free again on return.
+template <class G>
+__device__ void extent_chunk(const tdp_plan_t& p, const int* gen, int B, int K1, int q, int* partials, int* jsh) {
+    const int tid = static_cast<int>(threadIdx.x);
+    const int j = q / K1, c = q - j * K1, t = j / B, b = j - t * B;
+    const long long N = (long long)p.dims[0] * p.dims[1] * p.dims[2];
+    const TileTokens tt = tile_tokens(p, t);
+    const int csz = (tt.n + K1 - 1) / K1;
+    const int j0 = min(tt.n, c * csz), j1 = min(tt.n, j0 + csz);
+    if (tid < 6) jsh[tid] = (tid & 1) ? INT_MIN : INT_MAX;
+    int mn[3] = {INT_MAX, INT_MAX, INT_MAX}, mx[3] = {INT_MIN, INT_MIN, INT_MIN};
+    extent_partial<G>(p, tt, gen + (long long)b * 3 * N * 2, N, j0, j1, mn, mx);
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        mn[d] = warp_min(mn[d]);
+        mx[d] = warp_max(mx[d]);
+    }
+    G::sync();   // jsh initialised
+    if ((tid & 31) == 0) {
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            atomicMin(&jsh[2 * d], mn[d]);
+            atomicMax(&jsh[2 * d + 1], mx[d]);
+        }
+    }
+    G::sync();
+    if (tid < 6) partials[(long long)q * 6 + tid] = jsh[tid];
+    G::sync();   // jsh is free for the next chunk
+}
+
+// The same reduction with its loads issued early: extent_chunk_issue copies
+// the chunk's tokens (8 bytes per token and axis, plane-major) into shared
+// memory with cp.async and returns at once; extent_chunk_finish, called
+// later by every thread of the same group, reduces what each thread
+// copied.  The copies' latency hides behind the caller's work in between.
+// data: room for (chunk tokens) * 3 int2.
+__device__ __forceinline__ void cp_async8(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+
+struct ChunkSpan {
+    int j0, j1;   // tokens [j0, j1) of the pair's token walk
+};
+
+__device__ __forceinline__ ChunkSpan chunk_span(const tdp_plan_t& p, int B, int K1, int q, TileTokens& tt, int& b) {
+    const int j = q / K1, c = q - j * K1, t = j / B;
+    b = j - t * B;
+    tt = tile_tokens(p, t);
+    const int csz = (tt.n + K1 - 1) / K1;
+    ChunkSpan cs;
+    cs.j0 = min(tt.n, c * csz);
+    cs.j1 = min(tt.n, cs.j0 + csz);
+    return cs;
+}
+
+template <class G>
+__device__ void extent_chunk_issue(const tdp_plan_t& p, const int* gen, int B, int K1, int q, int2* data) {
+    int b;
+    TileTokens tt;
+    const ChunkSpan cs = chunk_span(p, B, K1, q, tt, b);
+    const long long N = (long long)p.dims[0] * p.dims[1] * p.dims[2];
+    const int* gen_b = gen + (long long)b * 3 * N * 2;
+    const int n = cs.j1 - cs.j0;
+    TokenWalk tw;
+    tw.init(tt, cs.j0 + static_cast<int>(threadIdx.x), G::size());
+    for (int k = static_cast<int>(threadIdx.x); k < n; k += G::size(), tw.next(tt)) {
+        const long long tok = tw.token(p, tt);
+#pragma unroll
+        for (int d = 0; d < 3; ++d) cp_async8(data + (long long)d * n + k, gen_b + ((long long)d * N + tok) * 2);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Thread-by-thread end of extent_chunk_issue: each thread waits for its own
+// copies, reduces the tokens it copied, and its warp adds the result to
+// partials[q] with atomic min / max -- no barrier, so the warps of the CTA
+// finish independently.  partials[q] must hold (INT_MAX, INT_MIN) per axis
+// before the first warp gets here (chunk_slot_init).
+template <class G>
+__device__ void extent_chunk_finish(const tdp_plan_t& p, int B, int K1, int q, const int2* data, int* partials) {
+    int b;
+    TileTokens tt;
+    const ChunkSpan cs = chunk_span(p, B, K1, q, tt, b);
+    const int n = cs.j1 - cs.j0;
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    int mn[3] = {INT_MAX, INT_MAX, INT_MAX}, mx[3] = {INT_MIN, INT_MIN, INT_MIN};
+    for (int k = static_cast<int>(threadIdx.x); k < n; k += G::size()) {
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            const int2 v = data[(long long)d * n + k];
+            mn[d] = min(mn[d], v.x);
+            mx[d] = max(mx[d], v.y);
+        }
+    }
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        mn[d] = warp_min(mn[d]);
+        mx[d] = warp_max(mx[d]);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        int* slot = partials + (long long)q * 6;
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            if (mn[d] != INT_MAX) atomicMin(&slot[2 * d], mn[d]);
+            if (mx[d] != INT_MIN) atomicMax(&slot[2 * d + 1], mx[d]);
+        }
+    }
+}
+
+// Sets partials[q] to (INT_MAX, INT_MIN) per axis (threads 0-5).
+__device__ __forceinline__ void chunk_slot_init(int* partials, int q) {
+    if (threadIdx.x < 6) partials[(long long)q * 6 + threadIdx.x] = (threadIdx.x & 1) ? INT_MIN : INT_MAX;
+}
+
+struct TokenFinishArgs {
+    TokensArgs a;              // as tokens_kernel's
+    int* count;                // [B*M] (M > 0): zeroed by the extract launch
+    float* weight;             // [B*M] (M > 0)
+    float* max_abs_dev;        // NULL: no window maximum
+    const int* partials;       // [pairs * K1][6] from the extract launch
+    int* arrivals;             // [B]: zeroed by the extract launch
+    int K1, K2;                // chunks per pair: reduced by the extract launch / finished here
+    int window_ctas;           // 1 with the window maximum (CTA 0), else 0
+    int cond_ctas;             // pairs with M > 0, else 0: one conditioning CTA per pair
+};
+
+// Bytes of tokens_finish_kernel's dynamic shared memory: the window
+// maximum's tables or a pair's partials, whichever is larger.
+inline long long finish_smem(const tdp_plan_t& p, int K1, bool window) {
+    return std::max(6LL * K1 * 4, window ? window_max_bytes(p) : 0LL);
+}
+
+// The pair's extent [TS, TE) per axis into ext_sh from its K1 partials,
+// after the partial loads were issued into psh (threads < 6 * K1).
+__device__ __forceinline__ void pair_extent(const int* psh, int K1, int* ext_sh) {
+    __syncthreads();
+    const int tid = static_cast<int>(threadIdx.x);
+    if (tid < 6) {
+        int e = (tid & 1) ? INT_MIN : INT_MAX;
+        for (int k = 0; k < K1; ++k) e = (tid & 1) ? max(e, psh[k * 6 + tid]) : min(e, psh[k * 6 + tid]);
+        ext_sh[tid] = e;
+    }
+    __syncthreads();
+}
+
+// The second launch of tdp_extract_and_tokens.  CTA roles by index:
+//  * the window CTA (first, when asked for): max |S - 1| as
+//    window_max_kernel computes it, from the plan alone, so it runs before
+//    the wait for the extract launch and stores after it;
+//  * conditioning CTAs (one per pair, with M > 0): the pair's extent from
+//    its partials, the keep flags and kept lists as tokens_kernel computes
+//    them, each kept token added to its count (zeroed by the extract
+//    launch); the batch's last pair to finish (an arrival counter, also
+//    zeroed by the extract launch) then writes the batch's weights
+//    1 / count (IEEE fp32), so count equals the sum of the keep flags;
+//  * chunk CTAs (pairs * K2): the pair's extent, the pair's offsets and
+//    extent (part 0) and its part of the shifted positions, one batch of
+//    loads per thread issued together with the partial loads.
+__global__ void __launch_bounds__(kThreads, 1) tokens_finish_kernel(const __grid_constant__ tdp_plan_t p,
+                                                                 const __grid_constant__ TokenFinishArgs f) {
+    extern __shared__ __align__(16) unsigned char fsm[];
+    __shared__ int scan_sh[33];
+    __shared__ float warp_worst[kThreads / 32];
+    __shared__ int ext_sh[6];
+    __shared__ int last_sh;
+    pdl_launch_dependents();
+    const TokensArgs& a = f.a;
+    const int tid = static_cast<int>(threadIdx.x);
+    int blk = static_cast<int>(blockIdx.x);
+    if (blk < f.window_ctas) {
+        const float m = window_max_group<CtaGroup>(p, fsm, scan_sh, warp_worst);
+        pdl_wait();   // the result may still be read by an earlier kernel
+        if (tid == 0) *f.max_abs_dev = m;
+        return;
+    }
+    blk -= f.window_ctas;
+    // Everything derived from the plan alone is worked out before the wait
+    // for the extract launch (the plan's reads are constant-cache misses on
+    // a dependent chain); global data is read after it.
+    const long long N = (long long)p.dims[0] * p.dims[1] * p.dims[2];
+    int* psh = reinterpret_cast<int*>(fsm);   // the pair's partials
+    if (blk < f.cond_ctas) {
+        const int j = blk, t = j / a.B, b = j - t * a.B;
+        const long long row = (long long)t * a.B + b;   // (t, b) row of the per-tile outputs
+        const int T = p.total_tiles;
+        pdl_wait();   // the partial extents of the extract launch
+        const int pv = tid < 6 * f.K1 ? f.partials[(long long)j * f.K1 * 6 + tid] : 0;
+        int2 cv[3];
+        if (tid < a.M) {
+#pragma unroll
+            for (int d = 0; d < 3; ++d) cv[d] = *reinterpret_cast<const int2*>(a.cond + (((long long)b * 3 + d) * a.M + tid) * 2);
+        }
+        if (tid < 6 * f.K1) psh[tid] = pv;
+        pair_extent(psh, f.K1, ext_sh);
+        int ext[6];
+#pragma unroll
+        for (int i = 0; i < 6; ++i) ext[i] = ext_sh[i];
+        // keep flags, then the kept tokens compacted in their original
+        // order, one block scan per round
+        int total = 0;
+        for (int m0 = 0; m0 < a.M; m0 += kThreads) {
+            const int m = m0 + tid;
+            const bool in = m < a.M;
+            if (in && m0 > 0) {
+#pragma unroll
+                for (int d = 0; d < 3; ++d) cv[d] = *reinterpret_cast<const int2*>(a.cond + (((long long)b * 3 + d) * a.M + m) * 2);
+            }
+            const bool k = in && keep_token(cv, ext);
+            if (in) a.keep[row * a.M + m] = k ? 1 : 0;
+            if (k) atomicAdd(&f.count[(long long)b * a.M + m], 1);
+            int round_total;
+            const int at = total + block_excl_scan(k ? 1 : 0, scan_sh, &round_total);
+            if (in && a.slot_of) a.slot_of[row * a.M + m] = k ? at : -1;
+            if (k && a.kept_idx) a.kept_idx[row * a.M + at] = m;
+            if (k && a.tile_cond) {
+#pragma unroll
+                for (int d = 0; d < 3; ++d) {
+                    int2 q = cv[d];
+                    if (a.normalize) { q.x -= ext[2 * d]; q.y -= ext[2 * d]; }
+                    *reinterpret_cast<int2*>(a.tile_cond + ((row * 3 + d) * a.M + at) * 2) = q;
+                }
+            }
+            total += round_total;
+        }
+        if (a.kept_idx || a.tile_cond || a.slot_of) {
+            for (int q = total + tid; q < a.M; q += kThreads) {
+                if (a.kept_idx) a.kept_idx[row * a.M + q] = -1;
+                if (a.tile_cond) {
+#pragma unroll
+                    for (int d = 0; d < 3; ++d)
+                        *reinterpret_cast<int2*>(a.tile_cond + ((row * 3 + d) * a.M + q) * 2) = make_int2(0, 0);
+                }
+            }
+        }
+        if (tid == 0 && a.num_kept) a.num_kept[row] = total;
+        // the batch's last pair to get here writes its weights
+        __threadfence();   // this CTA's count additions before its arrival
+        __syncthreads();
+        if (tid == 0) last_sh = atomicAdd(&f.arrivals[b], 1) == T - 1;
+        __syncthreads();
+        if (last_sh) {
+            __threadfence();
+            for (int m = tid; m < a.M; m += kThreads) {
+                const int c = __ldcg(&f.count[(long long)b * a.M + m]);
+                f.weight[(long long)b * a.M + m] = c ? 1.0f / static_cast<float>(c) : 0.0f;
+            }
+        }
+        return;
+    }
+    blk -= f.cond_ctas;
+    const int j = blk / f.K2, c = blk - j * f.K2, t = j / a.B, b = j - t * a.B;
+    const long long row = (long long)t * a.B + b;
+    const TileTokens tt = tile_tokens(p, t);
+    const int* gen_b = a.gen + (long long)b * 3 * N * 2;
+    // this part's tokens: at most kJobTokenBatch per thread (K2 sees to it)
+    const int csz = (tt.n + f.K2 - 1) / f.K2;
+    const int j0 = min(tt.n, c * csz), j1 = min(tt.n, j0 + csz);
+    long long n[kJobTokenBatch];
+    int2 v[kJobTokenBatch][3];
+    if (a.tile_pos) {
+        TokenWalk tw;
+        tw.init(tt, j0 + tid, kThreads);
+#pragma unroll
+        for (int u = 0; u < kJobTokenBatch; ++u) {
+            n[u] = j0 + tid + u * kThreads < j1 ? tw.token(p, tt) : -1;
+            tw.next(tt);
+        }
+    }
+    pdl_wait();   // the partial extents of the extract launch
+    // the partial first (the extent waits on it), then the positions
+    const int pv = tid < 6 * f.K1 ? f.partials[(long long)j * f.K1 * 6 + tid] : 0;
+    if (a.tile_pos) {
+#pragma unroll
+        for (int u = 0; u < kJobTokenBatch; ++u)
+            if (n[u] >= 0) {
+#pragma unroll
+                for (int d = 0; d < 3; ++d) v[u][d] = *reinterpret_cast<const int2*>(gen_b + ((long long)d * N + n[u]) * 2);
+            }
+    }
+    if (tid < 6 * f.K1) psh[tid] = pv;
+    pair_extent(psh, f.K1, ext_sh);
+    if (c == 0 && tid < 3 && a.offsets) a.offsets[row * 3 + tid] = ext_sh[2 * tid];
+    if (c == 0 && tid < 6 && a.extent) a.extent[row * 6 + tid] = ext_sh[tid];
+    if (a.tile_pos) {
+        // shifted by TS (by 0 without normalize)
+        const int o0 = a.normalize ? ext_sh[0] : 0, o1 = a.normalize ? ext_sh[2] : 0, o2 = a.normalize ? ext_sh[4] : 0;
+        int* dst = a.tile_pos + tt.prefix * 6 * a.B + (long long)b * 3 * tt.n * 2;
+#pragma unroll
+        for (int u = 0; u < kJobTokenBatch; ++u)
+            if (n[u] >= 0) {
+                const long long k = j0 + tid + u * kThreads;
+                *reinterpret_cast<int2*>(dst + (0 * (long long)tt.n + k) * 2) = make_int2(v[u][0].x - o0, v[u][0].y - o0);
+                *reinterpret_cast<int2*>(dst + (1 * (long long)tt.n + k) * 2) = make_int2(v[u][1].x - o1, v[u][1].y - o1);
+                *reinterpret_cast<int2*>(dst + (2 * (long long)tt.n + k) * 2) = make_int2(v[u][2].x - o2, v[u][2].y - o2);
+            }
+    }
 }
 
 // =================================================================== slab blend
@@ -2415,6 +2827,74 @@ tdp_status tdp_blend(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_
     return launch_blend<float, float>(*plan, BC, tiles, n, out, stream);
 }
 
+// Workspace of tdp_extract_and_tokens: the partial extents, then one
+// arrival counter per batch.
+inline long long token_workspace_ints(long long J, int K1, int B) { return J * K1 * 6 + B; }
+
+int64_t tdp_extract_and_tokens_workspace(const tdp_plan_t* plan, int32_t B) {
+    if (!tdp::plan_is_valid(plan) || B < 0) return -1;
+    const long long J = (long long)plan->total_tiles * B;
+    return round_up(token_workspace_ints(J, extent_chunks_k1(*plan, J, kStreamMaxGrid), B) * 4, 16LL);
+}
+
+tdp_status tdp_extract_and_tokens(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype dtype, const void* latent,
+                                  void* tiles, const int32_t* gen_pos, int32_t normalize, int32_t* tile_pos,
+                                  int32_t* offsets, int32_t M, const int32_t* cond_pos, int32_t* tile_extent,
+                                  uint8_t* keep, int32_t* count, float* weight, int32_t* kept_idx,
+                                  int32_t* num_kept, int32_t* tile_cond_pos, int32_t* slot_of, float* max_abs_dev,
+                                  void* workspace, int64_t workspace_bytes, cudaStream_t stream) {
+    if (!tdp::plan_is_valid(plan) || B < 0 || C < 0 || M < 0 || workspace_bytes < 0) return TDP_ERR_INVALID_ARG;
+    const int esz = dtype_size(dtype);
+    if (!esz) return TDP_ERR_INVALID_ARG;
+    if (B == 0) return max_abs_dev ? tdp_window_sum(plan, max_abs_dev, nullptr, stream) : TDP_OK;
+    if (C > 0 && (!latent || !tiles)) return TDP_ERR_INVALID_ARG;
+    if (!gen_pos || (tile_pos && !offsets)) return TDP_ERR_INVALID_ARG;
+    if (M > 0 && (!cond_pos || !tile_extent || !keep || !count || !weight)) return TDP_ERR_INVALID_ARG;
+    const void* ptrs[] = {latent, tiles, gen_pos, tile_pos, offsets, cond_pos, tile_extent, keep, count,
+                          weight, kept_idx, num_kept, tile_cond_pos, slot_of, max_abs_dev, workspace};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return TDP_ERR_ALIGNMENT;
+    const tdp_plan_t& p = *plan;
+    const long long J = (long long)p.total_tiles * B;
+    if ((long long)B * C > INT_MAX || (long long)kCluster * J > INT_MAX || (long long)B * M > INT_MAX)
+        return TDP_ERR_INVALID_ARG;
+    const TokensArgs a{gen_pos, B, normalize ? 1 : 0, tile_pos, offsets, M, cond_pos, tile_extent, keep, kept_idx,
+                       num_kept, tile_cond_pos, slot_of};
+    // the two-launch form: the streaming extract reduces the partial extents
+    const int K1 = extent_chunks_k1(p, J, std::min(sm_count(), kStreamMaxGrid)), K2 = extent_chunks(p, kFinishTokens);
+    const long long need = token_workspace_ints(J, K1, B) * 4;
+    const long long cond_ctas = M > 0 ? J : 0;
+    const long long fsmem = finish_smem(p, K1, max_abs_dev != nullptr);
+    const long long fgrid = J * K2 + cond_ctas + (max_abs_dev ? 1 : 0);
+    if (C > 0 && workspace && workspace_bytes >= need && fsmem <= 40 * 1024 && 6LL * K1 <= kThreads &&
+        fgrid <= INT_MAX) {
+        bool taken = false;
+        int* partials = static_cast<int*>(workspace);
+        int* arrivals = partials + J * K1 * 6;
+        const StreamZero zero{M > 0 ? count : nullptr, B * M, arrivals, B};
+        const tdp_status sst =
+            esz == 2 ? launch_extract_stream<uint16_t>(p, B * C, latent, tiles, stream, &taken, gen_pos, B, K1, partials, zero)
+                     : launch_extract_stream<uint32_t>(p, B * C, latent, tiles, stream, &taken, gen_pos, B, K1, partials, zero);
+        if (sst != TDP_OK) return sst;
+        if (taken) {
+            const TokenFinishArgs fa{a, count, weight, max_abs_dev, partials, arrivals, K1, K2, max_abs_dev ? 1 : 0,
+                                     static_cast<int>(cond_ctas)};
+            tdp_status st = set_smem(tokens_finish_kernel, static_cast<int>(fsmem));
+            if (st != TDP_OK) return st;
+            return launch(tokens_finish_kernel, fgrid, kThreads, static_cast<int>(fsmem), stream, 1, p, fa);
+        }
+    }
+    // otherwise the separate kernels in turn
+    if (C > 0) {
+        const tdp_status st = tdp_extract(plan, B, C, dtype, latent, tiles, stream);
+        if (st != TDP_OK) return st;
+    }
+    tdp_status st = tdp_tokens(plan, B, gen_pos, normalize, tile_pos, offsets, M, cond_pos, tile_extent, keep, count,
+                               weight, kept_idx, num_kept, tile_cond_pos, slot_of, stream);
+    if (st != TDP_OK) return st;
+    return max_abs_dev ? tdp_window_sum(plan, max_abs_dev, nullptr, stream) : TDP_OK;
+}
+
 tdp_status tdp_blend_slab(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_dtype, const void* tiles,
                           int32_t row0, int32_t row1, tdp_dtype out_dtype, void* out, cudaStream_t stream) {
     if (!tdp::plan_is_valid(plan) || B < 0 || C < 0) return TDP_ERR_INVALID_ARG;
@@ -2450,7 +2930,7 @@ tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum
     const int smem = tables ? static_cast<int>(tab) : 0;
     if (!sum_out && tables) {
         // the maximum alone: one CTA over the runs of equal weight tuples
-        const long long reps = tab + 4LL * ((long long)p.dims[0] + p.dims[1] + p.dims[2]);
+        const long long reps = window_max_bytes(p);
         if (reps <= 40 * 1024) {
             tdp_status st = set_smem(window_max_kernel, static_cast<int>(reps));
             if (st != TDP_OK) return st;

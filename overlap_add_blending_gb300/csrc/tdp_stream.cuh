@@ -129,6 +129,41 @@ struct StreamArgs {
     int off_full, off_empty, off_tab, off_hdr, off_data;   // shared layout (bytes)
 };
 
+// Work the extract launch does besides its units in tdp_extract_and_tokens:
+// the partial extents of the (tile, batch) pairs' token chunks (the first
+// pass of the token steps, spread over the grid; the second launch of the
+// call finishes them).  The compute warps of a CTA with chunks reduce them
+// first, while its producer warp already stages the CTA's first units; the
+// host's split gives that CTA correspondingly fewer units.
+constexpr int kJobNone = 0, kJobExtent = 1;
+constexpr int kChunkLead = 5;   // units before a CTA's last at which its last chunk's loads are issued
+struct StreamJobs {
+    int kind;                       // kJobNone or kJobExtent
+    int B;                          // pair j is (tile j / B, batch j % B)
+    int K1;                         // chunks per pair: chunk q is pair q / K1, part q % K1
+    int off_job;                    // shared offset of the chunks' scratch (bytes)
+    int start[kStreamMaxGrid + 1];  // CTA i reduces chunks [start[i], start[i + 1])
+    const int* gen;                 // generated positions [B, 3, N, 2]
+    int* partials;                  // [pairs * K1][6]: per chunk, min start / max end per axis
+    int* zero_a;                    // CTA 0 sets zero_a[0, nzero_a) and zero_b[0, nzero_b) to 0
+    int* zero_b;                    // (the finishing launch's counters)
+    int nzero_a, nzero_b;
+    tdp_plan_t p;
+};
+
+// Ints the extract launch sets to zero for the launch after it.
+struct StreamZero {
+    int* a;
+    int na;
+    int* b;
+    int nb;
+};
+
+static_assert(sizeof(StreamArgs) + sizeof(StreamSplit) + sizeof(StreamTables) + sizeof(StreamJobs) <= 32764,
+              "streaming kernel parameters fit the 32 KB parameter space");
+static_assert(kChunkTokens == kJobTokenBatch * 32 * kStreamExtractWarps,
+              "an extent chunk is one batch of loads per extract compute thread");
+
 // ------------------------------------------------------------------ device helpers
 // Raise the transaction count of the barrier's current phase without
 // arriving (the bulk copies issued after it complete against it).
@@ -262,14 +297,17 @@ __device__ __forceinline__ StreamSmem stream_prologue(const StreamArgs& a, const
 template <typename E>
 __global__ void __launch_bounds__(kStreamExtractThreads, 1)
     extract_stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ StreamSplit sp,
-                          const __grid_constant__ StreamTables tb) {
+                          const __grid_constant__ StreamTables tb, const __grid_constant__ StreamJobs jb) {
     constexpr int esz = static_cast<int>(sizeof(E));
     constexpr int EPQ = 8 / esz;   // elements per 8-byte group
     constexpr int kWarps = kStreamExtractWarps;
     extern __shared__ __align__(128) unsigned char smem[];
     const StreamSmem m = stream_prologue(a, tb, smem, 1, kWarps);
     const int first = sp.start[blockIdx.x], last = sp.start[blockIdx.x + 1];
-    if (first >= last) return;
+    const int job0 = jb.kind == kJobExtent ? jb.start[blockIdx.x] : 0;
+    const int job1 = jb.kind == kJobExtent ? jb.start[blockIdx.x + 1] : 0;
+    const bool zeroes = jb.kind == kJobExtent && blockIdx.x == 0;
+    if (first >= last && job0 >= job1 && !zeroes) return;
     const int S = a.nstages, n = last - first;
     const int F = a.F, H = a.H, W = a.W, nw = a.nw;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -301,16 +339,39 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
         return;
     }
 
-    // ---- compute warps
+    // ---- compute warps: the CTA's token chunks and units.  Chunks before
+    // the last are reduced first; the last one's loads are issued
+    // kChunkLead units before the end and each warp reduces its share two
+    // units before the end, into the chunk's slot with atomics, so that
+    // the loads' latency hides behind the units and no barrier stops the
+    // warps.
+    using G = WarpsGroup<32 * kWarps>;
+    int* const jsh = reinterpret_cast<int*>(smem + jb.off_job);
+    int2* const cdata = reinterpret_cast<int2*>(smem + jb.off_job + 4 * kChunkShInts);
+    if (zeroes) {
+        for (int i = threadIdx.x; i < jb.nzero_a; i += 32 * kWarps) jb.zero_a[i] = 0;
+        for (int i = threadIdx.x; i < jb.nzero_b; i += 32 * kWarps) jb.zero_b[i] = 0;
+    }
+    const bool async_chunk = job1 > job0;
+    for (int q = job0; q < job1 - 1; ++q) extent_chunk<G>(jb.p, jb.gen, jb.B, jb.K1, q, jb.partials, jsh);
+    if (async_chunk) {
+        chunk_slot_init(jb.partials, job1 - 1);
+        G::sync();   // the slot is set before any warp adds to it
+    }
+    const int k_issue = max(0, n - kChunkLead);         // the last chunk's loads go out before this unit
+    const int k_fin = max(k_issue, n - 2);               // and each warp reduces its share after this one
+    bool chunk_done = !async_chunk;
+    if (async_chunk && n == 0) extent_chunk_issue<G>(jb.p, jb.gen, jb.B, jb.K1, job1 - 1, cdata);
     unsigned char* tiles = static_cast<unsigned char*>(a.dst);
     UnitCursor c;
     c.init(first, a.BC, a.nbands);
     int rot = 0;   // the warp that takes the unit's first span: the spans are dealt round robin across units
     for (int k = 0; k < n; ++k, c.next()) {
+        if (async_chunk && k == k_issue) extent_chunk_issue<G>(jb.p, jb.gen, jb.B, jb.K1, job1 - 1, cdata);
         const int s = k % S;
         if (!mbar_wait_bounded(&m.full[s], (k / S) & 1)) {
             if (lane == 0) atomicOr(&g_device_error, kErrExtractWait);
-            return;   // no release: the producer gives up and drains
+            break;   // no release: the producer gives up and drains (the chunk below still meets its barriers)
         }
         const BandEnt b = m.bands[c.band];
         const FrameEnt fe = m.frames[c.f];
@@ -391,7 +452,14 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&m.empty[s]);
+        if (k == k_fin && !chunk_done) {
+            extent_chunk_finish<G>(jb.p, jb.B, jb.K1, job1 - 1, cdata, jb.partials);
+            chunk_done = true;
+        }
     }
+    // (a CTA without units, or a warp that gave up waiting: its copies
+    // must land before the CTA's shared memory goes)
+    if (!chunk_done) extent_chunk_finish<G>(jb.p, jb.B, jb.K1, job1 - 1, cdata, jb.partials);
 }
 
 // =================================================================== blend
@@ -694,7 +762,19 @@ struct StreamLaunch {
     StreamArgs a;
     StreamSplit sp;
     StreamTables tb;
+    StreamJobs jb;
     int grid = 0, smem = 0;
+};
+
+// Jobs a launch takes besides its units, with their cost in the split's
+// measure (bytes a unit moves) and the shared scratch they need.
+constexpr int kStreamSmemMax = 227 * 1024;     // dynamic shared memory a CTA may opt in to
+constexpr long long kExtentCostPerToken = 4;    // a token chunk's share of its CTA, per token
+struct StreamJobPlan {
+    int kind = kJobNone;
+    int B = 0;                // kJobExtent: batch
+    int K1 = 0;               // kJobExtent: chunks per (tile, batch) pair
+    int scratch = 0;          // shared bytes of the chunks' scratch
 };
 
 // Shared bytes one staged run may take: its 16-byte chunks, at most
@@ -871,13 +951,30 @@ inline void stream_tables(const tdp_plan_t& p, bool blend, StreamLaunch& L) {
 // CTA i takes the units from the first one whose bytes-so-far reach i / G
 // of the total.  gcost[g] is the cost of one unit of group g = f * nbands +
 // band, and the units of a group are its BC (b, c) planes: u = g * BC + bc.
-inline void stream_split(const std::vector<long long>& gcost, long long BC, int G, StreamSplit& sp) {
+// With `reserve`, CTA i first runs jobs of cost reserve[i]: its share of
+// the units is (units' cost + all jobs' cost) / G less that, at least 0.
+inline void stream_split(const std::vector<long long>& gcost, long long BC, int G, StreamSplit& sp,
+                         const std::vector<long long>* reserve = nullptr) {
     const int NG = static_cast<int>(gcost.size());
     std::vector<__int128> cum(NG + 1, 0);   // cost of all units of the groups before g
     for (int g = 0; g < NG; ++g) cum[g + 1] = cum[g] + (__int128)gcost[g] * BC;
     const long long n = BC * NG;
+    std::vector<__int128> share(G + 1, 0);   // CTAs before i: their shares of the units, in G-ths
+    __int128 jobs = 0;
+    if (reserve)
+        for (int i = 0; i < G; ++i) jobs += (*reserve)[i];
+    for (int i = 0; i < G; ++i) {
+        __int128 c = 1;
+        if (reserve) {
+            c = cum[NG] + jobs - (__int128)G * (*reserve)[i];
+            if (c < 0) c = 0;
+        }
+        share[i + 1] = share[i] + c;
+    }
+    if (share[G] == 0)
+        for (int i = 0; i <= G; ++i) share[i] = i;
     for (int i = 0; i <= G; ++i) {
-        const __int128 target = cum[NG] * i / G;
+        const __int128 target = cum[NG] * share[i] / share[G];
         const int g = static_cast<int>(std::upper_bound(cum.begin(), cum.end(), target) - cum.begin()) - 1;
         long long u = n;
         if (g < NG) {
@@ -911,7 +1008,7 @@ inline int host_col_terms(const tdp_plan_t& p, int E) {
 // such band that leaves kStreamUnitsPerCta units per CTA wins; failing that
 // the shortest such band (the most units); failing that any band that fits.
 inline tdp_status stream_geometry(const tdp_plan_t& p, bool blend, int BC, int esz_src, int esz_dst, int sms,
-                                  StreamLaunch& L) {
+                                  StreamLaunch& L, const StreamJobPlan& jobs = StreamJobPlan{}) {
     const int F = p.dims[0], H = p.dims[1], W = p.dims[2];
     sms = std::max(1, std::min(sms, kStreamMaxGrid));
     const int cpr = blend ? W * esz_dst / 16 : 0;
@@ -965,7 +1062,31 @@ inline tdp_status stream_geometry(const tdp_plan_t& p, bool blend, int BC, int e
                 host_run_rows(p, f, hb0, hb1) * p.prefix[2][p.num_tiles[2]] * (blend ? esz_src : esz_dst);
             gcost.push_back(lat + runs);
         }
-    stream_split(gcost, BC, L.grid, L.sp);
+    // jobs: their CTAs, the shared scratch after the ring, and their cost
+    std::memset(&L.jb, 0, sizeof(L.jb));
+    L.jb.kind = jobs.kind;
+    L.jb.B = jobs.B;
+    L.jb.K1 = jobs.K1;
+    L.jb.p = p;
+    std::vector<long long> reserve(L.grid, 0);
+    if (jobs.kind == kJobExtent) {
+        L.jb.off_job = round_up(L.smem, 16);
+        L.smem = L.jb.off_job + round_up(jobs.scratch, 16);
+        if (L.smem > kStreamSmemMax) return TDP_ERR_UNSUPPORTED;
+        // chunk q on CTA i when ceil(i Q / G) <= q < ceil((i + 1) Q / G)
+        const long long Q = (long long)p.total_tiles * jobs.B * jobs.K1, G = L.grid;
+        if (Q > INT_MAX) return TDP_ERR_UNSUPPORTED;
+        for (int i = 0; i <= L.grid; ++i) L.jb.start[i] = static_cast<int>((i * Q + G - 1) / G);
+        for (int i = 0; i < L.grid; ++i)
+            for (int q = L.jb.start[i]; q < L.jb.start[i + 1]; ++q) {
+                int i_f, i_h, i_w;
+                tdp::tile_coords(p, q / jobs.K1 / jobs.B, i_f, i_h, i_w);
+                const long long tokens =
+                    (long long)tdp::tile_size(p, 0, i_f) * tdp::tile_size(p, 1, i_h) * tdp::tile_size(p, 2, i_w);
+                reserve[i] += (tokens + jobs.K1 - 1) / jobs.K1 * kExtentCostPerToken;
+            }
+    }
+    stream_split(gcost, BC, L.grid, L.sp, jobs.kind != kJobNone ? &reserve : nullptr);
     return TDP_OK;
 }
 
@@ -1001,31 +1122,57 @@ inline bool stream_eligible(const tdp_plan_t& p, bool blend, int esz_src, int es
 // Geometry of a launch on the current device, and the kernel's opt-in to
 // its dynamic shared memory.
 template <typename K>
-tdp_status stream_prepare(K kernel, const tdp_plan_t& p, bool blend, int BC, int esz_src, int esz_dst, StreamLaunch& L) {
-    tdp_status st = stream_geometry(p, blend, BC, esz_src, esz_dst, sm_count(), L);
+tdp_status stream_prepare(K kernel, const tdp_plan_t& p, bool blend, int BC, int esz_src, int esz_dst, StreamLaunch& L,
+                          const StreamJobPlan& jobs = StreamJobPlan{}) {
+    tdp_status st = stream_geometry(p, blend, BC, esz_src, esz_dst, sm_count(), L, jobs);
     if (st != TDP_OK) return st;
     return cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem));
 }
 
+// The streaming extract, if it takes the plan (*taken); with `gen`, also
+// the partial extents of every (tile, batch) pair's K1 token chunks (B
+// batches) into `partials` in the same launch.
 template <typename E>
 tdp_status launch_extract_stream(const tdp_plan_t& p, int BC, const void* latent, void* tiles, cudaStream_t stream,
-                                 bool* taken) {
+                                 bool* taken, const int* gen = nullptr, int B = 0, int K1 = 0,
+                                 int* partials = nullptr, const StreamZero& zero = StreamZero{}) {
     constexpr int esz = static_cast<int>(sizeof(E));
     *taken = false;
     int kt = 0;
     if (!stream_eligible(p, false, esz, esz, &kt)) return TDP_OK;
-    static thread_local StreamLaunch L;   // 9 KB: kept off the caller's stack
-    tdp_status st = stream_prepare(extract_stream_kernel<E>, p, false, BC, esz, esz, L);
+    static thread_local StreamLaunch L;   // 13 KB: kept off the caller's stack
+    StreamJobPlan jobs;
+    if (gen) {
+        // scratch: the reduction's ints, then one chunk's tokens (3 int2 each)
+        int nmax = 1;
+        for (int t = 0; t < p.total_tiles; ++t) {
+            int i_f, i_h, i_w;
+            tdp::tile_coords(p, t, i_f, i_h, i_w);
+            nmax = std::max(nmax, tdp::tile_size(p, 0, i_f) * tdp::tile_size(p, 1, i_h) * tdp::tile_size(p, 2, i_w));
+        }
+        jobs.kind = kJobExtent;
+        jobs.B = B;
+        jobs.K1 = K1;
+        jobs.scratch = 4 * kChunkShInts + 24 * ((nmax + K1 - 1) / K1);
+    }
+    tdp_status st = stream_prepare(extract_stream_kernel<E>, p, false, BC, esz, esz, L, jobs);
     if (st == TDP_ERR_UNSUPPORTED) return TDP_OK;
     if (st != TDP_OK) return st;
     L.a.src = latent;
     L.a.dst = tiles;
     L.a.src_bytes = (long long)BC * p.dims[0] * p.dims[1] * p.dims[2] * esz;
     L.a.dst_bytes = (long long)BC * tdp::total_volume(p) * esz;
+    L.jb.gen = gen;
+    L.jb.partials = partials;
+    L.jb.zero_a = zero.a;
+    L.jb.nzero_a = zero.a ? zero.na : 0;
+    L.jb.zero_b = zero.b;
+    L.jb.nzero_b = zero.b ? zero.nb : 0;
     *taken = true;
-    return launch(extract_stream_kernel<E>, L.grid, kStreamExtractThreads, L.smem, stream, 1, L.a, L.sp, L.tb);
+    return launch(extract_stream_kernel<E>, L.grid, kStreamExtractThreads, L.smem, stream, 1, L.a, L.sp, L.tb, L.jb);
 }
 
+// The streaming blend, if it takes the plan (*taken).
 template <typename Tin, typename Tout>
 tdp_status launch_blend_stream(const tdp_plan_t& p, int BC, const void* tiles, long long tiles_numel, void* out,
                                cudaStream_t stream, bool* taken) {
@@ -1034,7 +1181,7 @@ tdp_status launch_blend_stream(const tdp_plan_t& p, int BC, const void* tiles, l
     int kt = 0;
     if (!stream_eligible(p, true, isz, osz, &kt)) return TDP_OK;
     auto go = [&](auto kernel) -> tdp_status {
-        static thread_local StreamLaunch L;   // 9 KB: kept off the caller's stack
+        static thread_local StreamLaunch L;   // 13 KB: kept off the caller's stack
         tdp_status st = stream_prepare(kernel, p, true, BC, isz, osz, L);
         if (st == TDP_ERR_UNSUPPORTED) return TDP_OK;
         if (st != TDP_OK) return st;

@@ -141,6 +141,13 @@ _lib.tdp_tokens.argtypes = [_P(Plan), C.c_int32, C.c_void_p, C.c_int32, C.c_void
                             C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                             C.c_void_p, C.c_void_p, C.c_void_p]
 _lib.tdp_tokens.restype = C.c_int
+_lib.tdp_extract_and_tokens.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_void_p,
+                                        C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p,
+                                        C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                        C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p]
+_lib.tdp_extract_and_tokens.restype = C.c_int
+_lib.tdp_extract_and_tokens_workspace.argtypes = [_P(Plan), C.c_int32]
+_lib.tdp_extract_and_tokens_workspace.restype = C.c_int64
 _lib.tdp_cond_combine.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_void_p,
                                   C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]
 _lib.tdp_cond_combine.restype = C.c_int
@@ -180,6 +187,7 @@ if _lib.tdp_plan_struct_size() != C.sizeof(Plan):
 EXPORTS = ("tdp_plan", "tdp_tile_offset", "tdp_tiles_numel", "tdp_tile_box", "tdp_plan_stats",
            "tdp_balanced_tile_split", "tdp_search_layouts",
            "tdp_extract", "tdp_positions", "tdp_cond_select", "tdp_tokens", "tdp_cond_combine", "tdp_blend",
+           "tdp_extract_and_tokens", "tdp_extract_and_tokens_workspace",
            "tdp_shard_plan", "tdp_blend_slab",
            "tdp_extract_tokens", "tdp_blend_tokens", "tdp_window_sum",
            "tdp_launch_geometry", "tdp_device_error", "tdp_status_str", "tdp_last_cuda_error",
@@ -471,21 +479,9 @@ def tokens(p: Plan, gen_pos: torch.Tensor, cond_pos: torch.Tensor, normalize: bo
     N = p.dims[0] * p.dims[1] * p.dims[2]
     if tuple(gen_pos.shape) != (B, 3, N, 2) or tuple(cond_pos.shape) != (B, 3, M, 2):
         raise ValueError("gen_pos must be [B, 3, F*H*W, 2] and cond_pos [B, 3, M, 2]")
-    dev = gen_pos.device
-    T = p.T
     o = out if out is not None else {}
     if not o:
-        o["tile_pos"] = torch.empty(6 * B * p.tokens_numel(), dtype=torch.int32, device=dev)
-        o["offsets"] = torch.empty((T, B, 3), dtype=torch.int32, device=dev)
-        o["extent"] = torch.empty((T, B, 3, 2), dtype=torch.int32, device=dev)
-        o["keep"] = torch.empty((T, B, M), dtype=torch.uint8, device=dev)
-        o["count"] = torch.empty((B, M), dtype=torch.int32, device=dev)
-        o["weight"] = torch.empty((B, M), dtype=torch.float32, device=dev)
-        if with_lists:
-            o["kept_idx"] = torch.empty((T, B, M), dtype=torch.int32, device=dev)
-            o["num_kept"] = torch.empty((T, B), dtype=torch.int32, device=dev)
-            o["tile_cond_pos"] = torch.empty((T, B, 3, M, 2), dtype=torch.int32, device=dev)
-            o["slot_of"] = torch.empty((T, B, M), dtype=torch.int32, device=dev)
+        o.update(token_outputs(p, B, M, gen_pos.device, with_lists))
 
     def opt(name, dtype):
         return _dev(o[name], name, dtype) if name in o else None
@@ -498,6 +494,81 @@ def tokens(p: Plan, gen_pos: torch.Tensor, cond_pos: torch.Tensor, normalize: bo
                            opt("tile_cond_pos", torch.int32), opt("slot_of", torch.int32), _stream(stream)),
            "tdp_tokens")
     return o
+
+
+def token_outputs(p: Plan, B: int, M: int, device, with_lists: bool = True) -> dict:
+    """Empty device buffers for every output of tdp_tokens (the dict tokens
+    and extract_and_tokens fill)."""
+    T = p.T
+    o = {"tile_pos": torch.empty(6 * B * p.tokens_numel(), dtype=torch.int32, device=device),
+         "offsets": torch.empty((T, B, 3), dtype=torch.int32, device=device),
+         "extent": torch.empty((T, B, 3, 2), dtype=torch.int32, device=device),
+         "keep": torch.empty((T, B, M), dtype=torch.uint8, device=device),
+         "count": torch.empty((B, M), dtype=torch.int32, device=device),
+         "weight": torch.empty((B, M), dtype=torch.float32, device=device)}
+    if with_lists:
+        o["kept_idx"] = torch.empty((T, B, M), dtype=torch.int32, device=device)
+        o["num_kept"] = torch.empty((T, B), dtype=torch.int32, device=device)
+        o["tile_cond_pos"] = torch.empty((T, B, 3, M, 2), dtype=torch.int32, device=device)
+        o["slot_of"] = torch.empty((T, B, M), dtype=torch.int32, device=device)
+    return o
+
+
+def extract_and_tokens_workspace(p: Plan, B: int) -> int:
+    """tdp_extract_and_tokens_workspace: bytes of device workspace the call needs."""
+    n = int(_lib.tdp_extract_and_tokens_workspace(C.byref(p), int(B)))
+    if n < 0:
+        raise ValueError("invalid plan or batch")
+    return n
+
+
+def extract_and_tokens(p: Plan, latent: torch.Tensor, gen_pos: torch.Tensor, cond_pos: torch.Tensor,
+                       tiles: Optional[torch.Tensor] = None, tok: Optional[dict] = None,
+                       max_dev: Optional[torch.Tensor] = None, window_max: bool = True,
+                       workspace: Optional[torch.Tensor] = None, normalize: bool = True,
+                       stream: Optional[torch.cuda.Stream] = None):
+    """tdp_extract_and_tokens: the tiles, every output of tokens() and (unless
+    window_max is False) max |S-1| in two launches.  `tok` as token_outputs()
+    makes it (keys left out are not written; an empty or missing dict is
+    filled with new buffers); max_dev a 4-float buffer; workspace a byte
+    buffer of extract_and_tokens_workspace() bytes (made here when None).
+    Returns (tiles, tok, max_dev[:1] or None)."""
+    if latent.dim() != 5 or tuple(latent.shape[2:]) != tuple(p.dims):
+        raise ValueError(f"latent must be [B, C, {tuple(p.dims)}], got {tuple(latent.shape)}")
+    B, Cc = int(latent.shape[0]), int(latent.shape[1])
+    M = int(cond_pos.shape[2])
+    N = p.dims[0] * p.dims[1] * p.dims[2]
+    if tuple(gen_pos.shape) != (B, 3, N, 2) or tuple(cond_pos.shape) != (B, 3, M, 2):
+        raise ValueError("gen_pos must be [B, 3, F*H*W, 2] and cond_pos [B, 3, M, 2]")
+    n = p.tiles_numel(B, Cc)
+    if tiles is None:
+        tiles = torch.empty(n, dtype=latent.dtype, device=latent.device)
+    if tiles.numel() != n or tiles.dtype != latent.dtype:
+        raise ValueError("tiles buffer has the wrong size or dtype")
+    o = tok if tok is not None else {}
+    if not o:
+        o.update(token_outputs(p, B, M, latent.device))
+    if window_max and max_dev is None:
+        max_dev = torch.empty(4, dtype=torch.float32, device=latent.device)
+    if workspace is None:
+        workspace = torch.empty(max(16, extract_and_tokens_workspace(p, B)), dtype=torch.uint8, device=latent.device)
+
+    def opt(name, dtype):
+        return _dev(o[name], name, dtype) if name in o else None
+
+    _check(_lib.tdp_extract_and_tokens(C.byref(p), B, Cc, _dtype_code(latent.dtype), _dev(latent, "latent"),
+                                       _dev(tiles, "tiles"), _dev(gen_pos, "gen_pos", torch.int32),
+                                       1 if normalize else 0, opt("tile_pos", torch.int32),
+                                       opt("offsets", torch.int32), M,
+                                       _dev(cond_pos, "cond_pos", torch.int32) if M > 0 else None,
+                                       opt("extent", torch.int32), opt("keep", torch.uint8),
+                                       opt("count", torch.int32), opt("weight", torch.float32),
+                                       opt("kept_idx", torch.int32), opt("num_kept", torch.int32),
+                                       opt("tile_cond_pos", torch.int32), opt("slot_of", torch.int32),
+                                       _dev(max_dev, "max_dev", torch.float32) if window_max else None,
+                                       _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+                                       _stream(stream)), "tdp_extract_and_tokens")
+    return tiles, o, (max_dev[:1] if window_max else None)
 
 
 def cond_combine(p: Plan, tile_cond_out: torch.Tensor, slot_of: torch.Tensor, weight: torch.Tensor,
