@@ -322,6 +322,25 @@ tdp_status tdp_extract_and_tokens(const tdp_plan_t* plan, int32_t B, int32_t C, 
                                   void* workspace, int64_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * tdp_extract_and_tokens_no_alloc -- tdp_extract_and_tokens with the
+ * library's own scratch instead of a caller's workspace: a file-scope
+ * device array of 64 KiB (one instance per device, found with
+ * cudaGetSymbolAddress on the current device); nothing is allocated.
+ * Arguments, results and errors as tdp_extract_and_tokens; a plan and
+ * batch whose tdp_extract_and_tokens_workspace exceeds 64 KiB give
+ * TDP_ERR_UNSUPPORTED.  Calls that overlap on one device (other streams,
+ * other host threads) share the scratch and race: run them one after
+ * another.  Nothing is claimed for CUDA graph capture.
+ */
+tdp_status tdp_extract_and_tokens_no_alloc(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype dtype,
+                                           const void* latent, void* tiles, const int32_t* gen_pos,
+                                           int32_t normalize, int32_t* tile_pos, int32_t* offsets, int32_t M,
+                                           const int32_t* cond_pos, int32_t* tile_extent, uint8_t* keep,
+                                           int32_t* count, float* weight, int32_t* kept_idx, int32_t* num_kept,
+                                           int32_t* tile_cond_pos, int32_t* slot_of, float* max_abs_dev,
+                                           cudaStream_t stream);
+
+/*
  * tdp_cond_combine -- the blend of the conditioning tokens' per-tile
  * outputs (the step after tdp_cond_select).
  *

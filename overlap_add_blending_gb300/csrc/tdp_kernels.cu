@@ -65,6 +65,9 @@ constexpr int kBlendConsumers = 256;            // blend threads that compute (8
 constexpr int kBlendThreads = kBlendConsumers + 32;   // + one producer warp
 
 __device__ unsigned int g_device_error = 0;
+// Scratch of tdp_extract_and_tokens_no_alloc (the partial token extents and
+// arrival counters of one call): 64 KiB, one instance per device.
+static __device__ __align__(256) int g_token_scratch[16384];
 
 // Debug builds: records a failed index check (kErrIndex) and tells the
 // caller to skip the access.  Release builds: always false, no code.
@@ -2893,6 +2896,24 @@ tdp_status tdp_extract_and_tokens(const tdp_plan_t* plan, int32_t B, int32_t C, 
                                weight, kept_idx, num_kept, tile_cond_pos, slot_of, stream);
     if (st != TDP_OK) return st;
     return max_abs_dev ? tdp_window_sum(plan, max_abs_dev, nullptr, stream) : TDP_OK;
+}
+
+tdp_status tdp_extract_and_tokens_no_alloc(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype dtype,
+                                           const void* latent, void* tiles, const int32_t* gen_pos,
+                                           int32_t normalize, int32_t* tile_pos, int32_t* offsets, int32_t M,
+                                           const int32_t* cond_pos, int32_t* tile_extent, uint8_t* keep,
+                                           int32_t* count, float* weight, int32_t* kept_idx, int32_t* num_kept,
+                                           int32_t* tile_cond_pos, int32_t* slot_of, float* max_abs_dev,
+                                           cudaStream_t stream) {
+    const int64_t need = tdp_extract_and_tokens_workspace(plan, B);
+    if (need < 0) return TDP_ERR_INVALID_ARG;
+    if (need > (int64_t)sizeof(g_token_scratch)) return TDP_ERR_UNSUPPORTED;
+    void* scratch = nullptr;   // this device's instance of the library's scratch array
+    const tdp_status st = cuda_status(cudaGetSymbolAddress(&scratch, g_token_scratch));
+    if (st != TDP_OK) return st;
+    return tdp_extract_and_tokens(plan, B, C, dtype, latent, tiles, gen_pos, normalize, tile_pos, offsets, M,
+                                  cond_pos, tile_extent, keep, count, weight, kept_idx, num_kept, tile_cond_pos,
+                                  slot_of, max_abs_dev, scratch, (int64_t)sizeof(g_token_scratch), stream);
 }
 
 tdp_status tdp_blend_slab(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtype in_dtype, const void* tiles,

@@ -146,6 +146,12 @@ _lib.tdp_extract_and_tokens.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int,
                                         C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                         C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p]
 _lib.tdp_extract_and_tokens.restype = C.c_int
+_lib.tdp_extract_and_tokens_no_alloc.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_void_p,
+                                                 C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32,
+                                                 C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                                 C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                                 C.c_void_p]
+_lib.tdp_extract_and_tokens_no_alloc.restype = C.c_int
 _lib.tdp_extract_and_tokens_workspace.argtypes = [_P(Plan), C.c_int32]
 _lib.tdp_extract_and_tokens_workspace.restype = C.c_int64
 _lib.tdp_cond_combine.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_void_p,
@@ -187,7 +193,7 @@ if _lib.tdp_plan_struct_size() != C.sizeof(Plan):
 EXPORTS = ("tdp_plan", "tdp_tile_offset", "tdp_tiles_numel", "tdp_tile_box", "tdp_plan_stats",
            "tdp_balanced_tile_split", "tdp_search_layouts",
            "tdp_extract", "tdp_positions", "tdp_cond_select", "tdp_tokens", "tdp_cond_combine", "tdp_blend",
-           "tdp_extract_and_tokens", "tdp_extract_and_tokens_workspace",
+           "tdp_extract_and_tokens", "tdp_extract_and_tokens_workspace", "tdp_extract_and_tokens_no_alloc",
            "tdp_shard_plan", "tdp_blend_slab",
            "tdp_extract_tokens", "tdp_blend_tokens", "tdp_window_sum",
            "tdp_launch_geometry", "tdp_device_error", "tdp_status_str", "tdp_last_cuda_error",
@@ -569,6 +575,30 @@ def extract_and_tokens(p: Plan, latent: torch.Tensor, gen_pos: torch.Tensor, con
                                        _dev(workspace, "workspace", torch.uint8), workspace.numel(),
                                        _stream(stream)), "tdp_extract_and_tokens")
     return tiles, o, (max_dev[:1] if window_max else None)
+
+
+def extract_and_tokens_no_alloc(p: Plan, latent: torch.Tensor, gen_pos: torch.Tensor, cond_pos: torch.Tensor,
+                                tiles: torch.Tensor, tok: dict, max_dev: Optional[torch.Tensor] = None,
+                                normalize: bool = True, stream: Optional[torch.cuda.Stream] = None):
+    """tdp_extract_and_tokens_no_alloc: extract_and_tokens into the caller's
+    buffers (tiles, tok as token_outputs() makes it, max_dev a 4-float buffer
+    or None) with the library's own scratch; this binding allocates nothing
+    either."""
+    B, Cc = int(latent.shape[0]), int(latent.shape[1])
+    M = int(cond_pos.shape[2])
+
+    def opt(name, dtype):
+        return _dev(tok[name], name, dtype) if name in tok else None
+
+    _check(_lib.tdp_extract_and_tokens_no_alloc(
+        C.byref(p), B, Cc, _dtype_code(latent.dtype), _dev(latent, "latent"), _dev(tiles, "tiles"),
+        _dev(gen_pos, "gen_pos", torch.int32), 1 if normalize else 0, opt("tile_pos", torch.int32),
+        opt("offsets", torch.int32), M, _dev(cond_pos, "cond_pos", torch.int32) if M > 0 else None,
+        opt("extent", torch.int32), opt("keep", torch.uint8), opt("count", torch.int32),
+        opt("weight", torch.float32), opt("kept_idx", torch.int32), opt("num_kept", torch.int32),
+        opt("tile_cond_pos", torch.int32), opt("slot_of", torch.int32),
+        None if max_dev is None else _dev(max_dev, "max_dev", torch.float32), _stream(stream)),
+        "tdp_extract_and_tokens_no_alloc")
 
 
 def cond_combine(p: Plan, tile_cond_out: torch.Tensor, slot_of: torch.Tensor, weight: torch.Tensor,
