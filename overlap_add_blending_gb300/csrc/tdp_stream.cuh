@@ -104,14 +104,18 @@ struct __align__(16) RunEnt {
 // Blend: the column tiles ("terms") touching one 16-byte output chunk, each
 // with its tile row's bytes and the chunk's byte offset in the tile row
 // (may be negative), r_w per column (0 where the tile does not reach) and
-// the columns it reaches (bit m: column m of the chunk).
+// the columns it reaches (bit m: column m of the chunk).  The entries are
+// ordered by class -- 0: one term reaching every column with r_w = 1; 1:
+// one term otherwise; 2, 3: two, three terms -- and `col` is the chunk
+// column an entry describes.
 struct __align__(16) ChunkEnt {
     int nq;
     int iw[3], swb[3], xob[3];
     float rw[3][8];
     uint32_t in[3];
-    int pad[2];
+    int col, cls;
 };
+constexpr int kChunkClasses = 4;
 
 struct StreamArgs {
     const void* src;          // extract: latent; blend: packed tiles
@@ -123,6 +127,7 @@ struct StreamArgs {
     int nstages, stage_bytes;
     int run_slot, max_runs, runs_per_band;   // blend: shared bytes per staged run, runs per unit, per band
     int cpr, rbh;             // blend: 16-byte chunks per latent row, rows per compute thread
+    int ncls[4];              // blend: chunk entries per class, in table order
     int esz;                  // element size of the staged data (extract: latent; blend: tiles)
     // tables, as 16-byte word offsets into StreamTables (and its shared copy)
     int t_band, t_frame, t_row, t_hs, t_fcon, t_wcon, t_runs, t_chunk, t_words;
@@ -490,6 +495,7 @@ template <typename Tin, int E, int KT>
 struct ColTerms {
     static constexpr int NW = E * static_cast<int>(sizeof(Tin)) / 4;   // raw words per window
     int nq;                 // column tiles touching the chunk (<= KT)
+    bool one;               // one term reaching every column of the chunk (no masking needed)
     int iw[KT];             // column tile
     int swb[KT], xob[KT];   // tile row bytes; byte offset of column j*E in the tile row (may be < 0)
     float2 rw[KT][E / 2];   // r_w per column (0 where the tile does not reach)
@@ -500,6 +506,7 @@ template <typename Tin, int E, int KT>
 __device__ __forceinline__ void col_terms(const ChunkEnt& c, ColTerms<Tin, E, KT>& t) {
     constexpr int esz = static_cast<int>(sizeof(Tin));
     t.nq = c.nq;
+    t.one = c.nq == 1 && c.in[0] == (1u << E) - 1;
 #pragma unroll
     for (int q = 0; q < KT; ++q) {
         t.iw[q] = c.iw[q];
@@ -518,8 +525,10 @@ __device__ __forceinline__ void col_terms(const ChunkEnt& c, ColTerms<Tin, E, KT
     }
 }
 
-// inner += r_w * (term q's masked window at shared offset `ad`), per fp32 pair.
-template <typename Tin, int E, int KT>
+// inner += r_w * (term q's masked window at shared offset `ad`), per fp32
+// pair.  MASK false: the term reaches every column of the chunk (its mask is
+// all ones), so the window is used as loaded.
+template <typename Tin, int E, int KT, bool MASK = true>
 __device__ __forceinline__ void add_term(const unsigned char* smem, uint32_t ad, const ColTerms<Tin, E, KT>& t, int q,
                                          float2 (&inner)[E / 2], uint32_t lo, uint32_t hi) {
     constexpr int esz = static_cast<int>(sizeof(Tin));
@@ -528,8 +537,10 @@ __device__ __forceinline__ void add_term(const unsigned char* smem, uint32_t ad,
     if (index_bad((ad & ~3u) < lo || (ad & ~3u) + 4u * (NW + 1) > hi)) return;
     uint32_t w[NW];
     lds_words_at<esz, NW>(smem, ad, w);
+    if constexpr (MASK) {
 #pragma unroll
-    for (int k = 0; k < NW; ++k) w[k] &= t.wmask[q][k];
+        for (int k = 0; k < NW; ++k) w[k] &= t.wmask[q][k];
+    }
     float2 x[E / 2];
     if constexpr (esz == 2) {
 #pragma unroll
@@ -552,6 +563,31 @@ __device__ __forceinline__ void store_chunk(unsigned char* dst, const float2 (&a
     } else {
         stg_u4(dst, make_uint4(__float_as_uint(acc[0].x), __float_as_uint(acc[0].y), __float_as_uint(acc[1].x),
                                __float_as_uint(acc[1].y)));
+    }
+}
+
+// The output chunk of a term whose weights are all 1: its elements, as the
+// weighted sum computes them (fma(1, x, 0) = x, then rounded to Tout).
+template <typename Tin, typename Tout, int E>
+__device__ __forceinline__ void copy_chunk(const unsigned char* smem, uint32_t ad, unsigned char* dst, uint32_t lo,
+                                           uint32_t hi) {
+    constexpr int esz = static_cast<int>(sizeof(Tin));
+    constexpr int NW = E * esz / 4;
+    if (index_bad((ad & ~3u) < lo || (ad & ~3u) + 4u * (NW + 1) > hi)) return;
+    uint32_t w[NW];
+    lds_words_at<esz, NW>(smem, ad, w);
+    if constexpr (sizeof(Tin) == sizeof(Tout)) {
+        stg_u4(dst, make_uint4(w[0], w[1], w[2], w[3]));
+    } else {
+        float2 acc[E / 2];
+        if constexpr (esz == 2) {
+#pragma unroll
+            for (int k = 0; k < E / 2; ++k) acc[k] = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
+        } else {
+#pragma unroll
+            for (int k = 0; k < E / 2; ++k) acc[k] = make_float2(__uint_as_float(w[2 * k]), __uint_as_float(w[2 * k + 1]));
+        }
+        store_chunk<Tout, E>(dst, acc);
     }
 }
 
@@ -651,14 +687,37 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
         return;
     }
 
-    // ---- compute warps
-    const int cpr = a.cpr;
-    const int RG = kThreads / cpr;
-    const int rg = static_cast<int>(threadIdx.x) / cpr, jc = static_cast<int>(threadIdx.x) - rg * cpr;
-    const bool active = rg < RG;
+    // ---- compute warps.  Thread t takes one (row group, chunk entry) pair,
+    // class by class: the entries of class c (chunk table order) times the
+    // RG row groups fill threads [RG * (entries before c), RG * (entries
+    // through c)), row group major, so that the lanes of a warp mostly share
+    // one class and one row cover.
+    const int RG = kThreads / a.cpr;
+    int rg = 0, ent = 0, cls = 0;
+    bool active = false;
+    {
+        const int t = static_cast<int>(threadIdx.x);
+        int before = 0;
+#pragma unroll
+        for (int q = 0; q < kChunkClasses; ++q) {
+            const int nc = a.ncls[q];
+            if (nc > 0 && t >= before * RG && t < (before + nc) * RG) {
+                const int l = t - before * RG;
+                rg = l / nc;
+                ent = before + (l - rg * nc);
+                cls = q;
+                active = true;
+            }
+            before += nc;
+        }
+    }
     const int r_lo = rg * a.rbh;   // this thread's rows of a band: [r_lo, r_lo + rbh)
     ColTerms<Tin, E, KT> tm;
-    if (active) col_terms<Tin, E, KT>(m.chunks[jc], tm);
+    int jc = 0;
+    if (active) {
+        col_terms<Tin, E, KT>(m.chunks[ent], tm);
+        jc = m.chunks[ent].col;
+    }
     unsigned char* out = static_cast<unsigned char*>(a.dst);
     const uint32_t ring_lo = static_cast<uint32_t>(a.off_data);   // (index checks) the staged data
     const uint32_t ring_hi = ring_lo + static_cast<uint32_t>(S * a.stage_bytes);
@@ -683,6 +742,14 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
 #pragma unroll 1
             for (int h = b.hb0 + r_lo; h < h1; ++h) {
                 const RowEnt re = m.rows[h];
+                if (cls == 0 && fe.n == 1 && re.n == 1 && fe.w[0] == 1.0f && re.w[0] == 1.0f) {
+                    // one tile, weight 1 on every axis: the output is its elements
+                    const int* hrun = hdr_f0 + (re.lo - b.ihlo) * nw;
+                    const uint32_t ad = static_cast<uint32_t>(hrun[tm.iw[0]] + (h - m.hs[re.lo]) * tm.swb[0] + tm.xob[0]);
+                    if (!range_bad(oplane + (long long)h * W * osz, 16, out, a.dst_bytes))
+                        copy_chunk<Tin, Tout, E>(smem, ad, oplane + (long long)h * W * osz, ring_lo, ring_hi);
+                    continue;
+                }
                 const int npairs = fe.n * re.n;
                 float2 acc[E / 2];
 #pragma unroll
@@ -698,14 +765,18 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
                     float2 inner[E / 2];
 #pragma unroll
                     for (int mm = 0; mm < E / 2; ++mm) inner[mm] = make_float2(0.0f, 0.0f);
-                    add_term<Tin, E, KT>(smem, static_cast<uint32_t>(hrun[tm.iw[0]] + yo * tm.swb[0] + tm.xob[0]), tm, 0,
-                                         inner, ring_lo, ring_hi);
-                    if (KT > 1 && tm.nq > 1)
-                        add_term<Tin, E, KT>(smem, static_cast<uint32_t>(hrun[tm.iw[q1]] + yo * tm.swb[q1] + tm.xob[q1]),
-                                             tm, q1, inner, ring_lo, ring_hi);
-                    if (KT > 2 && tm.nq > 2)
-                        add_term<Tin, E, KT>(smem, static_cast<uint32_t>(hrun[tm.iw[q2]] + yo * tm.swb[q2] + tm.xob[q2]),
-                                             tm, q2, inner, ring_lo, ring_hi);
+                    const uint32_t ad0 = static_cast<uint32_t>(hrun[tm.iw[0]] + yo * tm.swb[0] + tm.xob[0]);
+                    if (tm.one) {
+                        add_term<Tin, E, KT, false>(smem, ad0, tm, 0, inner, ring_lo, ring_hi);
+                    } else {
+                        add_term<Tin, E, KT>(smem, ad0, tm, 0, inner, ring_lo, ring_hi);
+                        if (KT > 1 && tm.nq > 1)
+                            add_term<Tin, E, KT>(smem, static_cast<uint32_t>(hrun[tm.iw[q1]] + yo * tm.swb[q1] + tm.xob[q1]),
+                                                 tm, q1, inner, ring_lo, ring_hi);
+                        if (KT > 2 && tm.nq > 2)
+                            add_term<Tin, E, KT>(smem, static_cast<uint32_t>(hrun[tm.iw[q2]] + yo * tm.swb[q2] + tm.xob[q2]),
+                                                 tm, q2, inner, ring_lo, ring_hi);
+                    }
                     const float2 w2 = make_float2(wfh, wfh);
 #pragma unroll
                     for (int mm = 0; mm < E / 2; ++mm) acc[mm] = __ffma2_rn(w2, inner[mm], acc[mm]);
@@ -922,12 +993,13 @@ inline void stream_tables(const tdp_plan_t& p, bool blend, StreamLaunch& L) {
     if (blend) {
         ChunkEnt* chunks = reinterpret_cast<ChunkEnt*>(base + 16 * a.t_chunk);
         const int E = p.dims[2] / a.cpr;   // output elements per chunk
+        std::vector<ChunkEnt> ents(a.cpr);
         for (int jc = 0; jc < a.cpr; ++jc) {
             const int c0 = jc * E;
             int lo, hi, l2, h2;
             tdp::axis_cover(p, 2, c0, lo, hi);
             tdp::axis_cover(p, 2, c0 + E - 1, l2, h2);
-            ChunkEnt& ce = chunks[jc];
+            ChunkEnt& ce = ents[jc];
             std::memset(&ce, 0, sizeof(ce));
             ce.nq = h2 - lo + 1;
             for (int q = 0; q < 3; ++q) {
@@ -944,6 +1016,17 @@ inline void stream_tables(const tdp_plan_t& p, bool blend, StreamLaunch& L) {
                     if (in) ce.in[q] |= 1u << mm;
                 }
             }
+            ce.col = jc;
+            bool ones = ce.nq == 1 && ce.in[0] == (1u << E) - 1;
+            for (int mm = 0; mm < E && ones; ++mm) ones = ce.rw[0][mm] == 1.0f;
+            ce.cls = ones ? 0 : std::min(ce.nq, kChunkClasses - 1);
+        }
+        // entries grouped by class (stable), so that a warp's chunks share one
+        std::stable_sort(ents.begin(), ents.end(), [](const ChunkEnt& x, const ChunkEnt& y) { return x.cls < y.cls; });
+        for (int c = 0; c < kChunkClasses; ++c) a.ncls[c] = 0;
+        for (int k = 0; k < a.cpr; ++k) {
+            chunks[k] = ents[k];
+            ++a.ncls[ents[k].cls];
         }
     }
 }

@@ -103,9 +103,9 @@ COVER = np.dtype([("lo", "<i4"), ("n", "<i4"), ("w", "<f4", 2)])
 FCON = np.dtype([("base", "<i8"), ("sf", "<i4"), ("fs", "<i4")])
 WCON = np.dtype([("sw", "<i4"), ("ws", "<i4"), ("dq", "<i4"), ("dr", "<i4"), ("inv_sw", "<f4"), ("pad", "<i4", 3)])
 RUN = np.dtype([("A", "<i8"), ("slice", "<i4"), ("vrow", "<i4"), ("len", "<i4"), ("src_rel", "<i4"), ("pad", "<i4", 2)])
-CHUNK = np.dtype({"names": ["nq", "iw", "swb", "xob", "rw", "inb"],
-                  "formats": ["<i4", ("<i4", 3), ("<i4", 3), ("<i4", 3), ("<f4", (3, 8)), ("<u4", 3)],
-                  "offsets": [0, 4, 16, 28, 40, 136], "itemsize": 160})
+CHUNK = np.dtype({"names": ["nq", "iw", "swb", "xob", "rw", "inb", "col", "cls"],
+                  "formats": ["<i4", ("<i4", 3), ("<i4", 3), ("<i4", 3), ("<f4", (3, 8)), ("<u4", 3), "<i4", "<i4"],
+                  "offsets": [0, 4, 16, 28, 40, 136, 148, 152], "itemsize": 160})
 
 
 
@@ -161,14 +161,24 @@ def check_tables(p, g, buf, offs, BC, esz_stage, blend):
     cpr = g["chunks_per_row"]
     E = W // cpr
     chunks = np.frombuffer(buf, CHUNK, cpr, 16 * offs["chunk"])
-    for j in range(cpr):
+    # every chunk column once, the entries ordered by class: 0 = one term
+    # reaching all E columns with r_w = 1, 1 = one term otherwise, 2 / 3 =
+    # two / three terms; within a class in column order
+    assert sorted(chunks["col"]) == list(range(cpr))
+    assert list(chunks["cls"]) == sorted(chunks["cls"])
+    for k in range(cpr):
+        c = chunks[k]
+        j = int(c["col"])
         terms = col_terms(p, j, E)
-        c = chunks[j]
         assert c["nq"] == len(terms)
         for q, (iw, sw, xo, inn, rw) in enumerate(terms):
             assert (c["iw"][q], c["swb"][q], c["xob"][q]) == (iw, sw * esz_stage, xo * esz_stage)
             assert np.array_equal(c["rw"][q][:E], rw), (j, q)
             assert c["inb"][q] == sum(1 << m for m in range(E) if inn[m])
+        ones = len(terms) == 1 and all(terms[0][3][:E]) and np.all(terms[0][4] == 1.0)
+        assert c["cls"] == (0 if ones else min(len(terms), 3)), j
+        if k > 0 and chunks[k - 1]["cls"] == c["cls"]:
+            assert chunks[k - 1]["col"] < j
 
 
 # ----------------------------------------------------------------- extract
