@@ -204,8 +204,9 @@ __device__ __forceinline__ void lds_words_at(const unsigned char* smem, uint32_t
     }
 }
 
+// A 16-byte store of output written once (streaming: evict-first in L2).
 __device__ __forceinline__ void stg_u4(void* p, const uint4& v) {
-    *reinterpret_cast<uint4*>(p) = v;
+    __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
 // Decodes unit u = (f * nbands + band) * BC + bc into (bc, f, band) and
@@ -285,7 +286,8 @@ __device__ __forceinline__ StreamSmem stream_prologue(const StreamArgs& a, const
 
 // =================================================================== extract
 // Staging: the band's latent rows, one contiguous aligned span, one bulk
-// copy by the producer warp's lane 0.
+// copy by the producer warp's lane 0 (evict-first in L2: read once, while
+// the tiles written here are read next by the blend).
 // Writing: for every covering (frame tile, row tile, column tile), the run
 // of that tile's rows inside the band is a contiguous span of the packed
 // tiles.  The spans of successive units are dealt to the warps round robin
@@ -335,7 +337,7 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
                             !index_bad(static_cast<int>(bytes) > a.stage_bytes - 2 * kStreamPad);
             fence_proxy_async();   // the compute warps' reads of this stage come before the copy's writes
             mbar_arrive_expect_tx(&m.full[s], in ? bytes : 0u);
-            if (in) bulk_copy_g2s(smem + a.off_data + s * a.stage_bytes + kStreamPad, g, bytes, &m.full[s]);
+            if (in) bulk_copy_g2s_once(smem + a.off_data + s * a.stage_bytes + kStreamPad, g, bytes, &m.full[s]);
         }
         if (!ok) {
             atomicOr(&g_device_error, kErrExtractWait);
@@ -677,7 +679,8 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
                 __syncwarp();
 #pragma unroll
                 for (int i = 0; i < kRunsPerLane; ++i)
-                    if (cp_n[i]) bulk_copy_g2s(smem + cp_slot[i], reinterpret_cast<const void*>(cp_lo[i]), cp_n[i], &m.full[s]);
+                    if (cp_n[i])
+                        bulk_copy_g2s_once(smem + cp_slot[i], reinterpret_cast<const void*>(cp_lo[i]), cp_n[i], &m.full[s]);
             }
         }
         if (!ok && lane == 0) {
