@@ -143,6 +143,7 @@ struct StreamArgs {
 constexpr int kJobNone = 0, kJobExtent = 1;
 constexpr int kChunkLead = 5;   // units before a CTA's last at which its last chunk's loads are issued
 struct StreamJobs {
+    static constexpr bool kEnabled = true;
     int kind;                       // kJobNone or kJobExtent
     int B;                          // pair j is (tile j / B, batch j % B)
     int K1;                         // chunks per pair: chunk q is pair q / K1, part q % K1
@@ -154,6 +155,13 @@ struct StreamJobs {
     int* zero_b;                    // (the finishing launch's counters)
     int nzero_a, nzero_b;
     tdp_plan_t p;
+};
+
+// The launch argument of an extract without jobs (a plain tdp_extract): a
+// separate instantiation, so that it carries neither the job parameters
+// nor their registers.
+struct NoJobs {
+    static constexpr bool kEnabled = false;
 };
 
 // Ints the extract launch sets to zero for the launch after it.
@@ -301,19 +309,23 @@ __device__ __forceinline__ StreamSmem stream_prologue(const StreamArgs& a, const
 // (row, column) and band address incrementally.  The few elements before
 // the first boundary and after the last whole group are written one by one
 // by lanes 0-7 and 8-15.
-template <typename E>
+template <typename E, typename J>
 __global__ void __launch_bounds__(kStreamExtractThreads, 1)
     extract_stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ StreamSplit sp,
-                          const __grid_constant__ StreamTables tb, const __grid_constant__ StreamJobs jb) {
+                          const __grid_constant__ StreamTables tb, const __grid_constant__ J jb) {
     constexpr int esz = static_cast<int>(sizeof(E));
     constexpr int EPQ = 8 / esz;   // elements per 8-byte group
     constexpr int kWarps = kStreamExtractWarps;
     extern __shared__ __align__(128) unsigned char smem[];
     const StreamSmem m = stream_prologue(a, tb, smem, 1, kWarps);
     const int first = sp.start[blockIdx.x], last = sp.start[blockIdx.x + 1];
-    const int job0 = jb.kind == kJobExtent ? jb.start[blockIdx.x] : 0;
-    const int job1 = jb.kind == kJobExtent ? jb.start[blockIdx.x + 1] : 0;
-    const bool zeroes = jb.kind == kJobExtent && blockIdx.x == 0;
+    int job0 = 0, job1 = 0;
+    bool zeroes = false;
+    if constexpr (J::kEnabled) {
+        job0 = jb.kind == kJobExtent ? jb.start[blockIdx.x] : 0;
+        job1 = jb.kind == kJobExtent ? jb.start[blockIdx.x + 1] : 0;
+        zeroes = jb.kind == kJobExtent && blockIdx.x == 0;
+    }
     if (first >= last && job0 >= job1 && !zeroes) return;
     const int S = a.nstages, n = last - first;
     const int F = a.F, H = a.H, W = a.W, nw = a.nw;
@@ -353,28 +365,37 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
     // the loads' latency hides behind the units and no barrier stops the
     // warps.
     using G = WarpsGroup<32 * kWarps>;
-    int* const jsh = reinterpret_cast<int*>(smem + jb.off_job);
-    int2* const cdata = reinterpret_cast<int2*>(smem + jb.off_job + 4 * kChunkShInts);
-    if (zeroes) {
-        for (int i = threadIdx.x; i < jb.nzero_a; i += 32 * kWarps) jb.zero_a[i] = 0;
-        for (int i = threadIdx.x; i < jb.nzero_b; i += 32 * kWarps) jb.zero_b[i] = 0;
-    }
-    const bool async_chunk = job1 > job0;
-    for (int q = job0; q < job1 - 1; ++q) extent_chunk<G>(jb.p, jb.gen, jb.B, jb.K1, q, jb.partials, jsh);
-    if (async_chunk) {
-        chunk_slot_init(jb.partials, job1 - 1);
-        G::sync();   // the slot is set before any warp adds to it
+    int* jsh = nullptr;
+    int2* cdata = nullptr;
+    bool async_chunk = false;
+    if constexpr (J::kEnabled) {
+        jsh = reinterpret_cast<int*>(smem + jb.off_job);
+        cdata = reinterpret_cast<int2*>(smem + jb.off_job + 4 * kChunkShInts);
+        if (zeroes) {
+            for (int i = threadIdx.x; i < jb.nzero_a; i += 32 * kWarps) jb.zero_a[i] = 0;
+            for (int i = threadIdx.x; i < jb.nzero_b; i += 32 * kWarps) jb.zero_b[i] = 0;
+        }
+        async_chunk = job1 > job0;
+        for (int q = job0; q < job1 - 1; ++q) extent_chunk<G>(jb.p, jb.gen, jb.B, jb.K1, q, jb.partials, jsh);
+        if (async_chunk) {
+            chunk_slot_init(jb.partials, job1 - 1);
+            G::sync();   // the slot is set before any warp adds to it
+        }
     }
     const int k_issue = max(0, n - kChunkLead);         // the last chunk's loads go out before this unit
     const int k_fin = max(k_issue, n - 2);               // and each warp reduces its share after this one
     bool chunk_done = !async_chunk;
-    if (async_chunk && n == 0) extent_chunk_issue<G>(jb.p, jb.gen, jb.B, jb.K1, job1 - 1, cdata);
+    if constexpr (J::kEnabled) {
+        if (async_chunk && n == 0) extent_chunk_issue<G>(jb.p, jb.gen, jb.B, jb.K1, job1 - 1, cdata);
+    }
     unsigned char* tiles = static_cast<unsigned char*>(a.dst);
     UnitCursor c;
     c.init(first, a.BC, a.nbands);
     int rot = 0;   // the warp that takes the unit's first span: the spans are dealt round robin across units
     for (int k = 0; k < n; ++k, c.next()) {
-        if (async_chunk && k == k_issue) extent_chunk_issue<G>(jb.p, jb.gen, jb.B, jb.K1, job1 - 1, cdata);
+        if constexpr (J::kEnabled) {
+            if (async_chunk && k == k_issue) extent_chunk_issue<G>(jb.p, jb.gen, jb.B, jb.K1, job1 - 1, cdata);
+        }
         const int s = k % S;
         if (!mbar_wait_bounded(&m.full[s], (k / S) & 1)) {
             if (lane == 0) atomicOr(&g_device_error, kErrExtractWait);
@@ -459,14 +480,18 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&m.empty[s]);
-        if (k == k_fin && !chunk_done) {
-            extent_chunk_finish<G>(jb.p, jb.B, jb.K1, job1 - 1, cdata, jb.partials);
-            chunk_done = true;
+        if constexpr (J::kEnabled) {
+            if (k == k_fin && !chunk_done) {
+                extent_chunk_finish<G>(jb.p, jb.B, jb.K1, job1 - 1, cdata, jb.partials);
+                chunk_done = true;
+            }
         }
     }
     // (a CTA without units, or a warp that gave up waiting: its copies
     // must land before the CTA's shared memory goes)
-    if (!chunk_done) extent_chunk_finish<G>(jb.p, jb.B, jb.K1, job1 - 1, cdata, jb.partials);
+    if constexpr (J::kEnabled) {
+        if (!chunk_done) extent_chunk_finish<G>(jb.p, jb.B, jb.K1, job1 - 1, cdata, jb.partials);
+    }
 }
 
 // =================================================================== blend
@@ -1241,7 +1266,8 @@ tdp_status launch_extract_stream(const tdp_plan_t& p, int BC, const void* latent
         jobs.K1 = K1;
         jobs.scratch = 4 * kChunkShInts + 24 * ((nmax + K1 - 1) / K1);
     }
-    tdp_status st = stream_prepare(extract_stream_kernel<E>, p, false, BC, esz, esz, L, jobs);
+    tdp_status st = gen ? stream_prepare(extract_stream_kernel<E, StreamJobs>, p, false, BC, esz, esz, L, jobs)
+                        : stream_prepare(extract_stream_kernel<E, NoJobs>, p, false, BC, esz, esz, L, jobs);
     if (st == TDP_ERR_UNSUPPORTED) return TDP_OK;
     if (st != TDP_OK) return st;
     L.a.src = latent;
@@ -1255,7 +1281,11 @@ tdp_status launch_extract_stream(const tdp_plan_t& p, int BC, const void* latent
     L.jb.zero_b = zero.b;
     L.jb.nzero_b = zero.b ? zero.nb : 0;
     *taken = true;
-    return launch(extract_stream_kernel<E>, L.grid, kStreamExtractThreads, L.smem, stream, 1, L.a, L.sp, L.tb, L.jb);
+    if (!gen)
+        return launch(extract_stream_kernel<E, NoJobs>, L.grid, kStreamExtractThreads, L.smem, stream, 1, L.a, L.sp, L.tb,
+                      NoJobs{});
+    return launch(extract_stream_kernel<E, StreamJobs>, L.grid, kStreamExtractThreads, L.smem, stream, 1, L.a, L.sp, L.tb,
+                  L.jb);
 }
 
 // The streaming blend, if it takes the plan (*taken).
