@@ -339,7 +339,7 @@ __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __fl
 // warp storing 32 neighbouring columns of one channel.  With bf16 tokens a
 // chunk j holds two fp32 chunks, kept at j and J + j.
 template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(kTmThreads, 2) blend_tokens_kernel(const __grid_constant__ tdp_plan_t p,
+__global__ void __launch_bounds__(kTmThreads, 3) blend_tokens_kernel(const __grid_constant__ tdp_plan_t p,
                                                                      const TmArgs a) {
     constexpr int VEC = Elems<Tin>::kVec;
     constexpr int FCH = VEC / 4;          // fp32 chunks per 16-byte chunk
