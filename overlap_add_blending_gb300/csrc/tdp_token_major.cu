@@ -183,7 +183,7 @@ __device__ __forceinline__ int swz_extract(int j, int x, int mask, int n) {
 }
 
 template <typename E, bool PAIR>   // raw element: uint16_t (bf16) or uint32_t (fp32); a bit copy
-__global__ void __launch_bounds__(kTmThreads, 3) extract_tokens_kernel(const __grid_constant__ tdp_plan_t p,
+__global__ void __launch_bounds__(kTmThreads, 4) extract_tokens_kernel(const __grid_constant__ tdp_plan_t p,
                                                                        const TmArgs a) {
     constexpr int VEC = 16 / sizeof(E);
     constexpr int NI = PAIR ? kTmItems / 2 : kTmItems;   // items per thread
