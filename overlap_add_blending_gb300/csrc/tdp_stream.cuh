@@ -98,7 +98,8 @@ struct __align__(16) RunEnt {
     int vrow;         // (first band row - tile's first row) * w_t
     int len;          // elements of the run (its rows times w_t)
     int src_rel;      // extract: byte offset of the run's (row 0, column 0) in the staged band
-    int pad[2];
+    int iw;           // its column tile
+    int pad;
 };
 
 // Blend: the column tiles ("terms") touching one 16-byte output chunk, each
@@ -216,6 +217,21 @@ __device__ __forceinline__ void lds_words_at(const unsigned char* smem, uint32_t
 __device__ __forceinline__ void stg_u4(void* p, const uint4& v) {
     __stcs(reinterpret_cast<uint4*>(p), v);
 }
+
+// A position in the ring of S stages: use j of the ring is stage j mod S
+// in its (j / S)-th round, whose parity is the phase a "full" wait on that
+// stage expects (and the one before it, the phase of the "empty" wait
+// before the stage is refilled).  Kept incrementally, without dividing.
+struct RingPos {
+    int s = 0;          // stage
+    uint32_t ph = 0u;   // parity of the round
+    __device__ __forceinline__ void next(int S) {
+        if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
 
 // Decodes unit u = (f * nbands + band) * BC + bc into (bc, f, band) and
 // steps to u + 1 without dividing.
@@ -338,10 +354,11 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
         UnitCursor cs;
         cs.init(first, a.BC, a.nbands);
         int k = 0;
+        RingPos rp;
         bool ok = true;
-        for (; k < n; ++k, cs.next()) {
-            const int s = k % S;
-            if (k >= S && !mbar_wait_backoff(&m.empty[s], ((k / S) - 1) & 1)) { ok = false; break; }
+        for (; k < n; ++k, cs.next(), rp.next(S)) {
+            const int s = rp.s;
+            if (k >= S && !mbar_wait_backoff(&m.empty[s], rp.ph ^ 1u)) { ok = false; break; }
             const BandEnt b = m.bands[cs.band];
             const uint32_t bytes = static_cast<uint32_t>((b.hb1 - b.hb0) * W * esz);
             const unsigned char* g = lat + (((long long)cs.bc * F + cs.f) * H + b.hb0) * (long long)W * esz;
@@ -392,12 +409,13 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
     UnitCursor c;
     c.init(first, a.BC, a.nbands);
     int rot = 0;   // the warp that takes the unit's first span: the spans are dealt round robin across units
-    for (int k = 0; k < n; ++k, c.next()) {
+    RingPos rp;
+    for (int k = 0; k < n; ++k, c.next(), rp.next(S)) {
         if constexpr (J::kEnabled) {
             if (async_chunk && k == k_issue) extent_chunk_issue<G>(jb.p, jb.gen, jb.B, jb.K1, job1 - 1, cdata);
         }
-        const int s = k % S;
-        if (!mbar_wait_bounded(&m.full[s], (k / S) & 1)) {
+        const int s = rp.s;
+        if (!mbar_wait_bounded(&m.full[s], rp.ph)) {
             if (lane == 0) atomicOr(&g_device_error, kErrExtractWait);
             break;   // no release: the producer gives up and drains (the chunk below still meets its barriers)
         }
@@ -413,8 +431,8 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
 #pragma unroll 1
         for (; spn < nspans; spn += kWarps) {
             const int fa = spn >= nr ? 1 : 0, rr = spn - fa * nr;
-            const int iw = rr % nw;
             const RunEnt re = band_runs[rr];
+            const int iw = re.iw;
             const ColCon wc = m.wcon[iw];
             const int sw = wc.sw, len = re.len;
             E* g0 = reinterpret_cast<E*>(tiles) + run_e0(re, m.fcon[fe.lo + fa], a.BC, c.bc, c.f);
@@ -644,15 +662,16 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
         UnitCursor cs;
         cs.init(first, a.BC, a.nbands);
         int j = 0;   // stages filled so far
+        RingPos rp;  // stage j's place in the ring
         bool ok = true;
         for (int k = 0; k < n && ok; ++k, cs.next()) {
             const BandEnt b = m.bands[cs.band];
             const FrameEnt fe = m.frames[cs.f];
             const int nr = b.NHB * nw;
             const RunEnt* band_runs = m.runs + cs.band * a.runs_per_band;
-            for (int fa = 0; fa < fe.n; ++fa, ++j) {
-                const int s = j % S;
-                const bool lane_ok = j < S || mbar_wait_backoff(&m.empty[s], ((j / S) - 1) & 1);
+            for (int fa = 0; fa < fe.n; ++fa, ++j, rp.next(S)) {
+                const int s = rp.s;
+                const bool lane_ok = j < S || mbar_wait_backoff(&m.empty[s], rp.ph ^ 1u);
                 if (!__all_sync(0xffffffffu, lane_ok)) { ok = false; break; }
                 const FrameCon fc = m.fcon[fe.lo + fa];
                 const uint32_t stage_off = static_cast<uint32_t>(a.off_data + s * a.stage_bytes + kStreamPad);
@@ -751,12 +770,14 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
     const uint32_t ring_hi = ring_lo + static_cast<uint32_t>(S * a.stage_bytes);
     UnitCursor c;
     c.init(first, a.BC, a.nbands);
-    int j = 0;   // the unit's first stage
+    RingPos r0;   // the unit's first stage
     for (int k = 0; k < n; ++k, c.next()) {
         const FrameEnt fe = m.frames[c.f];
-        const int s0 = j % S, s1 = (j + 1) % S;
-        bool landed = mbar_wait_bounded(&m.full[s0], (j / S) & 1);
-        if (landed && fe.n > 1) landed = mbar_wait_bounded(&m.full[s1], ((j + 1) / S) & 1);
+        RingPos r1 = r0;   // the one after it
+        r1.next(S);
+        const int s0 = r0.s, s1 = r1.s;
+        bool landed = mbar_wait_bounded(&m.full[s0], r0.ph);
+        if (landed && fe.n > 1) landed = mbar_wait_bounded(&m.full[s1], r1.ph);
         if (!landed) {
             if (lane == 0) atomicOr(&g_device_error, kErrBlendWait);
             return;   // no release: the producer gives up and drains
@@ -818,7 +839,8 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
             mbar_arrive(&m.empty[s0]);
             if (fe.n > 1) mbar_arrive(&m.empty[s1]);
         }
-        j += fe.n;
+        r0 = r1;
+        if (fe.n > 1) r0.next(S);
     }
 }
 
@@ -1014,6 +1036,7 @@ inline void stream_tables(const tdp_plan_t& p, bool blend, StreamLaunch& L) {
                 r.vrow = (r0 - hs) * sw;
                 r.len = (r1 - r0) * sw;
                 r.src_rel = ((r0 - b.hb0) * p.dims[2] + p.start[2][iw]) * a.esz;
+                r.iw = iw;
             }
             runs[bi * a.runs_per_band + rr] = r;
         }

@@ -102,7 +102,8 @@ BAND = np.dtype([("hb0", "<i4"), ("hb1", "<i4"), ("ihlo", "<i4"), ("NHB", "<i4")
 COVER = np.dtype([("lo", "<i4"), ("n", "<i4"), ("w", "<f4", 2)])
 FCON = np.dtype([("base", "<i8"), ("sf", "<i4"), ("fs", "<i4")])
 WCON = np.dtype([("sw", "<i4"), ("ws", "<i4"), ("dq", "<i4"), ("dr", "<i4"), ("inv_sw", "<f4"), ("pad", "<i4", 3)])
-RUN = np.dtype([("A", "<i8"), ("slice", "<i4"), ("vrow", "<i4"), ("len", "<i4"), ("src_rel", "<i4"), ("pad", "<i4", 2)])
+RUN = np.dtype([("A", "<i8"), ("slice", "<i4"), ("vrow", "<i4"), ("len", "<i4"), ("src_rel", "<i4"), ("iw", "<i4"),
+                ("pad", "<i4")])
 CHUNK = np.dtype({"names": ["nq", "iw", "swb", "xob", "rw", "inb", "col", "cls"],
                   "formats": ["<i4", ("<i4", 3), ("<i4", 3), ("<i4", 3), ("<f4", (3, 8)), ("<u4", 3), "<i4", "<i4"],
                   "offsets": [0, 4, 16, 28, 40, 136, 148, 152], "itemsize": 160})
@@ -142,6 +143,7 @@ def check_tables(p, g, buf, offs, BC, esz_stage, blend):
                 want = (p.prefix[1][ih] * SW + sh * p.prefix[2][iw], sh * sw, (r0 - hs) * sw, (r1 - r0) * sw,
                         ((r0 - hb0) * W + p.start[2][iw]) * esz_stage)
                 assert tuple(runs[b, rr])[:5] == want, (b, rr)
+                assert runs[b, rr]["iw"] == iw, (b, rr)   # the run's column tile, read instead of rr mod nw
     if not blend:
         wcon = np.frombuffer(buf, WCON, nw, 16 * offs["wcon"])
         for i in range(nw):
