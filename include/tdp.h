@@ -515,10 +515,9 @@ tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum
  *            with grid + 1 entries when cta_start_len > grid.
  * tables:    host buffer of tables_bytes bytes, or NULL; receives the plan
  *            tables passed with the launch (table_bytes of them, at most
- *            tables_bytes) and, in table_offsets (8 int32, or NULL), the
+ *            tables_bytes) and, in table_offsets (7 int32, or NULL), the
  *            16-byte word offsets of its sections: bands, frames, rows,
- *            row-tile starts, frame-tile constants, column-tile constants,
- *            runs, chunks.
+ *            frame-tile constants, column-tile constants, runs, chunks.
  */
 typedef struct {
     int32_t streaming;

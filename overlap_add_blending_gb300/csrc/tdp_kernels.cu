@@ -3079,8 +3079,7 @@ tdp_status tdp_launch_geometry(const tdp_plan_t* plan, int32_t B, int32_t C, int
     geometry->table_bytes = 16 * L.a.t_words;
     if (tables) std::memcpy(tables, L.tb.w, static_cast<size_t>(std::min(tables_bytes, 16 * L.a.t_words)));
     if (table_offsets) {
-        const int32_t offs[8] = {L.a.t_band, L.a.t_frame, L.a.t_row, L.a.t_hs, L.a.t_fcon, L.a.t_wcon, L.a.t_runs,
-                                 L.a.t_chunk};
+        const int32_t offs[7] = {L.a.t_band, L.a.t_frame, L.a.t_row, L.a.t_fcon, L.a.t_wcon, L.a.t_runs, L.a.t_chunk};
         std::memcpy(table_offsets, offs, sizeof(offs));
     }
     if (cta_start && cta_start_len > L.grid)

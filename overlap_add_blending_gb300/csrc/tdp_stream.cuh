@@ -99,7 +99,7 @@ struct __align__(16) RunEnt {
     int len;          // elements of the run (its rows times w_t)
     int src_rel;      // extract: byte offset of the run's (row 0, column 0) in the staged band
     int iw;           // its column tile
-    int pad;
+    int r0b;          // blend: its first row (a latent row) times its tile row's bytes
 };
 
 // Blend: the column tiles ("terms") touching one 16-byte output chunk, each
@@ -131,7 +131,7 @@ struct StreamArgs {
     int ncls[4];              // blend: chunk entries per class, in table order
     int esz;                  // element size of the staged data (extract: latent; blend: tiles)
     // tables, as 16-byte word offsets into StreamTables (and its shared copy)
-    int t_band, t_frame, t_row, t_hs, t_fcon, t_wcon, t_runs, t_chunk, t_words;
+    int t_band, t_frame, t_row, t_fcon, t_wcon, t_runs, t_chunk, t_words;
     int off_full, off_empty, off_tab, off_hdr, off_data;   // shared layout (bytes)
 };
 
@@ -268,7 +268,6 @@ struct StreamSmem {
     const BandEnt* bands;      // [nbands]
     const FrameEnt* frames;    // [F]
     const RowEnt* rows;        // [H] (blend)
-    const int* hs;             // [n_h] first row of each row tile (blend)
     const FrameCon* fcon;      // [n_f]
     const ColCon* wcon;        // [n_w] (extract)
     const RunEnt* runs;        // [nbands][runs_per_band]
@@ -291,7 +290,6 @@ __device__ __forceinline__ StreamSmem stream_prologue(const StreamArgs& a, const
     m.bands = reinterpret_cast<const BandEnt*>(tab + a.t_band);
     m.frames = reinterpret_cast<const FrameEnt*>(tab + a.t_frame);
     m.rows = reinterpret_cast<const RowEnt*>(tab + a.t_row);
-    m.hs = reinterpret_cast<const int*>(tab + a.t_hs);
     m.fcon = reinterpret_cast<const FrameCon*>(tab + a.t_fcon);
     m.wcon = reinterpret_cast<const ColCon*>(tab + a.t_wcon);
     m.runs = reinterpret_cast<const RunEnt*>(tab + a.t_runs);
@@ -518,8 +516,10 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
 // tile's runs -- one per (row tile meeting the band, column tile) -- each in
 // its own fixed slot, as the 16-byte chunks around it, one bulk copy per run
 // by the producer warp's lanes (lane l takes runs l, l + 32, ...).  A run's base entry (the
-// shared offset of its slice's tile element (0, 0), as if the whole slice
-// were staged) goes to the run-base table; elements in the tile buffer's
+// shared offset its slice's tile element (0, 0) would have if the whole
+// slice were staged, less the tile's first latent row times its row bytes,
+// so that latent row h of the tile starts at entry + h * row bytes) goes to
+// the run-base table; elements in the tile buffer's
 // last, partial 16 bytes are loaded plainly.  Lane 0 then arrives once on
 // the stage's barrier with the stage's bulk bytes (publishing the warp's
 // entries and plain loads) before the lanes issue their copies: one
@@ -705,7 +705,7 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
                                       a.src_bytes))
                             continue;
                     }
-                    hdr[r] = static_cast<int>(slot + static_cast<uint32_t>(g0 - lo)) - re.vrow * esz;
+                    hdr[r] = static_cast<int>(slot + static_cast<uint32_t>(g0 - lo)) - re.r0b;
                     for (uintptr_t t = (hi > g0 ? hi : g0); t < g1; t += esz)
                         *reinterpret_cast<Tin*>(smem + slot + static_cast<uint32_t>(t - lo)) =
                             *reinterpret_cast<const Tin*>(t);
@@ -794,12 +794,15 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
                 if (cls == 0 && fe.n == 1 && re.n == 1 && fe.w[0] == 1.0f && re.w[0] == 1.0f) {
                     // one tile, weight 1 on every axis: the output is its elements
                     const int* hrun = hdr_f0 + (re.lo - b.ihlo) * nw;
-                    const uint32_t ad = static_cast<uint32_t>(hrun[tm.iw[0]] + (h - m.hs[re.lo]) * tm.swb[0] + tm.xob[0]);
+                    const uint32_t ad = static_cast<uint32_t>(hrun[tm.iw[0]] + h * tm.swb[0] + tm.xob[0]);
                     if (!range_bad(oplane + (long long)h * W * osz, 16, out, a.dst_bytes))
                         copy_chunk<Tin, Tout, E>(smem, ad, oplane + (long long)h * W * osz, ring_lo, ring_hi);
                     continue;
                 }
                 const int npairs = fe.n * re.n;
+                int hx[KT];   // each term's row offset in its tile run: h * row bytes + the chunk's column bytes
+#pragma unroll
+                for (int q = 0; q < KT; ++q) hx[q] = h * tm.swb[q] + tm.xob[q];
                 float2 acc[E / 2];
 #pragma unroll
                 for (int mm = 0; mm < E / 2; ++mm) acc[mm] = make_float2(0.0f, 0.0f);
@@ -810,20 +813,19 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
                     const int ih = re.lo + jh;
                     const float wfh = __fmul_rn(fa ? fe.w[1] : fe.w[0], jh ? re.w[1] : re.w[0]);
                     const int* hrun = (fa ? hdr_f1 : hdr_f0) + (ih - b.ihlo) * nw;
-                    const int yo = h - m.hs[ih];
                     float2 inner[E / 2];
 #pragma unroll
                     for (int mm = 0; mm < E / 2; ++mm) inner[mm] = make_float2(0.0f, 0.0f);
-                    const uint32_t ad0 = static_cast<uint32_t>(hrun[tm.iw[0]] + yo * tm.swb[0] + tm.xob[0]);
+                    const uint32_t ad0 = static_cast<uint32_t>(hrun[tm.iw[0]] + hx[0]);
                     if (tm.one) {
                         add_term<Tin, E, KT, false>(smem, ad0, tm, 0, inner, ring_lo, ring_hi);
                     } else {
                         add_term<Tin, E, KT>(smem, ad0, tm, 0, inner, ring_lo, ring_hi);
                         if (KT > 1 && tm.nq > 1)
-                            add_term<Tin, E, KT>(smem, static_cast<uint32_t>(hrun[tm.iw[q1]] + yo * tm.swb[q1] + tm.xob[q1]),
+                            add_term<Tin, E, KT>(smem, static_cast<uint32_t>(hrun[tm.iw[q1]] + hx[q1]),
                                                  tm, q1, inner, ring_lo, ring_hi);
                         if (KT > 2 && tm.nq > 2)
-                            add_term<Tin, E, KT>(smem, static_cast<uint32_t>(hrun[tm.iw[q2]] + yo * tm.swb[q2] + tm.xob[q2]),
+                            add_term<Tin, E, KT>(smem, static_cast<uint32_t>(hrun[tm.iw[q2]] + hx[q2]),
                                                  tm, q2, inner, ring_lo, ring_hi);
                     }
                     const float2 w2 = make_float2(wfh, wfh);
@@ -922,7 +924,6 @@ inline int stream_table_words(const tdp_plan_t& p, bool blend, StreamArgs& a) {
     a.t_band = o; o += words((long long)a.nbands * sizeof(BandEnt));
     a.t_frame = o; o += words((long long)p.dims[0] * sizeof(FrameEnt));
     a.t_row = o; o += blend ? words((long long)p.dims[1] * sizeof(RowEnt)) : 0;
-    a.t_hs = o; o += blend ? words((long long)p.num_tiles[1] * sizeof(int)) : 0;
     a.t_fcon = o; o += words((long long)p.num_tiles[0] * sizeof(FrameCon));
     a.t_wcon = o; o += blend ? 0 : words((long long)p.num_tiles[2] * sizeof(ColCon));
     a.t_runs = o; o += words((long long)a.nbands * a.runs_per_band * sizeof(RunEnt));
@@ -1001,8 +1002,6 @@ inline void stream_tables(const tdp_plan_t& p, bool blend, StreamLaunch& L) {
             r.w[0] = host_axis_weight(p, 1, lo, h);
             r.w[1] = hi > lo ? host_axis_weight(p, 1, lo + 1, h) : 0.0f;
         }
-        int* hs = reinterpret_cast<int*>(base + 16 * a.t_hs);
-        for (int i = 0; i < p.num_tiles[1]; ++i) hs[i] = p.start[1][i];
     }
     FrameCon* fcon = reinterpret_cast<FrameCon*>(base + 16 * a.t_fcon);
     for (int i = 0; i < p.num_tiles[0]; ++i) {
@@ -1037,6 +1036,7 @@ inline void stream_tables(const tdp_plan_t& p, bool blend, StreamLaunch& L) {
                 r.len = (r1 - r0) * sw;
                 r.src_rel = ((r0 - b.hb0) * p.dims[2] + p.start[2][iw]) * a.esz;
                 r.iw = iw;
+                r.r0b = r0 * sw * a.esz;
             }
             runs[bi * a.runs_per_band + rr] = r;
         }

@@ -246,7 +246,7 @@ def launch_geometry(p: Plan, B: int, C_: int, blend: bool, in_dtype: torch.dtype
     g = LaunchGeometry()
     starts = (C.c_int32 * 1025)()
     buf = (C.c_uint8 * 65536)()
-    offs = (C.c_int32 * 8)()
+    offs = (C.c_int32 * 7)()
     _check(_lib.tdp_launch_geometry(C.byref(p), B, C_, 1 if blend else 0, _dtype_code(in_dtype),
                                     _dtype_code(out_dtype), sm_count, C.byref(g), starts, len(starts),
                                     buf if tables else None, len(buf) if tables else 0, offs),
@@ -255,7 +255,7 @@ def launch_geometry(p: Plan, B: int, C_: int, blend: bool, in_dtype: torch.dtype
     st = [int(v) for v in starts[:d["grid"] + 1]] if d["streaming"] else []
     if not tables:
         return d, st
-    names = ("band", "frame", "row", "hs", "fcon", "wcon", "runs", "chunk")
+    names = ("band", "frame", "row", "fcon", "wcon", "runs", "chunk")
     return d, st, bytes(buf[:d["table_bytes"]]), dict(zip(names, [int(v) for v in offs]))
 
 

@@ -103,7 +103,7 @@ COVER = np.dtype([("lo", "<i4"), ("n", "<i4"), ("w", "<f4", 2)])
 FCON = np.dtype([("base", "<i8"), ("sf", "<i4"), ("fs", "<i4")])
 WCON = np.dtype([("sw", "<i4"), ("ws", "<i4"), ("dq", "<i4"), ("dr", "<i4"), ("inv_sw", "<f4"), ("pad", "<i4", 3)])
 RUN = np.dtype([("A", "<i8"), ("slice", "<i4"), ("vrow", "<i4"), ("len", "<i4"), ("src_rel", "<i4"), ("iw", "<i4"),
-                ("pad", "<i4")])
+                ("r0b", "<i4")])
 CHUNK = np.dtype({"names": ["nq", "iw", "swb", "xob", "rw", "inb", "col", "cls"],
                   "formats": ["<i4", ("<i4", 3), ("<i4", 3), ("<i4", 3), ("<f4", (3, 8)), ("<u4", 3), "<i4", "<i4"],
                   "offsets": [0, 4, 16, 28, 40, 136, 148, 152], "itemsize": 160})
@@ -144,6 +144,7 @@ def check_tables(p, g, buf, offs, BC, esz_stage, blend):
                         ((r0 - hb0) * W + p.start[2][iw]) * esz_stage)
                 assert tuple(runs[b, rr])[:5] == want, (b, rr)
                 assert runs[b, rr]["iw"] == iw, (b, rr)   # the run's column tile, read instead of rr mod nw
+                assert runs[b, rr]["r0b"] == r0 * sw * esz_stage, (b, rr)   # first latent row x tile row bytes
     if not blend:
         wcon = np.frombuffer(buf, WCON, nw, 16 * offs["wcon"])
         for i in range(nw):
@@ -158,8 +159,6 @@ def check_tables(p, g, buf, offs, BC, esz_stage, blend):
         assert (rows[h]["lo"], rows[h]["n"]) == (lo, hi - lo + 1)
         assert rows[h]["w"][0] == weight32(p, 1, lo, h)
         assert rows[h]["w"][1] == (weight32(p, 1, lo + 1, h) if hi > lo else 0)
-    hs = np.frombuffer(buf, "<i4", p.num_tiles[1], 16 * offs["hs"])
-    assert list(hs) == [p.start[1][i] for i in range(p.num_tiles[1])]
     cpr = g["chunks_per_row"]
     E = W // cpr
     chunks = np.frombuffer(buf, CHUNK, cpr, 16 * offs["chunk"])
@@ -322,7 +321,7 @@ def model_blend(p, g, starts, B, C, in_esz, out_esz, tiles_bytes, ctas):
                 smem[off:off + hi - lo] = tiles_bytes[lo:hi]
                 t0 = max(hi, g0)
                 smem[off + t0 - lo:off + g1 - lo] = tiles_bytes[t0:g1]
-                hdr[r] = off + (g0 - lo) - vrow * in_esz
+                hdr[r] = off + (g0 - lo) - r0 * sw * in_esz   # latent row h of the tile starts at hdr + h * row bytes
             fe = [(i, weight32(p, 0, i, f)) for i in range(flo, fhi + 1)]
             for h in range(hb0, hb1):
                 assert (h - hb0) // rbh < RG   # some consumer thread's block holds the row
@@ -338,7 +337,7 @@ def model_blend(p, g, starts, B, C, in_esz, out_esz, tiles_bytes, ctas):
                         for j in range(cpr):
                             inner = np.zeros(E)
                             for (iw, sw, xo, inn, rw) in terms[j]:
-                                ad = hdr[base + iw] + (yo * sw + xo) * in_esz
+                                ad = hdr[base + iw] + (h * sw + xo) * in_esz
                                 check_window(ad, total, E * in_esz, in_esz)
                                 m = np.arange(E)
                                 pos = ad + m * in_esz
