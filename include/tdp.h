@@ -503,9 +503,17 @@ tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum
  *   off_hdr, off_data  shared offsets of the run-base entries and the ring
  *   chunks_per_row  blend: 16-byte output chunks per latent row
  *   column_terms    blend: most column tiles touching one output chunk
- *   rows_per_thread blend: consecutive band rows each thread computes (its
- *                   chunk column of rows [g * n, (g + 1) * n) of every band,
- *                   g = thread / chunks_per_row)
+ *   rows_per_thread blend: most band rows one thread computes in one unit
+ *   class_first[c], row_groups[c], row_step[c]  blend, per chunk class c
+ *                   (0: one term of weight 1 over the whole chunk; 1: one
+ *                   term otherwise; 2, 3: two, three terms): its first
+ *                   compute thread (a warp boundary where the classes fit
+ *                   in whole warps) and G = row_groups[c] threads per chunk
+ *                   entry (0 without entries).  Thread class_first[c] + l,
+ *                   l < n_c * G (n_c the class's entries, in chunk-table
+ *                   order), takes entry l mod n_c and group g = l / n_c,
+ *                   which computes band rows g', g' + G, ... of the CTA's
+ *                   k-th unit, g' = (g + k * row_step[c]) mod G
  *   threads         compute threads of a CTA (the launch adds one producer
  *                   warp)
  *   run_slot        blend: shared bytes of each staged run's slot (run r of
@@ -524,6 +532,7 @@ typedef struct {
     int32_t band_rows, nbands, units, grid, stages, stage_bytes, max_runs, shared_bytes;
     int32_t off_hdr, off_data, chunks_per_row, column_terms, rows_per_thread, threads, run_slot;
     int32_t table_bytes;
+    int32_t class_first[4], row_groups[4], row_step[4];
 } tdp_launch_geometry_t;
 
 tdp_status tdp_launch_geometry(const tdp_plan_t* plan, int32_t B, int32_t C, int32_t blend, tdp_dtype in_dtype,

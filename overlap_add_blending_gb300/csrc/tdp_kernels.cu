@@ -3073,7 +3073,16 @@ tdp_status tdp_launch_geometry(const tdp_plan_t* plan, int32_t B, int32_t C, int
     geometry->off_data = L.a.off_data;
     geometry->chunks_per_row = blend ? L.a.cpr : 0;
     geometry->column_terms = blend ? kt : 0;
-    geometry->rows_per_thread = blend ? L.a.rbh : 0;
+    if (blend) {
+        for (int c = 0; c < kChunkClasses; ++c) {
+            geometry->class_first[c] = L.a.tfirst[c];
+            geometry->row_groups[c] = L.a.grp[c];
+            geometry->row_step[c] = L.a.gstep[c];
+            if (L.a.grp[c] > 0)
+                geometry->rows_per_thread =
+                    std::max(geometry->rows_per_thread, (L.a.band_rows + L.a.grp[c] - 1) / L.a.grp[c]);
+        }
+    }
     geometry->threads = 32 * (blend ? kStreamBlendWarps : kStreamExtractWarps);
     geometry->run_slot = blend ? L.a.run_slot : 0;
     geometry->table_bytes = 16 * L.a.t_words;

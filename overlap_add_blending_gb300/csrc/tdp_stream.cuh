@@ -36,7 +36,7 @@
 // (bounded, with a distinct code if they do not) and returns.
 
 constexpr int kStreamExtractWarps = 24;   // compute warps; one more warp stages
-constexpr int kStreamBlendWarps = 16;
+constexpr int kStreamBlendWarps = 19;   // 20 warps with the producer: 5 per SM sub-partition at up to 96 registers
 constexpr int kStreamExtractThreads = 32 * (kStreamExtractWarps + 1);
 constexpr int kStreamBlendThreads = 32 * (kStreamBlendWarps + 1);
 constexpr int kStreamMaxStageRuns = 64;     // blend: runs per stage, two per producer lane
@@ -127,7 +127,10 @@ struct StreamArgs {
     int BC, band_rows, nbands, n_units;
     int nstages, stage_bytes;
     int run_slot, max_runs, runs_per_band;   // blend: shared bytes per staged run, runs per unit, per band
-    int cpr, rbh;             // blend: 16-byte chunks per latent row, rows per compute thread
+    int cpr;                  // blend: 16-byte chunks per latent row
+    int tfirst[4], grp[4], gstep[4];   // blend, per chunk class: first compute thread, row groups (threads
+                                       // per entry), the groups' step per unit
+    int cwarps;                        // blend: compute warps holding chunk entries (the rest return at once)
     int ncls[4];              // blend: chunk entries per class, in table order
     int esz;                  // element size of the staged data (extract: latent; blend: tiles)
     // tables, as 16-byte word offsets into StreamTables (and its shared copy)
@@ -525,10 +528,11 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
 // entries and plain loads) before the lanes issue their copies: one
 // arrival per stage, as every arrival on one barrier is serialised.
 // Compute: a thread owns one 16-byte output chunk column j (E = 16 / sizeof
-// (Tout) latent columns) for the whole kernel and a block of rbh
-// consecutive rows of every band: rows [rg * rbh, (rg + 1) * rbh), row
-// group rg = thread / chunks per row.  Its column tiles ("terms", at most
-// KT) are fixed, so their offsets, r_w weights and masks live in registers.
+// (Tout) latent columns) for the whole kernel and every G-th row of each
+// band from a start that moves on each unit, G the row groups of its
+// chunk's class (more for the classes with more terms).  Its column tiles
+// ("terms", at most KT) are fixed, so their offsets, r_w weights and masks
+// live in registers.
 // Per output row and covering (frame tile, row tile) pair it forms inner =
 // sum over terms of r_w * value, then acc = fma(w_fh, inner, acc) with
 // w_fh = r_f * r_h rounded: the same weights, grouping and order as the
@@ -643,16 +647,18 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
     constexpr int esz = static_cast<int>(sizeof(Tin));
     constexpr int osz = static_cast<int>(sizeof(Tout));
     constexpr int E = 16 / osz;   // output elements per chunk
-    constexpr int kWarps = kStreamBlendWarps, kThreads = 32 * kStreamBlendWarps;   // compute threads
+    constexpr int kWarps = kStreamBlendWarps;   // compute warps
     constexpr int q1 = KT > 1 ? 1 : 0, q2 = KT > 2 ? 2 : 0;
     extern __shared__ __align__(128) unsigned char smem[];
-    const StreamSmem m = stream_prologue(a, tb, smem, 1, kWarps);
+    // only the compute warps holding chunk entries release stages
+    const StreamSmem m = stream_prologue(a, tb, smem, 1, static_cast<uint32_t>(a.cwarps));
     const int first = sp.start[blockIdx.x], last = sp.start[blockIdx.x + 1];
     if (first >= last) return;
     const int S = a.nstages, n = last - first;
     const int F = a.F, H = a.H, W = a.W, nw = a.nw;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int* const hdr0 = reinterpret_cast<int*>(smem + a.off_hdr);
+    if (warp >= a.cwarps && warp < kWarps) return;   // a compute warp without entries
 
     if (warp == kWarps) {
         // ---- producer warp
@@ -735,30 +741,33 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
     }
 
     // ---- compute warps.  Thread t takes one (row group, chunk entry) pair,
-    // class by class: the entries of class c (chunk table order) times the
-    // RG row groups fill threads [RG * (entries before c), RG * (entries
-    // through c)), row group major, so that the lanes of a warp mostly share
-    // one class and one row cover.
-    const int RG = kThreads / a.cpr;
-    int rg = 0, ent = 0, cls = 0;
+    // class by class: the entries of class c (chunk table order) times its
+    // G_c row groups fill the threads from the class's first (a warp
+    // boundary where the classes fit), row group major, so that the lanes of
+    // a warp share one class and mostly one row cover.  Row group g of an
+    // entry computes band rows g', g' + G_c, ... of the unit, g' = g in the
+    // CTA's first unit and moved on by a fixed step (band rows mod G_c)
+    // each unit, so that the groups with one row more take turns.
+    int G = 1, gp = 0, gstep = 0, ent = 0, cls = 0;
     bool active = false;
     {
         const int t = static_cast<int>(threadIdx.x);
-        int before = 0;
+        int before = 0;   // entries of the classes before q
 #pragma unroll
         for (int q = 0; q < kChunkClasses; ++q) {
-            const int nc = a.ncls[q];
-            if (nc > 0 && t >= before * RG && t < (before + nc) * RG) {
-                const int l = t - before * RG;
-                rg = l / nc;
-                ent = before + (l - rg * nc);
+            const int nc = a.ncls[q], gq = a.grp[q], t0 = a.tfirst[q];
+            if (nc > 0 && t >= t0 && t < t0 + nc * gq) {
+                const int l = t - t0;
+                gp = l / nc;
+                ent = before + (l - gp * nc);
                 cls = q;
+                G = gq;
+                gstep = a.gstep[q];
                 active = true;
             }
             before += nc;
         }
     }
-    const int r_lo = rg * a.rbh;   // this thread's rows of a band: [r_lo, r_lo + rbh)
     ColTerms<Tin, E, KT> tm;
     int jc = 0;
     if (active) {
@@ -787,9 +796,8 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
             const int* hdr_f0 = hdr0 + s0 * a.max_runs;
             const int* hdr_f1 = hdr0 + s1 * a.max_runs;
             unsigned char* oplane = out + ((((long long)c.bc * F + c.f) * H) * W + (long long)jc * E) * osz;
-            const int h1 = min(b.hb1, b.hb0 + r_lo + a.rbh);
 #pragma unroll 1
-            for (int h = b.hb0 + r_lo; h < h1; ++h) {
+            for (int h = b.hb0 + gp; h < b.hb1; h += G) {
                 const RowEnt re = m.rows[h];
                 if (cls == 0 && fe.n == 1 && re.n == 1 && fe.w[0] == 1.0f && re.w[0] == 1.0f) {
                     // one tile, weight 1 on every axis: the output is its elements
@@ -843,6 +851,8 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
         }
         r0 = r1;
         if (fe.n > 1) r0.next(S);
+        gp += gstep;
+        if (gp >= G) gp -= G;
     }
 }
 
@@ -1134,13 +1144,64 @@ inline int host_col_terms(const tdp_plan_t& p, int E) {
     return best;
 }
 
+// Blend: the compute threads of each chunk class c and its row groups G_c
+// (threads per chunk entry).  Each class starts on a warp boundary, so
+// that no warp holds two classes (a warp would run both code paths one
+// after the other), and gets whole warps: first as few as hold one group
+// per entry, then, while warps are left, one more to the class whose
+// threads carry the most rows; G_c is as many groups per entry as its
+// warps hold.  (Weighting the classes by their terms gained nothing on
+// the 4K tiling.)  If the classes do not fit in whole warps they are
+// packed one after another with one group each.  A group's step per unit
+// is band rows mod G_c.
+inline void blend_row_groups(const int (&ncls)[kChunkClasses], int band_rows, int warps, int (&tfirst)[kChunkClasses],
+                             int (&grp)[kChunkClasses], int (&gstep)[kChunkClasses]) {
+    int wc[kChunkClasses], used = 0;
+    for (int c = 0; c < kChunkClasses; ++c) {
+        wc[c] = (ncls[c] + 31) / 32;
+        used += wc[c];
+    }
+    auto groups = [&](int c) { return std::min(band_rows, 32 * wc[c] / ncls[c]); };
+    if (used <= warps) {
+        for (;;) {
+            int best = -1;
+            double worst = 0.0;
+            for (int c = 0; c < kChunkClasses; ++c) {
+                if (ncls[c] == 0 || groups(c) >= band_rows) continue;
+                const double load = static_cast<double>(band_rows) / groups(c);
+                if (load > worst) {
+                    worst = load;
+                    best = c;
+                }
+            }
+            if (best < 0 || used == warps) break;
+            ++wc[best];
+            ++used;
+        }
+        int t = 0;
+        for (int c = 0; c < kChunkClasses; ++c) {
+            tfirst[c] = t;
+            grp[c] = ncls[c] > 0 ? groups(c) : 0;
+            t += 32 * wc[c];
+        }
+    } else {
+        int t = 0;
+        for (int c = 0; c < kChunkClasses; ++c) {
+            tfirst[c] = t;
+            grp[c] = ncls[c] > 0 ? 1 : 0;
+            t += ncls[c];
+        }
+    }
+    for (int c = 0; c < kChunkClasses; ++c) gstep[c] = grp[c] > 0 ? band_rows % grp[c] : 0;
+}
+
 // Picks the band height, the ring, the split and the tables for `sms` SMs
-// (host only).  A band is at least `min_rows` tall -- blend: the row groups,
-// so that every compute thread has a row in every unit; extract: about 2
-// KB of latent, so that the warps' spans are not mostly partial -- and, for
-// blend, a whole multiple of the row groups where possible.  The tallest
-// such band that leaves kStreamUnitsPerCta units per CTA wins; failing that
-// the shortest such band (the most units); failing that any band that fits.
+// (host only).  A band is at least `min_rows` tall -- blend: the compute
+// threads over the chunks per row, so that a thread has about a row in
+// every unit; extract: about 2 KB of latent, so that the warps' spans are
+// not mostly partial.  The tallest such band that leaves kStreamUnitsPerCta
+// units per CTA wins; failing that the shortest such band (the most
+// units); failing that any band that fits.
 inline tdp_status stream_geometry(const tdp_plan_t& p, bool blend, int BC, int esz_src, int esz_dst, int sms,
                                   StreamLaunch& L, const StreamJobPlan& jobs = StreamJobPlan{}) {
     const int F = p.dims[0], H = p.dims[1], W = p.dims[2];
@@ -1155,7 +1216,6 @@ inline tdp_status stream_geometry(const tdp_plan_t& p, bool blend, int BC, int e
         if (heights.empty() || heights.back() != br) heights.push_back(br);
     }
     auto units_of = [&](int br) { return (long long)BC * F * ((H + br - 1) / br); };
-    auto whole = [&](int br) { return !blend || br % rg == 0 || br == H; };
     auto fits = [&](int br) {
         StreamArgs a{};
         a.cpr = cpr;
@@ -1164,11 +1224,9 @@ inline tdp_status stream_geometry(const tdp_plan_t& p, bool blend, int BC, int e
         return units_of(br) <= INT_MAX && stream_layout(p, blend, br, a, smem);
     };
     int chosen = -1;
-    for (int br : heights)   // tallest whole band with enough units that fits
-        if (br >= min_rows && whole(br) && units_of(br) >= want && fits(br)) { chosen = br; break; }
+    for (int br : heights)   // tallest band with enough units that fits
+        if (br >= min_rows && units_of(br) >= want && fits(br)) { chosen = br; break; }
     for (auto it = heights.rbegin(); chosen < 0 && it != heights.rend(); ++it)   // else the most units
-        if (*it >= min_rows && whole(*it) && fits(*it)) chosen = *it;
-    for (auto it = heights.rbegin(); chosen < 0 && it != heights.rend(); ++it)
         if (*it >= min_rows && fits(*it)) chosen = *it;
     for (int br : heights)
         if (chosen < 0 && fits(br)) chosen = br;
@@ -1183,9 +1241,15 @@ inline tdp_status stream_geometry(const tdp_plan_t& p, bool blend, int BC, int e
     L.a.nw = p.num_tiles[2];
     L.a.BC = BC;
     L.a.n_units = BC * F * L.a.nbands;
-    L.a.rbh = blend ? (L.a.band_rows + rg - 1) / rg : 0;
     L.grid = static_cast<int>(std::min<long long>((long long)L.a.n_units, (long long)sms));
     stream_tables(p, blend, L);
+    if (blend) {
+        blend_row_groups(L.a.ncls, L.a.band_rows, kStreamBlendWarps, L.a.tfirst, L.a.grp, L.a.gstep);
+        int end = 0;
+        for (int c = 0; c < kChunkClasses; ++c)
+            if (L.a.ncls[c] > 0) end = std::max(end, L.a.tfirst[c] + L.a.ncls[c] * L.a.grp[c]);
+        L.a.cwarps = (end + 31) / 32;
+    }
     // cost of one unit per (frame, band) group: latent rows plus packed tile rows
     std::vector<long long> gcost;
     for (int f = 0; f < F; ++f)

@@ -176,10 +176,11 @@ class LaunchGeometry(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "streaming", "band_rows", "nbands", "units", "grid", "stages", "stage_bytes", "max_runs", "shared_bytes",
         "off_hdr", "off_data", "chunks_per_row", "column_terms", "rows_per_thread", "threads", "run_slot",
-        "table_bytes")]
+        "table_bytes")] + [(n, C.c_int32 * 4) for n in ("class_first", "row_groups", "row_step")]
 
     def as_dict(self) -> dict:
-        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+        return {n: (list(getattr(self, n)) if n in ("class_first", "row_groups", "row_step") else int(getattr(self, n)))
+                for n, _ in self._fields_}
 
 
 _lib.tdp_launch_geometry.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int32, C.c_int, C.c_int, C.c_int32,

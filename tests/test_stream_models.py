@@ -273,14 +273,27 @@ def model_blend(p, g, starts, B, C, in_esz, out_esz, tiles_bytes, ctas):
     E = 16 // out_esz
     cpr = g["chunks_per_row"]
     assert cpr == W * out_esz // 16 and cpr <= g["threads"]
-    RG = g["threads"] // cpr
-    rbh = g["rows_per_thread"]
-    # the row groups' blocks of rbh rows cover every band row
-    assert RG * rbh >= br
     BC = B * C
     limit = len(tiles_bytes) & ~15
     terms = [col_terms(p, j, E) for j in range(cpr)]
     assert max(len(t) for t in terms) == g["column_terms"]
+    # the row groups of each chunk class (0: one term of weight 1 over the
+    # chunk, 1: one term otherwise, 2/3: two/three terms): every class with
+    # entries has some, their threads fit the CTA, and the step is band rows
+    # mod groups
+    def cls_of(t):
+        return (0 if t[0][3].all() and (t[0][4] == 1).all() else 1) if len(t) == 1 else len(t)
+    ncls = [sum(cls_of(t) == c for t in terms) for c in range(4)]
+    G, step, first = g["row_groups"], g["row_step"], g["class_first"]
+    assert all((G[c] > 0) == (ncls[c] > 0) and G[c] <= br for c in range(4))
+    # the classes' thread ranges follow one another inside the CTA's compute threads, on warp
+    # boundaries when they fit in whole warps
+    ends = [first[c] + ncls[c] * G[c] for c in range(4)]
+    assert all(first[c + 1] >= ends[c] for c in range(3)) and ends[3] <= g["threads"]
+    if sum(-(-n // 32) for n in ncls) <= g["threads"] // 32:
+        assert all(f % 32 == 0 for f in first)
+    assert all(step[c] == (br % G[c] if G[c] else 0) for c in range(4))
+    assert g["rows_per_thread"] == max(-(-br // G[c]) for c in range(4) if G[c])
     out = np.full(BC * F * H * W, np.nan)
     count = np.zeros(BC * F * H * cpr, np.int64)
     for cta in ctas:
@@ -323,8 +336,15 @@ def model_blend(p, g, starts, B, C, in_esz, out_esz, tiles_bytes, ctas):
                 smem[off + t0 - lo:off + g1 - lo] = tiles_bytes[t0:g1]
                 hdr[r] = off + (g0 - lo) - r0 * sw * in_esz   # latent row h of the tile starts at hdr + h * row bytes
             fe = [(i, weight32(p, 0, i, f)) for i in range(flo, fhi + 1)]
+            # the k-th unit's rows of each chunk entry: group g takes rows g', g' + G, ... of the band,
+            # g' = (g + k * step) mod G; every (entry, row) exactly once
+            taken = np.zeros((cpr, hb1 - hb0), np.int64)
+            for jc in range(cpr):
+                c = cls_of(terms[jc])
+                for grp in range(G[c]):
+                    taken[jc, (grp + k * step[c]) % G[c]::G[c]] += 1
+            assert (taken == 1).all()
             for h in range(hb0, hb1):
-                assert (h - hb0) // rbh < RG   # some consumer thread's block holds the row
                 hlo, hhi = cover(p, 1, h)
                 acc = np.zeros((cpr, E))
                 for fa, (i_f, rf) in enumerate(fe):
