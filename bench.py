@@ -689,6 +689,26 @@ def run_tdp(args, rank: int, world: int):
     tmb_ms = time_b2b(tmb, S.n, L, stream, max(200e-6, 3 * L * host_rate(tmb, S.n)))
     del tm_tiles, tm_out
 
+    # The sharded blend: rank 0 of 2's output slab (tdp_shard_plan's rows) of
+    # the same tiles, back to back over the rotating sets.  Bytes: the tile
+    # elements at the slab's rows (every tile meeting them) plus the slab.
+    sh = tdp.shard_plan(p, 2, 0)
+    slab_out = torch.empty((S.n, wl.B, wl.C, wl.dims[0], sh.row1 - sh.row0, wl.dims[2]), dtype=dt, device=dev)
+    slb = lambda i: tdp.blend_slab(p, S.tiles[i], wl.B, wl.C, sh.row0, sh.row1, out=slab_out[i])
+    for i in range(S.n):
+        slb(i)
+    torch.cuda.synchronize()
+    if not torch.equal(slab_out[0], S.X0[:, :, :, sh.row0:sh.row1, :]):
+        raise SystemExit("the slab blend's identity round trip is not exact")
+    slab_ms = time_b2b(slb, S.n, L, stream, max(200e-6, 3 * L * host_rate(slb, S.n)))
+    el_bytes = torch.empty((), dtype=dt).element_size()
+    slab_tile_el = 0
+    for t in range(p.T):
+        (_, t_h0, _), (t_f, t_h, t_w) = p.box(t)
+        slab_tile_el += t_f * t_w * max(0, min(t_h0 + t_h, sh.row1) - max(t_h0, sh.row0))
+    slab_bytes = (wl.B * wl.C * slab_tile_el + slab_out[0].numel()) * el_bytes
+    del slab_out
+
     # The host planner: the layout search for this latent at 8 ranks.
     t0 = time.perf_counter()
     for _ in range(20):
@@ -816,6 +836,10 @@ def run_tdp(args, rank: int, world: int):
                           "blend_tokens": {"ms": tmb_ms, "gbs": ab["blend"] / (tmb_ms * 1e-3) / 1e9},
                           "workload": "the step's latent and tiles with each tile as [B, N_t, C] tokens; "
                                       "back to back over the rotating sets"},
+                      "sharded_blend": {"ms": slab_ms, "gbs": slab_bytes / (slab_ms * 1e-3) / 1e9,
+                                        "rows": [sh.row0, sh.row1], "algorithmic_bytes": int(slab_bytes),
+                                        "workload": "rank 0 of 2: tdp_blend_slab of the step's tiles to output "
+                                                    "rows [row0, row1); back to back over the rotating sets"},
                       "layout_search": {"us": search_us, "ranks": 8, "candidates": len(cands), "picks": picks,
                                         "workload": "host layout search for this latent, frame tiling and "
                                                     "overlaps; mean of 20 calls"}},

@@ -481,8 +481,10 @@ tdp_status tdp_window_sum(const tdp_plan_t* plan, float* max_abs_dev, float* sum
 
 /*
  * tdp_launch_geometry -- how tdp_extract (blend == 0) or tdp_blend
- * (blend == 1) lays out a call with these sizes on a GPU with `sm_count`
- * SMs.  Host only; touches no GPU.  It describes a launch, not a step of
+ * (blend == 1; tdp_blend_slab for output rows [row0, row1) other than
+ * [0, H)) lays out a call with these sizes on a GPU with `sm_count`
+ * SMs.  Extract takes row0 = 0, row1 = H; 0 <= row0 < row1 <= H, else
+ * TDP_ERR_INVALID_ARG.  Host only; touches no GPU.  It describes a launch, not a step of
  * the method: it lets the kernels' index arithmetic be checked on the CPU
  * and a benchmark report the launch configuration.
  *   streaming       1 when the 16-byte streaming kernel takes the call (each
@@ -538,7 +540,7 @@ typedef struct {
 tdp_status tdp_launch_geometry(const tdp_plan_t* plan, int32_t B, int32_t C, int32_t blend, tdp_dtype in_dtype,
                                tdp_dtype out_dtype, int32_t sm_count, tdp_launch_geometry_t* geometry,
                                int32_t* cta_start, int32_t cta_start_len, void* tables, int32_t tables_bytes,
-                               int32_t* table_offsets);
+                               int32_t* table_offsets, int32_t row0, int32_t row1);
 
 /* Diagnostic word of the current device, an OR of
  *   1  an extract kernel gave up waiting for its staged copies (bounded

@@ -2686,13 +2686,13 @@ static_assert(sizeof(tdp_plan_t) + sizeof(BlendArgs) <= 4096, "blend kernel para
 
 template <typename Tin, typename Tout>
 tdp_status launch_blend_stream(const tdp_plan_t& p, int BC, const void* tiles, long long tiles_numel, void* out,
-                               cudaStream_t stream, bool* taken);
+                               cudaStream_t stream, bool* taken, int row0, int row1);
 
 template <typename Tin, typename Tout>
 tdp_status launch_blend(const tdp_plan_t& p, int BC, const void* tiles, long long tiles_numel, void* out,
                         cudaStream_t stream) {
     bool taken = false;
-    const tdp_status sst = launch_blend_stream<Tin, Tout>(p, BC, tiles, tiles_numel, out, stream, &taken);
+    const tdp_status sst = launch_blend_stream<Tin, Tout>(p, BC, tiles, tiles_numel, out, stream, &taken, 0, p.dims[1]);
     if (sst != TDP_OK || taken) return sst;
     int band_rows = p.dims[1];
     BlendLayout L;
@@ -2943,6 +2943,11 @@ tdp_status tdp_blend_slab(const tdp_plan_t* plan, int32_t B, int32_t C, tdp_dtyp
     auto go = [&](auto tin, auto tout) {
         using Ti = decltype(tin);
         using To = decltype(tout);
+        // the streaming blend restricted to the slab's rows where it takes the plan
+        bool taken = false;
+        const tdp_status sst = launch_blend_stream<Ti, To>(*plan, BC, tiles, (long long)BC * tdp::total_volume(*plan),
+                                                           out, stream, &taken, row0, row1);
+        if (sst != TDP_OK || taken) return sst;
         return launch(blend_slab_kernel<Ti, To>, blocks, kThreads, 0, stream, 1, *plan, static_cast<const Ti*>(tiles),
                       (long long)BC * tdp::total_volume(*plan), BC, row0, row1, static_cast<To*>(out));
     };
@@ -3046,9 +3051,11 @@ tdp_status tdp_cond_combine(const tdp_plan_t* plan, int32_t B, int32_t M, int32_
 tdp_status tdp_launch_geometry(const tdp_plan_t* plan, int32_t B, int32_t C, int32_t blend, tdp_dtype in_dtype,
                                tdp_dtype out_dtype, int32_t sm_count, tdp_launch_geometry_t* geometry,
                                int32_t* cta_start, int32_t cta_start_len, void* tables, int32_t tables_bytes,
-                               int32_t* table_offsets) {
+                               int32_t* table_offsets, int32_t row0, int32_t row1) {
     if (!tdp::plan_is_valid(plan) || !geometry || B < 1 || C < 1 || sm_count < 1 || cta_start_len < 0 ||
         tables_bytes < 0)
+        return TDP_ERR_INVALID_ARG;
+    if (row0 < 0 || row1 <= row0 || row1 > plan->dims[1] || (!blend && (row0 != 0 || row1 != plan->dims[1])))
         return TDP_ERR_INVALID_ARG;
     const int isz = dtype_size(in_dtype), osz = dtype_size(out_dtype);
     if (!isz || !osz || (!blend && isz != osz)) return TDP_ERR_INVALID_ARG;
@@ -3057,7 +3064,7 @@ tdp_status tdp_launch_geometry(const tdp_plan_t* plan, int32_t B, int32_t C, int
     int kt = 0;
     if (!stream_eligible(*plan, blend != 0, isz, osz, &kt)) return TDP_OK;
     static thread_local StreamLaunch L;   // 9 KB: kept off the caller's stack
-    const tdp_status st = stream_geometry(*plan, blend != 0, B * C, isz, osz, sm_count, L);
+    const tdp_status st = stream_geometry(*plan, blend != 0, B * C, isz, osz, sm_count, L, StreamJobPlan{}, row0, row1);
     if (st == TDP_ERR_UNSUPPORTED) return TDP_OK;
     if (st != TDP_OK) return st;
     geometry->streaming = 1;

@@ -125,6 +125,8 @@ struct StreamArgs {
     long long dst_bytes;      // size of the destination buffer (index checks of debug builds)
     int F, H, W, nw;          // latent frames, rows, columns; column tiles
     int BC, band_rows, nbands, n_units;
+    int row0, row1;           // the rows [row0, row1) the bands cover (the whole H but for a slab blend,
+                              // whose output holds rows row0.. of each (b, c, f) plane)
     int nstages, stage_bytes;
     int run_slot, max_runs, runs_per_band;   // blend: shared bytes per staged run, runs per unit, per band
     int cpr;                  // blend: 16-byte chunks per latent row
@@ -640,7 +642,10 @@ __device__ __forceinline__ void copy_chunk(const unsigned char* smem, uint32_t a
     }
 }
 
-template <typename Tin, typename Tout, int KT>
+// SLAB: the output holds rows row0 .. row1 - 1 of each (b, c, f) plane (a
+// slab of tdp_blend_slab) rather than all H (its own instantiation, so that
+// the whole-latent blend's code is not touched by the slab's offsets).
+template <typename Tin, typename Tout, int KT, bool SLAB>
 __global__ void __launch_bounds__(kStreamBlendThreads, 1)
     blend_stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ StreamSplit sp,
                         const __grid_constant__ StreamTables tb) {
@@ -655,7 +660,7 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
     const int first = sp.start[blockIdx.x], last = sp.start[blockIdx.x + 1];
     if (first >= last) return;
     const int S = a.nstages, n = last - first;
-    const int F = a.F, H = a.H, W = a.W, nw = a.nw;
+    const int F = a.F, W = a.W, nw = a.nw;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int* const hdr0 = reinterpret_cast<int*>(smem + a.off_hdr);
     if (warp >= a.cwarps && warp < kWarps) return;   // a compute warp without entries
@@ -795,7 +800,14 @@ __global__ void __launch_bounds__(kStreamBlendThreads, 1)
             const BandEnt b = m.bands[c.band];
             const int* hdr_f0 = hdr0 + s0 * a.max_runs;
             const int* hdr_f1 = hdr0 + s1 * a.max_runs;
-            unsigned char* oplane = out + ((((long long)c.bc * F + c.f) * H) * W + (long long)jc * E) * osz;
+            // the byte offset of row h of this chunk column in the output plane of (bc, f) is
+            // obase + h * W * osz (for a slab, obase itself may be negative in its first plane)
+            long long obase;
+            if constexpr (SLAB)
+                obase = ((((long long)c.bc * F + c.f) * (a.row1 - a.row0) - a.row0) * W + (long long)jc * E) * osz;
+            else
+                obase = ((((long long)c.bc * F + c.f) * a.H) * W + (long long)jc * E) * osz;
+            unsigned char* const oplane = out + obase;
 #pragma unroll 1
             for (int h = b.hb0 + gp; h < b.hb1; h += G) {
                 const RowEnt re = m.rows[h];
@@ -912,10 +924,10 @@ struct StreamJobPlan {
 
 // Shared bytes one staged run may take: its 16-byte chunks, at most
 // round16(len) + 16 bytes, for the longest run of any band.
-inline int host_run_slot(const tdp_plan_t& p, int band_rows, int nbands, int esz) {
+inline int host_run_slot(const tdp_plan_t& p, int band_rows, int nbands, int row0, int row1, int esz) {
     int slot = 16;
     for (int bi = 0; bi < nbands; ++bi) {
-        const int hb0 = bi * band_rows, hb1 = std::min(p.dims[1], hb0 + band_rows);
+        const int hb0 = row0 + bi * band_rows, hb1 = std::min(row1, hb0 + band_rows);
         int hlo, hhi;
         tdp::axis_range_cover(p, 1, hb0, hb1, hlo, hhi);
         for (int i_h = hlo; i_h <= hhi; ++i_h) {
@@ -949,15 +961,17 @@ inline int stream_table_words(const tdp_plan_t& p, bool blend, StreamArgs& a) {
 // fit.  a.cpr and a.esz must be set.
 inline bool stream_layout(const tdp_plan_t& p, bool blend, int band_rows, StreamArgs& a, int& smem) {
     const int H = p.dims[1], W = p.dims[2];
+    const int r0 = a.row0, r1 = a.row1;   // the bands' rows
+    if (r0 < 0 || r1 > H || r1 <= r0) return false;
     a.band_rows = band_rows;
-    a.nbands = (H + band_rows - 1) / band_rows;
+    a.nbands = (r1 - r0 + band_rows - 1) / band_rows;
     int nhb_max = 1;
     for (int bi = 0; bi < a.nbands; ++bi)
-        nhb_max = std::max(nhb_max, host_nhb(p, bi * band_rows, std::min(H, bi * band_rows + band_rows)));
+        nhb_max = std::max(nhb_max, host_nhb(p, r0 + bi * band_rows, std::min(r1, r0 + bi * band_rows + band_rows)));
     a.runs_per_band = nhb_max * p.num_tiles[2];
     a.max_runs = blend ? a.runs_per_band : 0;   // one frame tile's runs per stage
     if (a.max_runs > kStreamMaxStageRuns) return false;
-    a.run_slot = blend ? host_run_slot(p, band_rows, a.nbands, a.esz) : 0;
+    a.run_slot = blend ? host_run_slot(p, band_rows, a.nbands, r0, r1, a.esz) : 0;
     const long long data = blend ? (long long)a.max_runs * a.run_slot : (long long)band_rows * W * a.esz;
     if (data > INT_MAX / 8) return false;
     if (stream_table_words(p, blend, a) > kStreamTableWords) return false;
@@ -985,8 +999,8 @@ inline void stream_tables(const tdp_plan_t& p, bool blend, StreamLaunch& L) {
     BandEnt* bands = reinterpret_cast<BandEnt*>(base + 16 * a.t_band);
     for (int bi = 0; bi < a.nbands; ++bi) {
         BandEnt& b = bands[bi];
-        b.hb0 = bi * a.band_rows;
-        b.hb1 = std::min(H, b.hb0 + a.band_rows);
+        b.hb0 = a.row0 + bi * a.band_rows;
+        b.hb1 = std::min(a.row1, b.hb0 + a.band_rows);
         int lo, hi;
         tdp::axis_range_cover(p, 1, b.hb0, b.hb1, lo, hi);
         b.ihlo = lo;
@@ -1203,23 +1217,29 @@ inline void blend_row_groups(const int (&ncls)[kChunkClasses], int band_rows, in
 // units per CTA wins; failing that the shortest such band (the most
 // units); failing that any band that fits.
 inline tdp_status stream_geometry(const tdp_plan_t& p, bool blend, int BC, int esz_src, int esz_dst, int sms,
-                                  StreamLaunch& L, const StreamJobPlan& jobs = StreamJobPlan{}) {
+                                  StreamLaunch& L, const StreamJobPlan& jobs = StreamJobPlan{}, int row0 = 0,
+                                  int row1 = -1) {
     const int F = p.dims[0], H = p.dims[1], W = p.dims[2];
+    if (row1 < 0) row1 = H;
+    if (row0 < 0 || row1 > H || row1 <= row0) return TDP_ERR_UNSUPPORTED;
+    const int HS = row1 - row0;   // the rows the bands split
     sms = std::max(1, std::min(sms, kStreamMaxGrid));
     const int cpr = blend ? W * esz_dst / 16 : 0;
     const int rg = blend ? std::max(1, 32 * kStreamBlendWarps / std::max(1, cpr)) : 1;
-    const int min_rows = std::min(H, blend ? rg : std::max(1, (2048 + W * esz_src - 1) / (W * esz_src)));
+    const int min_rows = std::min(HS, blend ? rg : std::max(1, (2048 + W * esz_src - 1) / (W * esz_src)));
     const long long want = (long long)kStreamUnitsPerCta * sms;
     std::vector<int> heights;   // one per band count, tallest first
-    for (int nb = 1; nb <= H; ++nb) {
-        const int br = (H + nb - 1) / nb;
+    for (int nb = 1; nb <= HS; ++nb) {
+        const int br = (HS + nb - 1) / nb;
         if (heights.empty() || heights.back() != br) heights.push_back(br);
     }
-    auto units_of = [&](int br) { return (long long)BC * F * ((H + br - 1) / br); };
+    auto units_of = [&](int br) { return (long long)BC * F * ((HS + br - 1) / br); };
     auto fits = [&](int br) {
         StreamArgs a{};
         a.cpr = cpr;
         a.esz = esz_src;
+        a.row0 = row0;
+        a.row1 = row1;
         int smem = 0;
         return units_of(br) <= INT_MAX && stream_layout(p, blend, br, a, smem);
     };
@@ -1234,6 +1254,8 @@ inline tdp_status stream_geometry(const tdp_plan_t& p, bool blend, int BC, int e
     std::memset(&L.a, 0, sizeof(L.a));
     L.a.cpr = cpr;
     L.a.esz = esz_src;   // extract stages the latent, blend the tiles
+    L.a.row0 = row0;
+    L.a.row1 = row1;
     if (!stream_layout(p, blend, chosen, L.a, L.smem)) return TDP_ERR_UNSUPPORTED;
     L.a.F = F;
     L.a.H = H;
@@ -1254,7 +1276,7 @@ inline tdp_status stream_geometry(const tdp_plan_t& p, bool blend, int BC, int e
     std::vector<long long> gcost;
     for (int f = 0; f < F; ++f)
         for (int bi = 0; bi < L.a.nbands; ++bi) {
-            const int hb0 = bi * L.a.band_rows, hb1 = std::min(H, hb0 + L.a.band_rows);
+            const int hb0 = row0 + bi * L.a.band_rows, hb1 = std::min(row1, hb0 + L.a.band_rows);
             const long long lat = (long long)(hb1 - hb0) * W * (blend ? esz_dst : esz_src);
             const long long runs =
                 host_run_rows(p, f, hb0, hb1) * p.prefix[2][p.num_tiles[2]] * (blend ? esz_src : esz_dst);
@@ -1321,8 +1343,8 @@ inline bool stream_eligible(const tdp_plan_t& p, bool blend, int esz_src, int es
 // its dynamic shared memory.
 template <typename K>
 tdp_status stream_prepare(K kernel, const tdp_plan_t& p, bool blend, int BC, int esz_src, int esz_dst, StreamLaunch& L,
-                          const StreamJobPlan& jobs = StreamJobPlan{}) {
-    tdp_status st = stream_geometry(p, blend, BC, esz_src, esz_dst, sm_count(), L, jobs);
+                          const StreamJobPlan& jobs = StreamJobPlan{}, int row0 = 0, int row1 = -1) {
+    tdp_status st = stream_geometry(p, blend, BC, esz_src, esz_dst, sm_count(), L, jobs, row0, row1);
     if (st != TDP_OK) return st;
     return cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem));
 }
@@ -1375,27 +1397,33 @@ tdp_status launch_extract_stream(const tdp_plan_t& p, int BC, const void* latent
                   L.jb);
 }
 
-// The streaming blend, if it takes the plan (*taken).
+// The streaming blend of output rows [row0, row1) (out: [BC, F, row1 - row0,
+// W]), if it takes the plan (*taken).
 template <typename Tin, typename Tout>
 tdp_status launch_blend_stream(const tdp_plan_t& p, int BC, const void* tiles, long long tiles_numel, void* out,
-                               cudaStream_t stream, bool* taken) {
+                               cudaStream_t stream, bool* taken, int row0, int row1) {
     constexpr int isz = static_cast<int>(sizeof(Tin)), osz = static_cast<int>(sizeof(Tout));
     *taken = false;
     int kt = 0;
     if (!stream_eligible(p, true, isz, osz, &kt)) return TDP_OK;
     auto go = [&](auto kernel) -> tdp_status {
         static thread_local StreamLaunch L;   // 13 KB: kept off the caller's stack
-        tdp_status st = stream_prepare(kernel, p, true, BC, isz, osz, L);
+        tdp_status st = stream_prepare(kernel, p, true, BC, isz, osz, L, StreamJobPlan{}, row0, row1);
         if (st == TDP_ERR_UNSUPPORTED) return TDP_OK;
         if (st != TDP_OK) return st;
         L.a.src = tiles;
         L.a.dst = out;
         L.a.src_bytes = tiles_numel * isz;
-        L.a.dst_bytes = (long long)BC * p.dims[0] * p.dims[1] * p.dims[2] * osz;
+        L.a.dst_bytes = (long long)BC * p.dims[0] * (row1 - row0) * p.dims[2] * osz;
         *taken = true;
         return launch(kernel, L.grid, kStreamBlendThreads, L.smem, stream, 1, L.a, L.sp, L.tb);
     };
-    if (kt == 1) return go(blend_stream_kernel<Tin, Tout, 1>);
-    if (kt == 2) return go(blend_stream_kernel<Tin, Tout, 2>);
-    return go(blend_stream_kernel<Tin, Tout, 3>);
+    if (row0 != 0 || row1 != p.dims[1]) {
+        if (kt == 1) return go(blend_stream_kernel<Tin, Tout, 1, true>);
+        if (kt == 2) return go(blend_stream_kernel<Tin, Tout, 2, true>);
+        return go(blend_stream_kernel<Tin, Tout, 3, true>);
+    }
+    if (kt == 1) return go(blend_stream_kernel<Tin, Tout, 1, false>);
+    if (kt == 2) return go(blend_stream_kernel<Tin, Tout, 2, false>);
+    return go(blend_stream_kernel<Tin, Tout, 3, false>);
 }

@@ -185,7 +185,7 @@ class LaunchGeometry(C.Structure):
 
 _lib.tdp_launch_geometry.argtypes = [_P(Plan), C.c_int32, C.c_int32, C.c_int32, C.c_int, C.c_int, C.c_int32,
                                      _P(LaunchGeometry), _P(C.c_int32), C.c_int32, C.c_void_p, C.c_int32,
-                                     _P(C.c_int32)]
+                                     _P(C.c_int32), C.c_int32, C.c_int32]
 _lib.tdp_launch_geometry.restype = C.c_int
 
 if _lib.tdp_plan_struct_size() != C.sizeof(Plan):
@@ -239,18 +239,19 @@ def plan_stats(p: Plan, ranks: int = 1) -> PlanStats:
 
 
 def launch_geometry(p: Plan, B: int, C_: int, blend: bool, in_dtype: torch.dtype, out_dtype: torch.dtype,
-                    sm_count: int, tables: bool = False):
+                    sm_count: int, tables: bool = False, rows: Optional[Tuple[int, int]] = None):
     """tdp_launch_geometry: (geometry dict, per-CTA first units) of a tdp_extract
-    (blend False) or tdp_blend call on a GPU with `sm_count` SMs; with
-    tables=True also (the launch's plan tables as bytes, their section
-    offsets in 16-byte words).  Host only."""
+    (blend False) or tdp_blend call (tdp_blend_slab with rows=(row0, row1))
+    on a GPU with `sm_count` SMs; with tables=True also (the launch's plan
+    tables as bytes, their section offsets in 16-byte words).  Host only."""
+    row0, row1 = rows if rows is not None else (0, int(p.dims[1]))
     g = LaunchGeometry()
     starts = (C.c_int32 * 1025)()
     buf = (C.c_uint8 * 65536)()
     offs = (C.c_int32 * 7)()
     _check(_lib.tdp_launch_geometry(C.byref(p), B, C_, 1 if blend else 0, _dtype_code(in_dtype),
                                     _dtype_code(out_dtype), sm_count, C.byref(g), starts, len(starts),
-                                    buf if tables else None, len(buf) if tables else 0, offs),
+                                    buf if tables else None, len(buf) if tables else 0, offs, row0, row1),
            "tdp_launch_geometry")
     d = g.as_dict()
     st = [int(v) for v in starts[:d["grid"] + 1]] if d["streaming"] else []

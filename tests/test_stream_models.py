@@ -110,14 +110,17 @@ CHUNK = np.dtype({"names": ["nq", "iw", "swb", "xob", "rw", "inb", "col", "cls"]
 
 
 
-def check_tables(p, g, buf, offs, BC, esz_stage, blend):
-    """Every entry of the launch's tables against an independent reconstruction."""
+def check_tables(p, g, buf, offs, BC, esz_stage, blend, rows=None):
+    """Every entry of the launch's tables against an independent reconstruction
+    (bands over output rows [r0, r1), the whole H unless a slab)."""
     F, H, W = p.dims
+    w0, w1 = rows or (0, H)   # the bands' rows
     nw, br, nb = p.num_tiles[2], g["band_rows"], g["nbands"]
+    assert nb == -(-(w1 - w0) // br)
     bands = np.frombuffer(buf, BAND, nb, 16 * offs["band"])
-    rpb = max(cover(p, 1, min(H, b * br + br) - 1)[1] - cover(p, 1, b * br)[0] + 1 for b in range(nb)) * nw
+    rpb = max(cover(p, 1, min(w1, w0 + b * br + br) - 1)[1] - cover(p, 1, w0 + b * br)[0] + 1 for b in range(nb)) * nw
     for b in range(nb):
-        hb0, hb1 = b * br, min(H, b * br + br)
+        hb0, hb1 = w0 + b * br, min(w1, w0 + b * br + br)
         lo, hi = cover(p, 1, hb0)[0], cover(p, 1, hb1 - 1)[1]
         assert tuple(bands[b]) == (hb0, hb1, lo, hi - lo + 1)
     frames = np.frombuffer(buf, COVER, F, 16 * offs["frame"])
@@ -132,7 +135,7 @@ def check_tables(p, g, buf, offs, BC, esz_stage, blend):
         assert tuple(fcon[i]) == (p.prefix[0][i] * SH * SW, size(p, 0, i), p.start[0][i])
     runs = np.frombuffer(buf, RUN, nb * rpb, 16 * offs["runs"]).reshape(nb, rpb)
     for b in range(nb):
-        hb0, hb1 = b * br, min(H, b * br + br)
+        hb0, hb1 = w0 + b * br, min(w1, w0 + b * br + br)
         lo = cover(p, 1, hb0)[0]
         for rr in range(rpb):
             jh, iw = divmod(rr, nw)
@@ -264,7 +267,7 @@ def decode(b, esz):
     return (b.view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def model_blend(p, g, starts, B, C, in_esz, out_esz, tiles_bytes, ctas):
+def model_blend(p, g, starts, B, C, in_esz, out_esz, tiles_bytes, ctas, rows=None):
     F, H, W = p.dims
     nw = p.num_tiles[2]
     S, SB, off_data, off_hdr = g["stages"], g["stage_bytes"], g["off_data"], g["off_hdr"]
@@ -294,13 +297,15 @@ def model_blend(p, g, starts, B, C, in_esz, out_esz, tiles_bytes, ctas):
         assert all(f % 32 == 0 for f in first)
     assert all(step[c] == (br % G[c] if G[c] else 0) for c in range(4))
     assert g["rows_per_thread"] == max(-(-br // G[c]) for c in range(4) if G[c])
-    out = np.full(BC * F * H * W, np.nan)
-    count = np.zeros(BC * F * H * cpr, np.int64)
+    w0, w1 = rows or (0, H)   # the output rows (a slab's, else all): out is [BC, F, w1 - w0, W]
+    HS = w1 - w0
+    out = np.full(BC * F * HS * W, np.nan)
+    count = np.zeros(BC * F * HS * cpr, np.int64)
     for cta in ctas:
         j = 0   # stages filled so far: one per covering frame tile of a unit
         for k, u in enumerate(range(starts[cta], starts[cta + 1])):
             bc, f, band = unit_decode(u, BC, nb)
-            hb0, hb1 = band * br, min(H, band * br + br)
+            hb0, hb1 = w0 + band * br, min(w1, w0 + band * br + br)
             flo, fhi = cover(p, 0, f)
             ihlo, ihhi = cover(p, 1, hb0)[0], cover(p, 1, hb1 - 1)[1]
             NHB = ihhi - ihlo + 1
@@ -371,9 +376,9 @@ def model_blend(p, g, starts, B, C, in_esz, out_esz, tiles_bytes, ctas):
                                         "a term reads the wrong tile element"
                                 inner += np.where(inn, rw.astype(np.float64) * np.where(inn, val, 0.0), 0.0)
                             acc[j] += np.float64(wfh) * inner
-                row = ((bc * F + f) * H + h) * W
+                row = ((bc * F + f) * HS + h - w0) * W
                 out[row:row + W] = acc.ravel()
-                count[((bc * F + f) * H + h) * cpr + np.arange(cpr)] += 1
+                count[((bc * F + f) * HS + h - w0) * cpr + np.arange(cpr)] += 1
     return out, count
 
 
@@ -463,6 +468,52 @@ def test_blend_stream_model(T, case):
         done = ~np.isnan(out)
         assert done.sum() > 0
         assert np.allclose(out[done], ref[done], rtol=1e-6, atol=1e-6)
+
+
+SLAB_CASES = [
+    # (dims, tiling, B, C, esz in, esz out, (row0, row1))
+    ((16, 68, 120), ((2, 2), (4, 8), (4, 12)), 1, 2, 2, 2, (0, 34)),      # 4k-class tiling, rank 0 of 2
+    ((16, 68, 120), ((2, 2), (4, 8), (4, 12)), 1, 2, 2, 2, (22, 45)),     # rank 1 of 3: both ends inside overlaps
+    ((16, 68, 120), ((2, 2), (4, 8), (4, 12)), 1, 1, 2, 2, (67, 68)),     # one row
+    ((4, 16, 24), ((1, 0), (2, 4), (2, 6)), 1, 4, 2, 4, (5, 13)),         # bf16 tiles -> fp32 slab
+    ((8, 120, 64), ((2, 1), (4, 8), (2, 8)), 1, 1, 4, 4, (13, 101)),      # two bands, the last one short
+]
+
+
+@pytest.mark.parametrize("case", SLAB_CASES, ids=[f"{c[0]}-{c[6]}" for c in SLAB_CASES])
+def test_blend_slab_stream_model(T, case):
+    """The streaming blend restricted to output rows [row0, row1) (what
+    tdp_blend_slab launches): its tables, its split, and its staging and
+    addressing replayed in NumPy, every slab chunk written once and equal to
+    those rows of the oracle's blend."""
+    dims, tiling, B, C, in_esz, out_esz, rows = case
+    p, rp = _plan_pair(T, dims, tiling)
+    g, starts, buf, offs = T.launch_geometry(p, B, C, True, _dt(in_esz), _dt(out_esz), SMS, tables=True, rows=rows)
+    assert g["streaming"]
+    check_split(starts, g["units"], g["grid"])
+    check_tables(p, g, buf, offs, B * C, in_esz, True, rows=rows)
+    n = p.tiles_numel(B, C)
+    vals = np.random.default_rng(11).standard_normal(n).astype(np.float32)
+    if in_esz == 2:
+        bits = ((vals.view(np.uint32) + 0x7FFF + ((vals.view(np.uint32) >> 16) & 1)) >> 16).astype(np.uint16)
+        tiles_bytes = bits.view(np.uint8).copy()
+        tv = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    else:
+        tiles_bytes = vals.view(np.uint8).copy()
+        tv = vals.astype(np.float64)
+    out, count = model_blend(p, g, starts, B, C, in_esz, out_esz, tiles_bytes, range(g["grid"]), rows=rows)
+    ref = O.blend(rp, O.unpack(rp, B, C, tv))[..., rows[0]:rows[1], :].ravel()
+    assert (count == 1).all(), "a slab chunk is written zero or several times"
+    assert np.allclose(out, ref, rtol=1e-6, atol=1e-6)
+
+
+def test_launch_geometry_rows_checked(T):
+    p = T.plan((4, 16, 16), ((1, 0), (2, 4), (2, 4)))
+    for rows in ((0, 0), (5, 3), (-1, 4), (0, 17)):
+        with pytest.raises(T.TdpError):
+            T.launch_geometry(p, 1, 8, True, _dt(4), _dt(4), SMS, rows=rows)
+    with pytest.raises(T.TdpError):   # extract covers the whole latent
+        T.launch_geometry(p, 1, 8, False, _dt(4), _dt(4), SMS, rows=(0, 8))
 
 
 def test_split_balances_bytes(T):
