@@ -24,9 +24,11 @@ Headline: algorithmic extract+blend bytes per step / step time (GB/s):
 The roofline fraction divides the dominant kernel's achieved GB/s by the
 measured HBM copy bandwidth in MEASURED_PEAKS.json (else a fallback,
 named in the line).  The line also carries the other workloads
-("configs": tiny, stage-1, full-res, the geometry sweep), the CPU oracle's
-throughput on one thread and on every core, and an end-to-end figure
-through host buffers.
+("configs": tiny, stage-1, full-res, the geometry sweep), the rows outside
+the step ("next_rows": the conditioning combine, the token-major pair, one
+rank's slab of the sharded blend, the host layout search), the CPU
+oracle's throughput on one thread and on every core, and an end-to-end
+figure through host buffers.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tdp|reference]
 
