@@ -532,7 +532,7 @@ __global__ void __launch_bounds__(kStreamExtractThreads, 1)
 // Compute: a thread owns one 16-byte output chunk column j (E = 16 / sizeof
 // (Tout) latent columns) for the whole kernel and every G-th row of each
 // band from a start that moves on each unit, G the row groups of its
-// chunk's class (more for the classes with more terms).  Its column tiles
+// chunk's class (each class in whole warps of its own).  Its column tiles
 // ("terms", at most KT) are fixed, so their offsets, r_w weights and masks
 // live in registers.
 // Per output row and covering (frame tile, row tile) pair it forms inner =
