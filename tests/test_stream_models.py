@@ -507,6 +507,24 @@ def test_blend_slab_stream_model(T, case):
     assert np.allclose(out, ref, rtol=1e-6, atol=1e-6)
 
 
+def test_slabs_of_the_4k_workload_stream(T):
+    """Every rank's slab of the 4K-class workload, R = 2..7, takes the
+    streaming blend (tdp_blend_slab's fast path), its bands cover exactly
+    the slab's rows, and every chunk class starts on a warp boundary."""
+    p = T.plan((16, 68, 120), ((2, 2), (4, 8), (4, 12)))
+    for R in range(2, 8):
+        for r in range(R):
+            sh = T.shard_plan(p, R, r)
+            if sh.row0 == sh.row1:
+                continue
+            g, starts = T.launch_geometry(p, 1, 128, True, _dt(2), _dt(2), SMS,
+                                          rows=(sh.row0, sh.row1))
+            assert g["streaming"] == 1, (R, r)
+            assert g["nbands"] == -(-(sh.row1 - sh.row0) // g["band_rows"])
+            assert all(f % 32 == 0 for f in g["class_first"])
+            check_split(starts, g["units"], g["grid"])
+
+
 def test_launch_geometry_rows_checked(T):
     p = T.plan((4, 16, 16), ((1, 0), (2, 4), (2, 4)))
     for rows in ((0, 0), (5, 3), (-1, 4), (0, 17)):
