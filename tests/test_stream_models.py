@@ -525,6 +525,75 @@ def test_slabs_of_the_4k_workload_stream(T):
             check_split(starts, g["units"], g["grid"])
 
 
+def _random_plan(T, rng):
+    """A random plan within the partition-of-unity guard (overlap * (n + 1) <= dim)."""
+    dims = (int(rng.integers(1, 9)), int(rng.integers(8, 97)), 8 * int(rng.integers(2, 25)))
+    tiling = []
+    for d in dims:
+        n = int(rng.integers(1, min(5, d) + 1))
+        tiling.append((n, int(rng.integers(0, d // (n + 1) + 1)) if n > 1 else 0))
+    return T.plan(dims, tuple(tiling)), dims
+
+
+def test_random_blend_geometries(T):
+    """Seeded random plans, whole-latent and slab windows, bf16 and fp32:
+    wherever the streaming blend takes the call, its tables match an
+    independent reconstruction, the split is monotone, every chunk class
+    starts on a warp boundary, and in every unit of every CTA each (chunk
+    entry, band row) is taken by exactly one thread."""
+    rng = np.random.default_rng(2024)
+    streamed = 0
+    for _ in range(60):
+        p, dims = _random_plan(T, rng)
+        H = dims[1]
+        r0 = int(rng.integers(0, H))
+        r1 = int(rng.integers(r0 + 1, H + 1))
+        for rows in ((0, H), (r0, r1)):
+            esz = int(rng.choice([2, 4]))
+            B, C = 1, int(rng.integers(1, 5))
+            g, starts, buf, offs = T.launch_geometry(p, B, C, True, _dt(esz), _dt(esz), SMS, tables=True, rows=rows)
+            if not g["streaming"]:
+                continue
+            streamed += 1
+            check_split(starts, g["units"], g["grid"])
+            check_tables(p, g, buf, offs, B * C, esz, True, rows=rows)
+            chunks = np.frombuffer(buf, CHUNK, g["chunks_per_row"], 16 * offs["chunk"])
+            ncls = [int((chunks["cls"] == c).sum()) for c in range(4)]
+            G, step, first = g["row_groups"], g["row_step"], g["class_first"]
+            br = g["band_rows"]
+            assert all((G[c] > 0) == (ncls[c] > 0) and G[c] <= br for c in range(4))
+            assert all(first[c] % 32 == 0 for c in range(4))
+            assert max(first[c] + ncls[c] * G[c] for c in range(4)) <= g["threads"]
+            for k in range(3):   # a CTA's first units: the rotating starts cover every row once
+                for c in range(4):
+                    if G[c] == 0:
+                        continue
+                    taken = np.zeros(br, np.int64)
+                    for grp in range(G[c]):
+                        taken[(grp + k * step[c]) % G[c]::G[c]] += 1
+                    assert (taken == 1).all()
+    assert streamed >= 40   # most random plans stream
+
+
+def test_random_extract_geometries(T):
+    """Seeded random plans, bf16 and fp32: wherever the streaming extract
+    takes the call, its tables match an independent reconstruction and the
+    split is monotone."""
+    rng = np.random.default_rng(4096)
+    streamed = 0
+    for _ in range(60):
+        p, dims = _random_plan(T, rng)
+        esz = int(rng.choice([2, 4]))
+        B, C = 1, int(rng.integers(1, 5))
+        g, starts, buf, offs = T.launch_geometry(p, B, C, False, _dt(esz), _dt(esz), SMS, tables=True)
+        if not g["streaming"]:
+            continue
+        streamed += 1
+        check_split(starts, g["units"], g["grid"])
+        check_tables(p, g, buf, offs, B * C, esz, False)
+    assert streamed >= 30
+
+
 def test_launch_geometry_rows_checked(T):
     p = T.plan((4, 16, 16), ((1, 0), (2, 4), (2, 4)))
     for rows in ((0, 0), (5, 3), (-1, 4), (0, 17)):
