@@ -594,6 +594,42 @@ def test_random_extract_geometries(T):
     assert streamed >= 30
 
 
+def test_random_blend_replays(T):
+    """Small seeded random plans and slab windows, replayed in NumPy through
+    the streaming blend's staging and addressing: every output chunk of the
+    window written once and equal to the oracle's blend there."""
+    rng = np.random.default_rng(77)
+    replayed = 0
+    while replayed < 16:
+        dims = (int(rng.integers(1, 4)), int(rng.integers(8, 33)), 8 * int(rng.integers(2, 7)))
+        tiling = []
+        for d in dims:
+            n = int(rng.integers(1, min(4, d) + 1))
+            tiling.append((n, int(rng.integers(0, d // (n + 1) + 1)) if n > 1 else 0))
+        p, rp = _plan_pair(T, dims, tuple(tiling))
+        H = dims[1]
+        r0 = int(rng.integers(0, H))
+        rows = (r0, int(rng.integers(r0 + 1, H + 1))) if replayed % 2 else (0, H)
+        esz = int(rng.choice([2, 4]))
+        g, starts, buf, offs = T.launch_geometry(p, 1, 1, True, _dt(esz), _dt(esz), SMS, tables=True, rows=rows)
+        if not g["streaming"]:
+            continue
+        n = p.tiles_numel(1, 1)
+        vals = rng.standard_normal(n).astype(np.float32)
+        if esz == 2:
+            bits = ((vals.view(np.uint32) + 0x7FFF + ((vals.view(np.uint32) >> 16) & 1)) >> 16).astype(np.uint16)
+            tiles_bytes = bits.view(np.uint8).copy()
+            tv = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        else:
+            tiles_bytes = vals.view(np.uint8).copy()
+            tv = vals.astype(np.float64)
+        out, count = model_blend(p, g, starts, 1, 1, esz, esz, tiles_bytes, range(g["grid"]), rows=rows)
+        ref = O.blend(rp, O.unpack(rp, 1, 1, tv))[..., rows[0]:rows[1], :].ravel()
+        assert (count == 1).all(), (dims, tiling, rows)
+        assert np.allclose(out, ref, rtol=1e-6, atol=1e-6), (dims, tiling, rows)
+        replayed += 1
+
+
 def test_launch_geometry_rows_checked(T):
     p = T.plan((4, 16, 16), ((1, 0), (2, 4), (2, 4)))
     for rows in ((0, 0), (5, 3), (-1, 4), (0, 17)):
