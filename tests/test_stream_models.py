@@ -630,6 +630,32 @@ def test_random_blend_replays(T):
         replayed += 1
 
 
+def test_random_extract_replays(T):
+    """Small seeded random plans replayed in NumPy through the streaming
+    extract's staging and span writes: every tile element written once and
+    equal to the oracle's packed tiles (a bit copy)."""
+    rng = np.random.default_rng(99)
+    replayed = 0
+    while replayed < 16:
+        dims = (int(rng.integers(1, 4)), int(rng.integers(8, 33)), 8 * int(rng.integers(2, 7)))
+        tiling = []
+        for d in dims:
+            n = int(rng.integers(1, min(4, d) + 1))
+            tiling.append((n, int(rng.integers(0, d // (n + 1) + 1)) if n > 1 else 0))
+        p, rp = _plan_pair(T, dims, tuple(tiling))
+        esz = int(rng.choice([2, 4]))
+        g, starts, buf, offs = T.launch_geometry(p, 1, 1, False, _dt(esz), _dt(esz), SMS, tables=True)
+        if not g["streaming"]:
+            continue
+        lat_bytes, Xv = _latent(1, 1, dims, esz, seed=replayed)
+        out, count = model_extract(p, g, starts, 1, 1, esz, lat_bytes, range(g["grid"]))
+        ref = O.pack(O.extract(rp, Xv.astype(np.float64))).astype(np.float32)
+        ref_bytes = (ref.view(np.uint32) >> 16).astype(np.uint16).view(np.uint8) if esz == 2 else ref.view(np.uint8)
+        assert (count == 1).all(), (dims, tiling)
+        assert np.array_equal(out, ref_bytes), (dims, tiling)
+        replayed += 1
+
+
 def test_launch_geometry_rows_checked(T):
     p = T.plan((4, 16, 16), ((1, 0), (2, 4), (2, 4)))
     for rows in ((0, 0), (5, 3), (-1, 4), (0, 17)):
