@@ -262,8 +262,35 @@ def test_token_major_models(T, dims, tiling, B, C, esz, compat):
     assert np.max(np.abs(model_blend_tokens(p, B, C, esz, tok) - want)) < 1e-12
     for blend in (False, True):
         a = tm_args(p, B, C, esz, blend)
-        for G in (1, 7, 304, a["units"]):
+        for G in (1, 7, 304, 456, 760, a["units"]):   # 456 / 760: the 4K launches' grids (3 / 5 CTAs per SM)
             assert sorted(walked_units(p, a, min(G, a["units"]))) == list(range(a["units"]))
+
+
+def test_token_major_models_random(T):
+    """Seeded random plans and channel counts (C * element size a multiple
+    of 16 bytes): the token-major extract and blend models equal the oracle,
+    and the unit walk covers every unit once for several grids."""
+    rng = np.random.default_rng(5150)
+    for _ in range(12):
+        dims = (int(rng.integers(1, 5)), int(rng.integers(2, 20)), int(rng.integers(2, 40)))
+        tiling = []
+        for d in dims:
+            n = int(rng.integers(1, min(4, d) + 1))
+            tiling.append((n, int(rng.integers(0, d // (n + 1) + 1)) if n > 1 else 0))
+        esz = int(rng.choice([2, 4]))
+        C = (16 // esz) * int(rng.integers(1, 6))
+        B = int(rng.integers(1, 3))
+        p = T.plan(dims, tuple(tiling))
+        rp = O.make_plan(dims, tuple(tiling))
+        X = rng.standard_normal((B, C) + dims)
+        assert np.array_equal(model_extract_tokens(p, B, C, esz, X), O.pack(O.extract_tokens(rp, X))), (dims, tiling)
+        tok = rng.standard_normal(p.tiles_numel(B, C))
+        want = O.blend_tokens(rp, O.unpack_tokens(rp, B, C, tok))
+        assert np.max(np.abs(model_blend_tokens(p, B, C, esz, tok) - want)) < 1e-12, (dims, tiling)
+        for blend in (False, True):
+            a = tm_args(p, B, C, esz, blend)
+            for G in (1, 5, 456, 760):
+                assert sorted(walked_units(p, a, min(G, a["units"]))) == list(range(a["units"]))
 
 
 def test_token_major_swizzles_are_conflict_free_on_the_4k_layout():
