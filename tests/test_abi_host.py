@@ -248,3 +248,20 @@ def test_bench_algorithmic_bytes_of_the_4k_workload(T):
     assert ab["extract"] == ab["blend"] == 2 * (latent + tiles) == 99_557_376
     assert ab["total"] == 199_114_752
     assert round(ab["overlap_factor"], 5) == 1.97868
+
+
+def test_extract_and_tokens_workspace_size(T):
+    """tdp_extract_and_tokens_workspace (host only): per (tile, batch) pair,
+    6 int32 for each of its K1 token chunks -- K1 = the most of ceil(tile
+    tokens / 3072) and 256 CTAs // pairs -- then one int32 per batch, rounded
+    up to 16 bytes; 0 for no batch; a negative batch is rejected."""
+    wl = WORKLOADS["4k"]
+    p = T.plan(wl.dims, wl.tiling)   # 32 tiles of 9 x 23 x 39 = 8073 tokens: 3 chunks of 3072 at least
+    r16 = lambda n: -(-n // 16) * 16
+    for B in (1, 2, 3, 6, 9):
+        pairs = 32 * B
+        K1 = max(3, 256 // pairs)
+        assert T.extract_and_tokens_workspace(p, B) == r16((pairs * K1 * 6 + B) * 4), B
+    assert T.extract_and_tokens_workspace(p, 0) == 0
+    with pytest.raises(ValueError):
+        T.extract_and_tokens_workspace(p, -1)
